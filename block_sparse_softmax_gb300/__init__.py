@@ -1,0 +1,235 @@
+"""GB300-native exact, causal, block-sparse and chunk-merged softmax attention.
+
+Thin PyTorch-facing binding over the C ABI of ``libbss_attn.so`` (declared in
+``include/bss_attn.h``).  PyTorch only provides device memory and the current
+CUDA stream; every step of the computation runs in the library's CUDA kernels.
+There is no CPU fallback: calls fail loudly when the library is not built or
+the tensors are not on a CUDA device.
+
+Functions carry the C names: ``attn_fwd``, ``attn_fwd_partial``,
+``attn_merge_states``, ``attn_blocklist_normalize``, ``attn_fwd_blocksparse``,
+``attn_bwd``, ``attn_poll_status``, ``attn_watchdog_selftest``.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+import torch
+
+from . import _lib
+
+__all__ = [
+    "AttnError", "attn_fwd", "attn_fwd_partial", "attn_merge_states", "attn_blocklist_normalize",
+    "attn_fwd_blocksparse", "attn_bwd", "attn_bwd_workspace_bytes", "attn_poll_status",
+    "attn_watchdog_selftest", "attn_fwd_splitkv", "library",
+]
+
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED = 2
+ERR_BAD_BLOCKLIST = 3
+ERR_CUDA = 4
+ERR_TIMEOUT = 5
+ERR_WORKSPACE = 6
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = _lib.load()
+        name = lib.attn_status_string(status).decode()
+        detail = lib.attn_last_error_message().decode()
+        super().__init__(f"{where}: {name}" + (f" ({detail})" if detail else ""))
+        self.status = status
+        self.name = name
+
+
+def library():
+    """The loaded ctypes library (raises if it has not been built)."""
+    return _lib.load()
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise AttnError(status, where)
+
+
+def _stream_of(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape: Sequence[int]) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _scale(scale: Optional[float], d: int) -> float:
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool = False,
+             scale: Optional[float] = None, q_offset: int = 0, k_offset: int = 0,
+             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None
+             ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O [B,H,Lq,d] bf16 and LSE [B,H,Lq] fp32 of exact (optionally causal) attention."""
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    _need(q, "q", torch.bfloat16, (B, H, Lq, d))
+    _need(k, "k", torch.bfloat16, (B, H, Lk, d))
+    _need(v, "v", torch.bfloat16, (B, H, Lk, d))
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32) if lse is None else lse
+    _need(out, "out", torch.bfloat16, (B, H, Lq, d))
+    _need(lse, "lse", torch.float32, (B, H, Lq))
+    st = _lib.load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                              lse.data_ptr(), B, H, Lq, Lk, d, _scale(scale, d), int(causal),
+                              int(q_offset), int(k_offset), _stream_of(q))
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_partial(q, k, v, *, causal: bool = False, scale: Optional[float] = None,
+                     q_offset: int = 0, k_offset: int = 0, m=None, l=None, acc=None):
+    """Unnormalised state (m, l, acc) of the query rows over one KV chunk."""
+    B, H, Lq, d = q.shape
+    Lk = k.shape[2]
+    _need(q, "q", torch.bfloat16, (B, H, Lq, d))
+    _need(k, "k", torch.bfloat16, (B, H, Lk, d))
+    _need(v, "v", torch.bfloat16, (B, H, Lk, d))
+    dev = q.device
+    m = torch.empty((B, H, Lq), device=dev, dtype=torch.float32) if m is None else m
+    l = torch.empty((B, H, Lq), device=dev, dtype=torch.float32) if l is None else l
+    acc = torch.empty((B, H, Lq, d), device=dev, dtype=torch.float32) if acc is None else acc
+    _need(m, "m", torch.float32, (B, H, Lq))
+    _need(l, "l", torch.float32, (B, H, Lq))
+    _need(acc, "acc", torch.float32, (B, H, Lq, d))
+    st = _lib.load().attn_fwd_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), m.data_ptr(),
+                                      l.data_ptr(), acc.data_ptr(), B, H, Lq, Lk, d,
+                                      _scale(scale, d), int(causal), int(q_offset), int(k_offset),
+                                      _stream_of(q))
+    _check(st, "attn_fwd_partial")
+    return m, l, acc
+
+
+def attn_merge_states(m: torch.Tensor, l: torch.Tensor, acc: torch.Tensor, *, out=None, lse=None):
+    """Merge C chunk states (m, l [C,B,H,L]; acc [C,B,H,L,d]) into O (bf16) and LSE."""
+    C, B, H, L, d = acc.shape
+    _need(m, "m", torch.float32, (C, B, H, L))
+    _need(l, "l", torch.float32, (C, B, H, L))
+    _need(acc, "acc", torch.float32, (C, B, H, L, d))
+    out = torch.empty((B, H, L, d), device=acc.device, dtype=torch.bfloat16) if out is None else out
+    lse = torch.empty((B, H, L), device=acc.device, dtype=torch.float32) if lse is None else lse
+    _need(out, "out", torch.bfloat16, (B, H, L, d))
+    _need(lse, "lse", torch.float32, (B, H, L))
+    st = _lib.load().attn_merge_states(C, m.data_ptr(), l.data_ptr(), acc.data_ptr(),
+                                       out.data_ptr(), lse.data_ptr(), B, H, L, d,
+                                       _stream_of(acc))
+    _check(st, "attn_merge_states")
+    return out, lse
+
+
+def attn_fwd_splitkv(q, k, v, chunks: int, *, causal: bool = False, scale: Optional[float] = None):
+    """Exact attention computed as ``chunks`` separate KV chunks (attn_fwd_partial on each)
+    followed by attn_merge_states: the Ring-Attention combine on one GPU."""
+    B, H, L, d = q.shape
+    Lk = k.shape[2]
+    step = (Lk + chunks - 1) // chunks
+    bounds = [(s, min(Lk, s + step)) for s in range(0, Lk, step)]
+    C = len(bounds)
+    m = torch.empty((C, B, H, L), device=q.device, dtype=torch.float32)
+    l = torch.empty_like(m)
+    acc = torch.empty((C, B, H, L, d), device=q.device, dtype=torch.float32)
+    for c, (s, e) in enumerate(bounds):
+        kc = k[:, :, s:e].contiguous() if chunks > 1 else k
+        vc = v[:, :, s:e].contiguous() if chunks > 1 else v
+        attn_fwd_partial(q, kc, vc, causal=causal, scale=scale, k_offset=s, m=m[c], l=l[c],
+                         acc=acc[c])
+    return attn_merge_states(m, l, acc)
+
+
+def attn_blocklist_normalize(row_ptr, col_idx, n_kblk: int) -> Tuple[np.ndarray, np.ndarray]:
+    """Canonical CSR (ascending, duplicates removed), computed by the library on the host."""
+    rp = np.ascontiguousarray(np.asarray(row_ptr, dtype=np.int32))
+    ci = np.ascontiguousarray(np.asarray(col_idx, dtype=np.int32))
+    n_qblk = len(rp) - 1
+    out_rp = np.zeros(n_qblk + 1, dtype=np.int32)
+    out_ci = np.zeros(max(1, len(ci)), dtype=np.int32)
+    nnz = np.zeros(1, dtype=np.int32)
+    st = _lib.load().attn_blocklist_normalize(
+        rp.ctypes.data, ci.ctypes.data if len(ci) else None, n_qblk, n_kblk, out_rp.ctypes.data,
+        out_ci.ctypes.data, nnz.ctypes.data)
+    _check(st, "attn_blocklist_normalize")
+    return out_rp, out_ci[:int(nnz[0])].copy()
+
+
+def attn_fwd_blocksparse(q, k, v, row_ptr, col_idx, *, causal: bool = False,
+                         scale: Optional[float] = None, block: int = 128, out=None, lse=None):
+    """Attention over per-query-block CSR lists of key blocks (raw form accepted)."""
+    B, H, L, d = q.shape
+    _need(q, "q", torch.bfloat16, (B, H, L, d))
+    _need(k, "k", torch.bfloat16, (B, H, L, d))
+    _need(v, "v", torch.bfloat16, (B, H, L, d))
+    rp = torch.as_tensor(np.asarray(row_ptr, dtype=np.int32) if not torch.is_tensor(row_ptr)
+                         else row_ptr).to(device=q.device, dtype=torch.int32).contiguous()
+    ci = torch.as_tensor(np.asarray(col_idx, dtype=np.int32) if not torch.is_tensor(col_idx)
+                         else col_idx).to(device=q.device, dtype=torch.int32).contiguous()
+    if ci.numel() == 0:
+        ci = torch.zeros(1, device=q.device, dtype=torch.int32)
+        nnz = 0
+    else:
+        nnz = ci.numel()
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, L), device=q.device, dtype=torch.float32) if lse is None else lse
+    _need(out, "out", torch.bfloat16, (B, H, L, d))
+    _need(lse, "lse", torch.float32, (B, H, L))
+    st = _lib.load().attn_fwd_blocksparse(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, L, d,
+        _scale(scale, d), int(causal), int(block), rp.data_ptr(), ci.data_ptr(), rp.numel() - 1,
+        nnz, _stream_of(q))
+    _check(st, "attn_fwd_blocksparse")
+    return out, lse
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, L: int, d: int) -> int:
+    return int(_lib.load().attn_bwd_workspace_bytes(B, H, L, d))
+
+
+def attn_bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: Optional[float] = None,
+             workspace: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None, delta=None):
+    """Gradients (dq, dk, dv) bf16 and delta = rowsum(dO * O) fp32, by recomputation."""
+    B, H, L, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need(t, name, torch.bfloat16, (B, H, L, d))
+    _need(lse, "lse", torch.float32, (B, H, L))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    delta = torch.empty((B, H, L), device=q.device, dtype=torch.float32) if delta is None else delta
+    nbytes = attn_bwd_workspace_bytes(B, H, L, d)
+    if workspace is None:
+        workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
+    st = _lib.load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), delta.data_ptr(), workspace.data_ptr(),
+                              workspace.numel() * workspace.element_size(), B, H, L, d,
+                              _scale(scale, d), int(causal), _stream_of(q))
+    _check(st, "attn_bwd")
+    return dq, dk, dv, delta
+
+
+def attn_poll_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) the kernels' error word."""
+    stream = torch.cuda.current_stream(device).cuda_stream
+    return int(_lib.load().attn_poll_status(stream))
+
+
+def attn_watchdog_selftest(timeout_cycles: int = 1 << 20, device=None) -> None:
+    stream = torch.cuda.current_stream(device).cuda_stream
+    _check(_lib.load().attn_watchdog_selftest(int(timeout_cycles), stream), "attn_watchdog_selftest")

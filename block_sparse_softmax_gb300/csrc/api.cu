@@ -1,0 +1,330 @@
+// The C ABI of libbss_attn.so: argument validation, TMA descriptor encoding,
+// the device status word, and the host-side block-list normalisation.  Every
+// arithmetic step of the attention path runs in the kernels of fwd.cu,
+// merge.cu and bwd.cu; this file only checks, describes and launches.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+
+namespace bss {
+namespace {
+
+// First error recorded by any kernel of this library on a device (0 = none).
+__device__ int g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {nullptr};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+thread_local char g_last_error[256] = {0};
+
+void set_error(const char* where, cudaError_t e) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
+}
+
+// Device address of the status word for the current device.
+attn_status_t status_word(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error("cudaGetDevice", e);
+    return ATTN_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_status_word);
+    if (e != cudaSuccess) {
+      set_error("cudaGetSymbolAddress", e);
+      return ATTN_ERR_CUDA;
+    }
+    g_status_ptr[dev] = static_cast<int*>(ptr);
+  }
+  *out = g_status_ptr[dev];
+  return ATTN_OK;
+}
+
+attn_status_t get_encoder() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode) return ATTN_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) {
+    set_error("cudaGetDriverEntryPointByVersion(cuTensorMapEncodeTiled)", e);
+    return ATTN_ERR_CUDA;
+  }
+  g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  return ATTN_OK;
+}
+
+// [B, H, L, d] bf16 contiguous, viewed as a 4-D tensor (d, L, H, B) with boxes
+// of 64 d-elements (128 bytes, swizzled) by 128 rows.  Rows beyond L (the
+// ragged tail of a head) are zero-filled by the copy engine.
+attn_status_t make_map(CUtensorMap* map, const void* ptr, int B, int H, long long L, int d) {
+  if (L < 1) L = 1;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(L) * d * 2,
+                           static_cast<cuuint64_t>(H) * L * d * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled failed (%d)",
+             static_cast<int>(r));
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+attn_status_t check_common(int B, int H, long long Lq, long long Lk, int d, float scale) {
+  if (B < 1 || H < 1 || Lq < 0 || Lk < 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+  if ((Lq + 255) / 256 > 65535) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+attn_status_t cuda_status(const char* where, cudaError_t e) {
+  if (e == cudaSuccess) return ATTN_OK;
+  set_error(where, e);
+  return ATTN_ERR_CUDA;
+}
+
+attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int H, int Lq,
+                         int Lk, int d, float scale, int causal, long long q_offset,
+                         long long k_offset, bool sparse, bool partial, FwdParams& p,
+                         void* stream) {
+  attn_status_t s = check_common(B, H, Lq, Lk, d, scale);
+  if (s != ATTN_OK) return s;
+  if (q_offset < 0 || k_offset < 0) return ATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v)) return ATTN_ERR_INVALID_ARG;
+  if (Lq == 0) return ATTN_OK;
+  if ((s = get_encoder()) != ATTN_OK) return s;
+  if ((s = status_word(&p.err)) != ATTN_OK) return s;
+  CUtensorMap tq, tk, tv;
+  if ((s = make_map(&tq, q, B, H, Lq, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tk, k, B, H, Lk, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tv, v, B, H, Lk, d)) != ATTN_OK) return s;
+  p.B = B;
+  p.H = H;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.scale_log2 = scale * kLog2e;
+  p.q_offset = q_offset;
+  p.k_offset = k_offset;
+  p.causal = causal ? 1 : 0;
+  p.n_pairs = (Lq + 255) / 256;
+  return cuda_status("attn fwd launch",
+                     launch_fwd(d, causal != 0, sparse, partial, tq, tk, tv, p,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+}  // namespace bss
+
+using namespace bss;
+
+extern "C" {
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_BAD_BLOCKLIST: return "ATTN_ERR_BAD_BLOCKLIST";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+const char* attn_last_error_message(void) { return g_last_error; }
+
+int attn_version(void) { return 100; }
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                       int H, int Lq, int Lk, int d, float scale, int causal, int64_t q_offset,
+                       int64_t k_offset, void* stream) {
+  if (!o || !lse || !aligned16(o) || !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
+  FwdParams p{};
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  return fwd_common(q, k, v, B, H, Lq, Lk, d, scale, causal, q_offset, k_offset, false, false, p,
+                    stream);
+}
+
+attn_status_t attn_fwd_partial(const void* q, const void* k, const void* v, float* m, float* l,
+                               float* acc, int B, int H, int Lq, int Lk, int d, float scale,
+                               int causal, int64_t q_offset, int64_t k_offset, void* stream) {
+  if (!m || !l || !acc || !aligned4(m) || !aligned4(l) || !aligned16(acc))
+    return ATTN_ERR_INVALID_ARG;
+  FwdParams p{};
+  p.m_out = m;
+  p.l_out = l;
+  p.acc_out = acc;
+  return fwd_common(q, k, v, B, H, Lq, Lk, d, scale, causal, q_offset, k_offset, false, true, p,
+                    stream);
+}
+
+attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int B, int H, int L, int d, float scale, int causal,
+                                   int block, const int32_t* row_ptr, const int32_t* col_idx,
+                                   int n_qblk, int nnz, void* stream) {
+  if (!o || !lse || !aligned16(o) || !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
+  if (block != 128) return ATTN_ERR_UNSUPPORTED;
+  if (L < 0) return ATTN_ERR_INVALID_ARG;
+  const long long nblk = (static_cast<long long>(L) + 127) / 128;
+  if (nblk > kMaxKBlocks) return ATTN_ERR_UNSUPPORTED;
+  if (n_qblk != nblk || nnz < 0) return ATTN_ERR_BAD_BLOCKLIST;
+  if (!row_ptr || (nnz > 0 && !col_idx) || !aligned4(row_ptr) || !aligned4(col_idx))
+    return ATTN_ERR_INVALID_ARG;
+  FwdParams p{};
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.row_ptr = row_ptr;
+  p.col_idx = col_idx;
+  p.n_qblk = n_qblk;
+  p.nnz = nnz;
+  return fwd_common(q, k, v, B, H, L, L, d, scale, causal, 0, 0, true, false, p, stream);
+}
+
+attn_status_t attn_merge_states(int C, const float* m, const float* l, const float* acc, void* o,
+                                float* lse, int B, int H, int L, int d, void* stream) {
+  if (C < 1 || C > 64 || B < 1 || H < 1 || L < 0) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!m || !l || !acc || !o || !lse || !aligned16(acc) || !aligned16(o) || !aligned4(m) ||
+      !aligned4(l) || !aligned4(lse))
+    return ATTN_ERR_INVALID_ARG;
+  int* err = nullptr;
+  attn_status_t s = status_word(&err);
+  if (s != ATTN_OK) return s;
+  MergeParams p{};
+  p.C = C;
+  p.rows = static_cast<long long>(B) * H * L;
+  p.m = m;
+  p.l = l;
+  p.acc = acc;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  return cuda_status("attn_merge_states launch",
+                     launch_merge(d, p, err, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_blocklist_normalize(const int32_t* row_ptr, const int32_t* col_idx, int n_qblk,
+                                       int n_kblk, int32_t* out_row_ptr, int32_t* out_col_idx,
+                                       int32_t* out_nnz) {
+  if (n_qblk < 0 || n_kblk < 0 || !row_ptr || !out_row_ptr || !out_nnz)
+    return ATTN_ERR_INVALID_ARG;
+  if (row_ptr[0] != 0) return ATTN_ERR_BAD_BLOCKLIST;
+  for (int a = 0; a < n_qblk; ++a)
+    if (row_ptr[a + 1] < row_ptr[a]) return ATTN_ERR_BAD_BLOCKLIST;
+  const int32_t total = row_ptr[n_qblk];
+  if (total > 0 && (!col_idx || !out_col_idx)) return ATTN_ERR_INVALID_ARG;
+  for (int32_t e = 0; e < total; ++e)
+    if (col_idx[e] < 0 || col_idx[e] >= n_kblk) return ATTN_ERR_BAD_BLOCKLIST;
+  std::vector<int32_t> row;
+  int32_t w = 0;
+  out_row_ptr[0] = 0;
+  for (int a = 0; a < n_qblk; ++a) {
+    row.assign(col_idx + row_ptr[a], col_idx + row_ptr[a + 1]);
+    std::sort(row.begin(), row.end());
+    row.erase(std::unique(row.begin(), row.end()), row.end());
+    for (int32_t c : row) out_col_idx[w++] = c;
+    out_row_ptr[a + 1] = w;
+  }
+  *out_nnz = w;
+  return ATTN_OK;
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int L, int d) {
+  if (B < 1 || H < 1 || L < 0 || d < 1) return 0;
+  return static_cast<size_t>(B) * H * static_cast<size_t>(L) * d * sizeof(float);
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                       float* delta, void* workspace, size_t workspace_bytes, int B, int H, int L,
+                       int d, float scale, int causal, void* stream) {
+  attn_status_t s = check_common(B, H, L, L, d, scale);
+  if (s != ATTN_OK) return s;
+  const void* ptrs16[] = {q, k, v, o, dout, dq, dk, dv, workspace};
+  for (const void* ptr : ptrs16)
+    if (!ptr || !aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
+  if (!lse || !delta || !aligned4(lse) || !aligned4(delta)) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_workspace_bytes(B, H, L, d)) return ATTN_ERR_WORKSPACE;
+  if (L == 0) return ATTN_OK;
+  if ((s = get_encoder()) != ATTN_OK) return s;
+  BwdParams p{};
+  if ((s = status_word(&p.err)) != ATTN_OK) return s;
+  CUtensorMap tq, tk, tv, tdo;
+  if ((s = make_map(&tq, q, B, H, L, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tk, k, B, H, L, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tv, v, B, H, L, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tdo, dout, B, H, L, d)) != ATTN_OK) return s;
+  p.B = B;
+  p.H = H;
+  p.L = L;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal ? 1 : 0;
+  p.o = static_cast<const __nv_bfloat16*>(o);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.lse = lse;
+  p.delta = delta;
+  p.dq_acc = static_cast<float*>(workspace);
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  return cuda_status("attn_bwd launch",
+                     launch_bwd(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_poll_status(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_status("cudaStreamSynchronize", e);
+  int* word = nullptr;
+  attn_status_t s = status_word(&word);
+  if (s != ATTN_OK) return s;
+  int value = 0;
+  e = cudaMemcpy(&value, word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status("status read", e);
+  if (value != 0) {
+    const int zero = 0;
+    e = cudaMemcpy(word, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_status("status reset", e);
+  }
+  return static_cast<attn_status_t>(value);
+}
+
+attn_status_t attn_watchdog_selftest(unsigned long long timeout_cycles, void* stream) {
+  int* err = nullptr;
+  attn_status_t s = status_word(&err);
+  if (s != ATTN_OK) return s;
+  return cuda_status("watchdog selftest launch",
+                     launch_watchdog_selftest(timeout_cycles, err, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,103 @@
+// Shared definitions of the device code: launch parameters, status codes,
+// and the bounded-wait watchdog every spin in this library goes through.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/bss_attn.h"
+#include "ptx.cuh"
+
+namespace bss {
+
+constexpr int kTileM = 128;      // query rows per tile (TMEM lanes)
+constexpr int kTileN = 128;      // keys per KV tile
+constexpr int kMaxKBlocks = 4096;  // key blocks a block-sparse launch can address
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Watchdog: a wait that has not completed after this many SM cycles (about a
+// second at GB300 clocks) gives up, records ATTN_ERR_TIMEOUT and the kernel
+// unwinds.
+constexpr long long kWaitLimitCycles = 1ll << 31;
+
+// Record the first error code in the library's device status word.
+__device__ __forceinline__ void record_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// Bounded wait on phase `parity` of an mbarrier.  Returns false (and raises the
+// CTA's abort flag) when the limit expires or another role already aborted.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int* err, long long limit = kWaitLimitCycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      *abort_flag = 1;
+      record_error(err, ATTN_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+struct FwdParams {
+  int B, H, Lq, Lk;
+  float scale_log2;        // scale * log2(e): scores are exponentiated in base 2
+  long long q_offset, k_offset;
+  int causal;
+  // regular output
+  __nv_bfloat16* o;        // [B,H,Lq,d]
+  float* lse;              // [B,H,Lq]
+  // partial-state output
+  float* m_out;            // [B,H,Lq]
+  float* l_out;            // [B,H,Lq]
+  float* acc_out;          // [B,H,Lq,d]
+  // block-sparse list (device CSR over 128-blocks)
+  const int* row_ptr;
+  const int* col_idx;
+  int n_qblk, nnz;
+  int n_pairs;             // CTAs along x: ceil(Lq / 256)
+  int* err;
+};
+
+struct MergeParams {
+  int C;
+  long long rows;          // B*H*L
+  const float* m;          // [C, rows]
+  const float* l;          // [C, rows]
+  const float* acc;        // [C, rows, d]
+  __nv_bfloat16* o;        // [rows, d]
+  float* lse;              // [rows]
+};
+
+struct BwdParams {
+  int B, H, L;
+  float scale, scale_log2;
+  int causal;
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dout;
+  const float* lse;
+  float* delta;
+  float* dq_acc;           // fp32 [B,H,L,d] workspace
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int* err;
+};
+
+}  // namespace bss
+
+// Host-side launchers (defined in the .cu files, called by api.cpp).
+namespace bss {
+cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUtensorMap& tq,
+                       const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                       cudaStream_t st);
+cudaError_t launch_merge(int d, const MergeParams& p, int* err, cudaStream_t st);
+cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, cudaStream_t st);
+cudaError_t launch_watchdog_selftest(unsigned long long cycles, int* err, cudaStream_t st);
+}  // namespace bss

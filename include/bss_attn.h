@@ -1,0 +1,177 @@
+/*
+ * bss_attn.h - C ABI of libbss_attn.so: exact, causal, block-sparse and
+ * chunk-merged softmax attention on GB300 (sm_103a), forward and backward.
+ *
+ * Operation.  For every batch b and head h, with Q [Lq, d], K and V [Lk, d]:
+ *     S = scale * Q K^T,   O = softmax_row(S over the allowed keys) V,
+ *     LSE_i = ln sum_{j allowed} exp(S_ij)
+ * computed tile by tile with the online-softmax state (m, l, A) so that S and
+ * P never reach device memory ("Exact Blocks, Rings, and Sparsity", sections 1
+ * and 2; "FlashAttention: Fast and Memory Efficient Exact Attention with IO
+ * Awareness", section 5.2 and Theorem 1).
+ *
+ * Conventions shared by every entry point.
+ *   - Tensors are contiguous row-major [B, H, L, d] (d fastest), bf16 unless
+ *     stated; LSE, partial states and delta are fp32.  d must be 64 or 128.
+ *   - All pointers to tensors are DEVICE pointers, 16-byte aligned, owned by
+ *     the caller.  The library never allocates, frees or synchronises device
+ *     memory (attn_poll_status excepted) and keeps no pointer after a call
+ *     returns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Work is only
+ *     enqueued; results are ready when the stream reaches it.
+ *   - Masks follow the pages' semantics: a masked pair contributes exactly
+ *     zero; a query row with no allowed key gets O = 0 and LSE = -inf (and
+ *     zero gradient); causal visibility is key + k_offset <= query + q_offset.
+ *   - LSE is the natural log of the normaliser of the scaled logits.
+ *   - Every call returns an attn_status_t; nothing is thrown or aborted across
+ *     the ABI.  Errors found inside a kernel (a block index out of range, a
+ *     watchdog timeout) are recorded in a per-library device word read by
+ *     attn_poll_status.
+ */
+#ifndef BSS_ATTN_H_
+#define BSS_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, non-finite or non-positive scale */
+  ATTN_ERR_UNSUPPORTED = 2,   /* d not in {64,128}, block != 128, size beyond a stated limit */
+  ATTN_ERR_BAD_BLOCKLIST = 3, /* malformed CSR: row_ptr not monotone, index out of range, nnz mismatch */
+  ATTN_ERR_CUDA = 4,          /* a CUDA runtime/driver call or kernel launch failed */
+  ATTN_ERR_TIMEOUT = 5,       /* a kernel's bounded wait expired (watchdog); the kernel returned early */
+  ATTN_ERR_WORKSPACE = 6      /* workspace missing or smaller than attn_bwd_workspace_bytes() */
+} attn_status_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* attn_status_string(int status);
+
+/* Library ABI version (major*100 + minor). */
+int attn_version(void);
+
+/* Text of the last CUDA/driver failure seen by this thread (for ATTN_ERR_CUDA
+ * diagnostics); empty string if none.  Static per-thread storage. */
+const char* attn_last_error_message(void);
+
+/*
+ * attn_fwd - exact attention forward, dense or causal.
+ * "Exact Blocks, Rings, and Sparsity", section 2 ('What the forward kernel
+ * keeps on chip'); causal element mask on the diagonal tiles only, tiles wholly
+ * in the future skipped (section 4, last paragraph).
+ *   q [B,H,Lq,d], k/v [B,H,Lk,d] bf16 in; o [B,H,Lq,d] bf16 out; lse [B,H,Lq] fp32 out.
+ *   causal != 0 applies key + k_offset <= query + q_offset (offsets >= 0).
+ *   scale must be finite and > 0 (the pages use d^-1/2).
+ */
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int H, int Lq, int Lk, int d, float scale, int causal,
+                       int64_t q_offset, int64_t k_offset, void* stream);
+
+/*
+ * attn_fwd_partial - unnormalised online-softmax state over one KV chunk.
+ * "Exact Blocks, Rings, and Sparsity", section 2 (state m, l, A and its merge
+ * invariant) and section 4 (one Ring-Attention step on a KV block).
+ *   Writes, per query row, m = max allowed scaled logit (natural-log units),
+ *   l = sum exp(s - m), acc = sum exp(s - m) V over the keys of this chunk.
+ *   Rows with no allowed key get the empty state m = -inf, l = 0, acc = 0.
+ *   m, l: fp32 [B,H,Lq]; acc: fp32 [B,H,Lq,d].  Other arguments as attn_fwd;
+ *   k_offset is the absolute position of the chunk's first key.
+ */
+attn_status_t attn_fwd_partial(const void* q, const void* k, const void* v,
+                               float* m, float* l, float* acc,
+                               int B, int H, int Lq, int Lk, int d, float scale, int causal,
+                               int64_t q_offset, int64_t k_offset, void* stream);
+
+/*
+ * attn_merge_states - combine C partial states over disjoint key sets.
+ * "Exact Blocks, Rings, and Sparsity", section 4 (the associative merge of two
+ * ring steps); "FlashAttention ..." section 5.1 (block-wise m and l).
+ *   m, l: fp32 [C,B,H,L]; acc: fp32 [C,B,H,L,d] (as written by attn_fwd_partial,
+ *   chunk-major).  Out: o bf16 [B,H,L,d] = A* / l*, lse fp32 [B,H,L] = m* + ln l*.
+ *   Empty states (m = -inf) are skipped without reading their acc rows; a row
+ *   whose states are all empty gets O = 0, LSE = -inf.  1 <= C <= 64.
+ */
+attn_status_t attn_merge_states(int C, const float* m, const float* l, const float* acc,
+                                void* o, float* lse, int B, int H, int L, int d, void* stream);
+
+/*
+ * attn_blocklist_normalize - HOST function: canonical form of a CSR block list.
+ * Block-sparse attention patterns page, 'Count active blocks and acknowledge the
+ * changed operator' (duplicate entries never count twice; order carries no meaning).
+ *   In: row_ptr[n_qblk+1], col_idx[row_ptr[n_qblk]] (host memory, any order,
+ *   duplicates allowed).  Out: out_row_ptr[n_qblk+1] and out_col_idx (capacity
+ *   >= row_ptr[n_qblk]) hold each row's set of key blocks in ascending order;
+ *   *out_nnz = total unique entries.  Returns ATTN_ERR_BAD_BLOCKLIST if row_ptr
+ *   does not start at 0, decreases, or an index is outside [0, n_kblk).
+ */
+attn_status_t attn_blocklist_normalize(const int32_t* row_ptr, const int32_t* col_idx,
+                                       int n_qblk, int n_kblk, int32_t* out_row_ptr,
+                                       int32_t* out_col_idx, int32_t* out_nnz);
+
+/*
+ * attn_fwd_blocksparse - attention over a per-query-block list of key blocks,
+ * renormalised over the sparse domain.
+ * "Exact Blocks, Rings, and Sparsity", section 5 ('Why the sparse unit is
+ * usually a block': the outer loop visits only the listed tiles) and section 6
+ * (drop-and-renormalise); block-sparse attention patterns page (triangular
+ * element mask inside diagonal blocks, partial blocks, duplicates, empty rows).
+ *   q/k/v/o/lse as attn_fwd with Lq = Lk = L.  block must be 128.
+ *   row_ptr [n_qblk+1], col_idx [nnz]: DEVICE int32 CSR, n_qblk = ceil(L/128),
+ *   raw form accepted (any order, duplicates counted once).  A listed block
+ *   wholly in the causal future contributes nothing.  An entry outside
+ *   [0, ceil(L/128)) is ignored and reported as ATTN_ERR_BAD_BLOCKLIST by
+ *   attn_poll_status; so is a row whose row_ptr range is not inside [0, nnz]
+ *   (that row is then treated as empty).  A query block with an empty list
+ *   gets O = 0, LSE = -inf.  L <= 4096*128 (at most 4096 key blocks).
+ */
+attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o,
+                                   float* lse, int B, int H, int L, int d, float scale,
+                                   int causal, int block, const int32_t* row_ptr,
+                                   const int32_t* col_idx, int n_qblk, int nnz, void* stream);
+
+/*
+ * attn_bwd_workspace_bytes - size of the caller-provided workspace of attn_bwd
+ * (an fp32 dQ accumulator of B*H*L*d elements).
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int L, int d);
+
+/*
+ * attn_bwd - gradients by recomputation from the saved LSE.
+ * "Exact Blocks, Rings, and Sparsity", section 3 (D_i = dO_i . O_i;
+ * P = exp(S - LSE); dS = P o (dP - D); dQ = scale dS K; dK = scale dS^T Q;
+ * dV = P^T dO; KV-owned traversal with accumulated dQ, 'The ownership
+ * conflict between dQ and dK, dV'); "FlashAttention ..." section 5.3.
+ *   q,k,v,o,dout bf16 [B,H,L,d]; lse fp32 [B,H,L] from attn_fwd with the same
+ *   scale and mask.  Out: dq, dk, dv bf16 [B,H,L,d]; delta fp32 [B,H,L].
+ *   workspace: device, >= attn_bwd_workspace_bytes(B,H,L,d) bytes, contents
+ *   on entry irrelevant (it is cleared on the stream).
+ */
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                       const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                       float* delta, void* workspace, size_t workspace_bytes,
+                       int B, int H, int L, int d, float scale, int causal, void* stream);
+
+/*
+ * attn_poll_status - synchronise `stream`, then return and clear the first
+ * error any kernel of this library recorded on the current device since the
+ * last poll (ATTN_OK if none).
+ */
+attn_status_t attn_poll_status(void* stream);
+
+/*
+ * attn_watchdog_selftest - launch one block that waits on a barrier nobody
+ * arrives at, with a limit of `timeout_cycles` SM clock cycles; the wait gives
+ * up, records ATTN_ERR_TIMEOUT and the block returns.  Lets a test observe the
+ * watchdog path without hanging or faulting the GPU.  Returns the launch status.
+ */
+attn_status_t attn_watchdog_selftest(unsigned long long timeout_cycles, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSS_ATTN_H_ */

@@ -1,0 +1,136 @@
+"""The C ABI without a GPU: the library loads, exports every function the header
+declares, normalises block lists exactly as the oracle's set semantics say,
+and rejects bad arguments with status codes before touching the device."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from workloads import local_global_random_blocklist, random_blocklist
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_softmax_gb300 import build
+    build.build()
+    from block_sparse_softmax_gb300 import _lib
+    return _lib.load()
+
+
+def _declared_functions():
+    names = []
+    for f in os.listdir(HEADER_DIR):
+        if f.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^[A-Za-z_][\w \t\*]*?\b(attn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for required in ("attn_fwd", "attn_fwd_partial", "attn_merge_states", "attn_fwd_blocksparse",
+                     "attn_blocklist_normalize", "attn_bwd", "attn_bwd_workspace_bytes",
+                     "attn_poll_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from block_sparse_softmax_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(\w+)$", out, flags=re.M))
+    for name in _declared_functions():
+        assert name in exported, name
+        assert getattr(lib, name) is not None
+    # the binding wraps exactly the declared set
+    from block_sparse_softmax_gb300 import _lib
+    assert sorted(_lib.exported_names()) == _declared_functions()
+
+
+def test_status_strings_and_version(lib):
+    assert lib.attn_status_string(0) == b"ATTN_OK"
+    assert lib.attn_status_string(3) == b"ATTN_ERR_BAD_BLOCKLIST"
+    assert lib.attn_status_string(99) == b"ATTN_ERR_UNKNOWN"
+    assert lib.attn_version() >= 100
+
+
+def _normalize(lib, rp, ci, n_kblk):
+    rp = np.ascontiguousarray(rp, dtype=np.int32)
+    ci = np.ascontiguousarray(ci, dtype=np.int32)
+    out_rp = np.zeros_like(rp)
+    out_ci = np.zeros(max(1, len(ci)), dtype=np.int32)
+    nnz = np.zeros(1, dtype=np.int32)
+    st = lib.attn_blocklist_normalize(rp.ctypes.data, ci.ctypes.data if len(ci) else None,
+                                      len(rp) - 1, n_kblk, out_rp.ctypes.data, out_ci.ctypes.data,
+                                      nnz.ctypes.data)
+    return st, out_rp, out_ci[:nnz[0]]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_blocklist_normalize_matches_oracle_exactly(lib, seed):
+    if seed == 0:
+        rp, ci = local_global_random_blocklist(128, seed=2)
+        nk = 128
+    else:
+        nk = 3 + 7 * seed
+        rp, ci = random_blocklist(nk + seed, nk, seed=seed, max_per_row=9)
+    st, out_rp, out_ci = _normalize(lib, rp, ci, nk)
+    assert st == 0
+    ref_rp, ref_ci = oracle.blocklist_normalize(rp, ci, nk)
+    assert np.array_equal(out_rp, ref_rp)
+    assert np.array_equal(out_ci, ref_ci)
+    # the realised block mask equals the oracle's set, row by row
+    sets = oracle.blocklist_sets(rp, ci, nk)
+    for a, s in enumerate(sets):
+        assert set(out_ci[out_rp[a]:out_rp[a + 1]].tolist()) == s
+
+
+@pytest.mark.parametrize("rp,ci", [
+    ([0, 2, 1], [0, 1]),
+    ([0, 1], [4]),
+    ([0, 1], [-1]),
+    ([1, 2], [0, 1]),
+])
+def test_blocklist_normalize_rejects_malformed(lib, rp, ci):
+    st, _, _ = _normalize(lib, np.array(rp), np.array(ci), 4)
+    assert st == 3
+
+
+def test_argument_errors_return_codes_before_any_device_work(lib):
+    P = ctypes.c_void_p(16 * 1000)       # aligned dummy addresses, never dereferenced
+    bad = ctypes.c_void_p(16 * 1000 + 2)
+    args = lambda q=P, d=64, scale=0.125, B=1: (q, P, P, P, P, B, 1, 256, 256, d, scale, 0, 0, 0, None)
+    assert lib.attn_fwd(*args(d=96)) == 2                 # unsupported head dim
+    assert lib.attn_fwd(*args(q=None)) == 1               # null pointer
+    assert lib.attn_fwd(*args(q=bad)) == 1                # misaligned pointer
+    assert lib.attn_fwd(*args(scale=float("nan"))) == 1   # non-finite scale
+    assert lib.attn_fwd(*args(scale=-1.0)) == 1           # non-positive scale
+    assert lib.attn_fwd(*args(B=0)) == 1                  # empty batch
+    # block size other than 128, CSR row count mismatch, too many key blocks
+    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 256, 64, 0.125, 1, 64, P, P, 2, 4, None) == 2
+    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 256, 64, 0.125, 1, 128, P, P, 3, 4, None) == 3
+    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 4097 * 128, 64, 0.125, 1, 128, P, P,
+                                    4097, 4, None) == 2
+    # merge: chunk count out of range
+    assert lib.attn_merge_states(0, P, P, P, P, P, 1, 1, 16, 64, None) == 1
+    assert lib.attn_merge_states(65, P, P, P, P, P, 1, 1, 16, 64, None) == 1
+    # backward: workspace too small
+    ws = lib.attn_bwd_workspace_bytes(2, 3, 100, 64)
+    assert ws == 2 * 3 * 100 * 64 * 4
+    assert lib.attn_bwd(P, P, P, P, P, P, P, P, P, P, P, ws - 4, 2, 3, 100, 64, 0.125, 1, None) == 6
+
+
+def test_binding_fails_loudly_on_cpu_tensors():
+    import torch
+    import block_sparse_softmax_gb300 as bss
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        bss.attn_fwd(q, q, q)

@@ -1,0 +1,123 @@
+"""Partial states over KV chunks and their merge on the GPU (the Ring-Attention
+combine on one device): the state itself against the oracle, chunked == unchunked
+in any order, empty states, and the long B=1 H=8 L=131072 workload."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.parity import TOL_LSE, TOL_O, compare_forward, oracle_forward, to_cuda
+from workloads import SPLITKV_128K, Workload, chunk_bounds, make_inputs, sample_rows, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bss():
+    import block_sparse_softmax_gb300 as m
+    m.library()
+    return m
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("s,e", [(0, 300), (250, 700), (640, 1000)])
+def test_partial_state_matches_oracle(bss, d, s, e):
+    L = 1000
+    w = Workload("p", 1, 2, L, d, True, seed=s + e)
+    cpu = make_inputs(w)
+    q = cpu["q"].cuda()
+    kc = cpu["k"][:, :, s:e].contiguous().cuda()
+    vc = cpu["v"][:, :, s:e].contiguous().cuda()
+    m, l, acc = bss.attn_fwd_partial(q, kc, vc, causal=True, scale=w.scale, k_offset=s)
+    torch.cuda.synchronize()
+    qn, kn, vn = (to_f64(cpu[n]) for n in ("q", "k", "v"))
+    for h in range(2):
+        M = oracle.allowed_rows(np.arange(L), e - s, causal=True, k_offset=s)
+        mr, lr, Ar = oracle.partial_state(qn[0, h], kn[0, h, s:e], vn[0, h, s:e], w.scale, M)
+        mg = m[0, h].double().cpu().numpy()
+        lg = l[0, h].double().cpu().numpy()
+        Ag = acc[0, h].double().cpu().numpy()
+        empty = np.isneginf(mr)
+        assert np.array_equal(np.isneginf(mg), empty)
+        assert np.all(lg[empty] == 0) and np.all(Ag[empty] == 0)
+        f = ~empty
+        # m is the exact maximum; l and A share it, so A/l and m + ln l are the
+        # chunk's O and LSE
+        assert np.abs(mg[f] - mr[f]).max() <= TOL_LSE
+        assert np.abs((Ag[f] / lg[f, None]) - (Ar[f] / lr[f, None])).max() <= TOL_O
+        assert np.abs((mg[f] + np.log(lg[f])) - (mr[f] + np.log(lr[f]))).max() <= TOL_LSE
+        assert lg[f].min() >= 1.0 - 1e-3          # the max element contributes e^0 = 1
+
+
+@pytest.mark.parametrize("chunks", [2, 3, 8])
+@pytest.mark.parametrize("causal", [True, False])
+def test_split_kv_merge_equals_oracle_and_unsplit(bss, chunks, causal):
+    L, d = 1100, 128
+    w = Workload("m", 1, 3, L, d, causal, seed=chunks)
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    o, lse = bss.attn_fwd_splitkv(inp["q"], inp["k"], inp["v"], chunks, causal=causal,
+                                  scale=w.scale)
+    o1, l1 = bss.attn_fwd(inp["q"], inp["k"], inp["v"], causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    O_ref, l_ref = oracle_forward(cpu, w.scale, causal=causal)
+    compare_forward(o, lse, O_ref, l_ref, f"{chunks} chunks")
+    assert (o.float() - o1.float()).abs().max().item() <= TOL_O
+    assert (lse - l1).abs().max().item() <= TOL_LSE
+
+
+def test_merge_order_does_not_matter(bss):
+    L, d, C = 700, 64, 5
+    w = Workload("o", 2, 2, L, d, True, seed=31)
+    inp = to_cuda(make_inputs(w))
+    bounds = chunk_bounds(L, C)
+    states = [bss.attn_fwd_partial(inp["q"], inp["k"][:, :, s:e].contiguous(),
+                                   inp["v"][:, :, s:e].contiguous(), causal=True, k_offset=s)
+              for s, e in bounds]
+    outs = []
+    for perm in ([0, 1, 2, 3, 4], [4, 2, 0, 3, 1], [3, 4, 1, 0, 2]):
+        m = torch.stack([states[i][0] for i in perm])
+        l = torch.stack([states[i][1] for i in perm])
+        a = torch.stack([states[i][2] for i in perm])
+        outs.append(bss.attn_merge_states(m, l, a))
+    torch.cuda.synchronize()
+    for o, lse in outs[1:]:
+        assert (o.float() - outs[0][0].float()).abs().max().item() <= 1e-2
+        assert (lse - outs[0][1]).abs().max().item() <= 1e-5
+
+
+def test_merge_of_empty_states(bss):
+    C, B, H, L, d = 3, 1, 2, 130, 64
+    m = torch.full((C, B, H, L), float("-inf"), device="cuda")
+    l = torch.zeros_like(m)
+    acc = torch.full((C, B, H, L, d), float("nan"), device="cuda")   # never read
+    m[1, 0, 1, 5] = 2.0
+    l[1, 0, 1, 5] = 4.0
+    acc[1, 0, 1, 5] = 8.0
+    o, lse = bss.attn_merge_states(m, l, acc)
+    torch.cuda.synchronize()
+    assert torch.isneginf(lse).sum().item() == B * H * L - 1
+    assert torch.all(o[0, 0] == 0)
+    assert torch.allclose(o[0, 1, 5].float(), torch.full((d,), 2.0, device="cuda"))
+    assert abs(lse[0, 1, 5].item() - (2.0 + np.log(4.0))) < 1e-5
+
+
+def test_long_context_split_kv_full_size(bss):
+    """B=1 H=8 L=131072 d=128 causal, values x0.5, 8 contiguous KV chunks each
+    attended separately then merged; compared with the unsplit kernel on every
+    row and with the oracle on sampled rows."""
+    w = SPLITKV_128K
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    o, lse = bss.attn_fwd_splitkv(inp["q"], inp["k"], inp["v"], w.chunks, causal=True,
+                                  scale=w.scale)
+    o1, l1 = bss.attn_fwd(inp["q"], inp["k"], inp["v"], causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    assert (o.float() - o1.float()).abs().max().item() <= TOL_O
+    assert (lse - l1).abs().max().item() <= TOL_LSE
+    rows = sample_rows(w.L, w.chunks, 96, seed=w.seed)
+    heads = [(0, 0), (0, 5)]
+    O_ref, l_ref = oracle_forward(cpu, w.scale, rows=rows, heads=heads, causal=True)
+    for n_, (b, h) in enumerate(heads):
+        compare_forward(o[b, h, rows], lse[b, h, rows], O_ref[n_], l_ref[n_], f"head {(b, h)}")

@@ -1,0 +1,150 @@
+"""Block-sparse forward parity on the GPU: the local + global + random pattern
+with duplicates, an empty row and a partial last block; unstructured lists;
+set semantics (order and duplicates never matter); equivalence with the dense
+kernels when every block is listed; bad entries reported."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests.parity import compare_forward, oracle_forward, tile_edge_rows, to_cuda
+from workloads import (SPARSE_16K, Workload, local_global_random_blocklist, make_inputs,
+                       random_blocklist)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bss():
+    import block_sparse_softmax_gb300 as m
+    m.library()
+    return m
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [True, False])
+def test_local_global_random_pattern_reduced(bss, d, causal):
+    L = 2048 - 64                                   # 16 blocks, the last one half full
+    n = (L + 127) // 128
+    rp, ci = local_global_random_blocklist(n, seed=2)
+    w = Workload("s", 1, 2, L, d, causal, seed=2)
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    o = torch.full_like(inp["q"], float("nan"))
+    lse = torch.full((1, 2, L), float("nan"), device="cuda")
+    bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=causal, scale=w.scale,
+                             out=o, lse=lse)
+    torch.cuda.synchronize()
+    O_ref, l_ref = oracle_forward(cpu, w.scale, causal=causal, block=128, row_ptr=rp, col_idx=ci)
+    compare_forward(o, lse, O_ref, l_ref, f"pattern d={d} causal={causal}")
+    assert torch.all(torch.isneginf(lse[:, :, (n // 2) * 128:(n // 2 + 1) * 128]))
+    assert bss.attn_poll_status() == 0
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+@pytest.mark.parametrize("d", [64, 128])
+def test_unstructured_lists(bss, seed, d):
+    L = 1000
+    n = (L + 127) // 128
+    rp, ci = random_blocklist(n, n, seed=seed, max_per_row=5)
+    causal = seed % 2 == 1
+    w = Workload("u", 2, 1, L, d, causal, seed=40 + seed)
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    o, lse = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=causal,
+                                      scale=w.scale)
+    torch.cuda.synchronize()
+    O_ref, l_ref = oracle_forward(cpu, w.scale, causal=causal, block=128, row_ptr=rp, col_idx=ci)
+    compare_forward(o, lse, O_ref, l_ref, f"random list seed={seed}")
+
+
+def test_order_and_duplicates_are_bit_identical(bss):
+    L, d = 1500, 128
+    n = (L + 127) // 128
+    rp, ci = random_blocklist(n, n, seed=9, max_per_row=7, p_empty=0.1)
+    cp, cc = bss.attn_blocklist_normalize(rp, ci, n)
+    rng = np.random.default_rng(0)
+    perm_ci = np.concatenate([rng.permutation(np.repeat(cc[cp[a]:cp[a + 1]], 3))
+                              for a in range(n)]).astype(np.int32)
+    perm_rp = (cp * 3).astype(np.int32)
+    w = Workload("p", 1, 2, L, d, True, seed=5)
+    inp = to_cuda(make_inputs(w))
+    a = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=True)
+    b = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], cp, cc, causal=True)
+    c = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], perm_rp, perm_ci, causal=True)
+    torch.cuda.synchronize()
+    for x in (b, c):
+        assert torch.equal(a[0], x[0]) and torch.equal(a[1], x[1])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_all_blocks_listed_equals_dense_kernel(bss, causal):
+    L, d = 777, 64
+    n = (L + 127) // 128
+    if causal:
+        rows = [list(range(a + 1)) for a in range(n)]
+    else:
+        rows = [list(range(n))[::-1] for _ in range(n)]
+    rp = np.cumsum([0] + [len(r) for r in rows]).astype(np.int32)
+    ci = np.array([c for r in rows for c in r], np.int32)
+    inp = to_cuda(make_inputs(Workload("a", 2, 2, L, d, causal, seed=77)))
+    o_s, l_s = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=causal)
+    o_d, l_d = bss.attn_fwd(inp["q"], inp["k"], inp["v"], causal=causal)
+    torch.cuda.synchronize()
+    assert torch.equal(o_s, o_d) and torch.equal(l_s, l_d)
+
+
+def test_future_blocks_contribute_nothing(bss):
+    L, d = 1024, 64
+    n = L // 128
+    base = [[a, 0] for a in range(n)]
+    extra = [[a, 0, min(n - 1, a + 2), n - 1] for a in range(n)]     # future blocks added
+    mk = lambda rows: (np.cumsum([0] + [len(r) for r in rows]).astype(np.int32),
+                       np.array([c for r in rows for c in r], np.int32))
+    inp = to_cuda(make_inputs(Workload("f", 1, 1, L, d, True, seed=3)))
+    a = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], *mk(base), causal=True)
+    b = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], *mk(extra), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_bad_entries_are_ignored_and_reported(bss):
+    L, d = 512, 64
+    rp = np.array([0, 2, 4, 6, 9], np.int32)
+    good = np.array([0, 0, 1, 0, 2, 1, 3, 0, 1], np.int32)
+    bad = good.copy()
+    bad[3] = 57          # out of range: ignored
+    bad[8] = -2          # negative: ignored
+    inp = to_cuda(make_inputs(Workload("b", 1, 1, L, d, True, seed=8)))
+    assert bss.attn_poll_status() == 0
+    out = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, bad, causal=True)
+    assert bss.attn_poll_status() == bss.ERR_BAD_BLOCKLIST
+    rows_wo = [[0, 0], [1], [2, 1], [3, 0]]
+    rp2 = np.cumsum([0] + [len(r) for r in rows_wo]).astype(np.int32)
+    ci2 = np.array([c for r in rows_wo for c in r], np.int32)
+    exp = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp2, ci2, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], exp[0]) and torch.equal(out[1], exp[1])
+
+
+def test_blocksparse_16k_full_size_sampled(bss):
+    """B=2 H=16 L'=16320 d=128 with the generated list (empty row 64, partial
+    last block), the benchmark's launch configuration; sampled heads and rows."""
+    w = SPARSE_16K
+    rp, ci = local_global_random_blocklist(w.n_blocks, seed=w.seed)
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    o, lse = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=True,
+                                      scale=w.scale)
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    assert torch.all(torch.isneginf(lse[:, :, 64 * 128:65 * 128]))
+    assert torch.all(o[:, :, 64 * 128:65 * 128] == 0)
+    rows = tile_edge_rows(w.L, n_random=48, seed=2)[::2]
+    rows = np.unique(np.concatenate([rows, np.arange(64 * 128 - 2, 65 * 128 + 2)]))
+    heads = [(0, 3), (1, 12)]
+    O_ref, l_ref = oracle_forward(cpu, w.scale, rows=rows, heads=heads, causal=True, block=128,
+                                  row_ptr=rp, col_idx=ci)
+    for n_, (b, h) in enumerate(heads):
+        compare_forward(o[b, h, rows], lse[b, h, rows], O_ref[n_], l_ref[n_], f"head {(b, h)}")
+    assert torch.isfinite(o).all()

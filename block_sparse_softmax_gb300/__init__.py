@@ -22,7 +22,8 @@ from . import _lib
 
 __all__ = [
     "AttnError", "attn_fwd", "attn_fwd_partial", "attn_merge_states", "attn_blocklist_normalize",
-    "attn_fwd_blocksparse", "attn_bwd", "attn_bwd_workspace_bytes", "attn_poll_status",
+    "attn_fwd_blocksparse", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_noalloc",
+    "attn_poll_status",
     "attn_watchdog_selftest", "attn_fwd_splitkv", "library",
 ]
 
@@ -221,6 +222,32 @@ def attn_bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: Optional[flo
                               workspace.numel() * workspace.element_size(), B, H, L, d,
                               _scale(scale, d), int(causal), _stream_of(q))
     _check(st, "attn_bwd")
+    return dq, dk, dv, delta
+
+
+NOALLOC_SCRATCH_FLOATS = 8 << 20
+
+
+def attn_bwd_noalloc(q, k, v, o, lse, dout, *, causal: bool = False,
+                     scale: Optional[float] = None, dq=None, dk=None, dv=None, delta=None):
+    """attn_bwd without a workspace, for callers that cannot allocate device memory:
+    the library keeps the fp32 dQ accumulator in a static 32 MiB device array
+    (B*H*L*d <= 8388608).  Calls share that array, so calls that overlap on the GPU
+    race; the first call on a device should come before any stream capture.
+    Outputs not given are allocated here by PyTorch, as for every other binding."""
+    B, H, L, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need(t, name, torch.bfloat16, (B, H, L, d))
+    _need(lse, "lse", torch.float32, (B, H, L))
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    delta = torch.empty((B, H, L), device=q.device, dtype=torch.float32) if delta is None else delta
+    st = _lib.load().attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr(), dout.data_ptr(), dq.data_ptr(),
+                                      dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), B, H, L, d,
+                                      _scale(scale, d), int(causal), _stream_of(q))
+    _check(st, "attn_bwd_noalloc")
     return dq, dk, dv, delta
 
 

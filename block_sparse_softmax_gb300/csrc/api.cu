@@ -141,6 +141,45 @@ attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int
                                 static_cast<cudaStream_t>(stream)));
 }
 
+// ---------------------------------------------------------------------------
+// Static scratch for attn_bwd_noalloc.
+//
+// Some callers cannot allocate device memory at all: code running under an
+// allocator that forbids it (a serving process that has pinned its memory
+// budget up front, a plugin host that hands out no device allocations), or a
+// caller that cannot own a workspace buffer across calls.  For them the fp32
+// dQ accumulator of the backward lives in this file-scope array instead of a
+// caller-provided workspace.  Every GPU that loads this library holds the
+// array (kNoAllocScratchFloats * 4 bytes = 32 MiB) until the process exits.
+// In host code `g_bwd_noalloc_scratch` is only a stand-in for the symbol; its
+// device address is looked up once per device with cudaGetSymbolAddress.
+constexpr size_t kNoAllocScratchFloats = size_t(8) << 20;
+static __device__ __align__(256) float g_bwd_noalloc_scratch[kNoAllocScratchFloats];
+float* g_noalloc_scratch_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch on the current device (looked up on first use).
+attn_status_t noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    set_error("cudaGetDevice", e);
+    return ATTN_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_noalloc_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_bwd_noalloc_scratch);
+    if (e != cudaSuccess) {
+      set_error("cudaGetSymbolAddress(g_bwd_noalloc_scratch)", e);
+      return ATTN_ERR_CUDA;
+    }
+    g_noalloc_scratch_ptr[dev] = static_cast<float*>(ptr);
+  }
+  *out = g_noalloc_scratch_ptr[dev];
+  return ATTN_OK;
+}
+
 }  // namespace
 }  // namespace bss
 
@@ -300,6 +339,26 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   p.dv = static_cast<__nv_bfloat16*>(dv);
   return cuda_status("attn_bwd launch",
                      launch_bwd(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream)));
+}
+
+attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               float* delta, int B, int H, int L, int d, float scale, int causal,
+                               void* stream) {
+  if (B < 1 || H < 1 || L < 0) return ATTN_ERR_INVALID_ARG;
+  const size_t need = static_cast<size_t>(B) * H * static_cast<size_t>(L) * (d > 0 ? d : 0);
+  if (need > kNoAllocScratchFloats) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "attn_bwd_noalloc: B*H*L*d = %zu exceeds the static scratch of %zu floats; "
+             "use attn_bwd with a caller-provided workspace",
+             need, kNoAllocScratchFloats);
+    return ATTN_ERR_WORKSPACE;
+  }
+  float* scratch = nullptr;
+  attn_status_t s = noalloc_scratch(&scratch);
+  if (s != ATTN_OK) return s;
+  return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, scratch,
+                  kNoAllocScratchFloats * sizeof(float), B, H, L, d, scale, causal, stream);
 }
 
 attn_status_t attn_poll_status(void* stream) {

@@ -156,6 +156,29 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        int B, int H, int L, int d, float scale, int causal, void* stream);
 
 /*
+ * attn_bwd_noalloc - attn_bwd for callers that cannot allocate device memory.
+ * The source pages have no counterpart: this entry exists for callers that
+ * may not call cudaMalloc or own a workspace (an allocator that forbids new
+ * device allocations, a host process that hands out none).  The fp32 dQ
+ * accumulator lives in a static device array inside the library, 32 MiB
+ * (8388608 floats) per GPU that loads the library, held until the process
+ * exits.  Arguments and results are those of attn_bwd without the workspace.
+ *   - B*H*L*d above 8388608 is rejected with ATTN_ERR_WORKSPACE before any
+ *     device work (attn_last_error_message says why).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call shares the one array and clears it on the stream before use.
+ *     Calls that can overlap on the GPU (different streams, no ordering) race
+ *     on it and give wrong gradients; serialise them.
+ *   - Nothing is allocated or freed (no cudaMalloc, cudaFree or allocating
+ *     library routine).
+ */
+attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                               float* delta, int B, int H, int L, int d, float scale, int causal,
+                               void* stream);
+
+/*
  * attn_poll_status - synchronise `stream`, then return and clear the first
  * error any kernel of this library recorded on the current device since the
  * last poll (ATTN_OK if none).

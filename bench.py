@@ -574,35 +574,44 @@ def run_reference(args):
 
 
 def run_profile_case(kind: str):
-    """A small case of one kernel for ncu: inputs larger than L2, a few hundred
-    MB on the device, one warm-up launch and one measured launch."""
+    """One kernel of the bench step on the step's own workload (causal B=4 H=16
+    L=4096 d=128, inputs 268 MB > L2), or the L=16384 target shape, for ncu:
+    one warm-up launch and one measured launch."""
     import block_sparse_softmax_gb300 as bss
     bss.library()
     dev = torch.device("cuda", 0)
-    if kind in ("fwd", "sparse"):
-        w = Workload("profile_fwd", 2, 16, 8192, 128, True, 1)
-        x = {k: t.to(dev) for k, t in make_inputs(w).items()}
-        if kind == "fwd":
-            fn = lambda: bss.attn_fwd(x["q"], x["k"], x["v"], causal=True, scale=w.scale)
-        else:
-            rp, ci = local_global_random_blocklist(w.n_blocks, seed=2)
-            rpd, cid = torch.from_numpy(rp).to(dev), torch.from_numpy(ci).to(dev)
-            fn = lambda: bss.attn_fwd_blocksparse(x["q"], x["k"], x["v"], rpd, cid, causal=True,
-                                                  scale=w.scale)
+    w = CAUSAL_16K if kind == "fwd16k" else CAUSAL_4K
+    w = Workload(w.name, w.B, w.H, w.L, w.d, True, w.seed, backward=True)
+    x = {k: t.to(dev) for k, t in make_inputs(w).items()}
+    if kind in ("fwd", "fwd16k"):
+        fn = lambda: bss.attn_fwd(x["q"], x["k"], x["v"], causal=True, scale=w.scale)
+    elif kind == "sparse":
+        rp, ci = local_global_random_blocklist(w.n_blocks, seed=2)
+        rpd, cid = torch.from_numpy(rp).to(dev), torch.from_numpy(ci).to(dev)
+        fn = lambda: bss.attn_fwd_blocksparse(x["q"], x["k"], x["v"], rpd, cid, causal=True,
+                                              scale=w.scale)
     elif kind == "bwd":
-        w = Workload("profile_bwd", 2, 16, 8192, 64, True, 4, backward=True)
-        x = {k: t.to(dev) for k, t in make_inputs(w).items()}
         o, lse = bss.attn_fwd(x["q"], x["k"], x["v"], causal=True, scale=w.scale)
         fn = lambda: bss.attn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], causal=True,
                                   scale=w.scale)
-    elif kind == "merge":
-        C, B, H, L, d = 8, 1, 8, 16384, 128
-        g = torch.Generator(device="cpu").manual_seed(0)
-        m = torch.randn(C, B, H, L, generator=g).to(dev)
-        m[0, :, :, : L // 2] = float("-inf")
-        l_ = torch.rand(C, B, H, L, generator=g).to(dev) + 1.0
-        acc = torch.randn(C, B, H, L, d, generator=g).to(dev)
-        fn = lambda: bss.attn_merge_states(m, l_, acc)
+    elif kind in ("partial", "merge"):
+        bounds = chunk_bounds(w.L, 8)
+        kc = [x["k"][:, :, s:e].contiguous() for s, e in bounds]
+        vc = [x["v"][:, :, s:e].contiguous() for s, e in bounds]
+        C = len(bounds)
+        m = torch.empty(C, w.B, w.H, w.L, device=dev)
+        l_ = torch.empty_like(m)
+        acc = torch.empty(C, w.B, w.H, w.L, w.d, device=dev)
+
+        def partials():
+            for c, (s, _) in enumerate(bounds):
+                bss.attn_fwd_partial(x["q"], kc[c], vc[c], causal=True, scale=w.scale,
+                                     k_offset=s, m=m[c], l=l_[c], acc=acc[c])
+        if kind == "partial":
+            fn = partials
+        else:
+            partials()
+            fn = lambda: bss.attn_merge_states(m, l_, acc)
     else:
         raise SystemExit(f"unknown profile case {kind}")
     for _ in range(2):
@@ -616,7 +625,8 @@ def run_profile_case(kind: str):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["fwd", "sparse", "bwd", "merge"], default=None,
+    ap.add_argument("--profile", choices=["fwd", "fwd16k", "sparse", "bwd", "partial", "merge"],
+                    default=None,
                     help="run one small case of one kernel (for ncu) and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)

@@ -29,6 +29,11 @@ EncodeTiledFn g_encode = nullptr;
 
 thread_local char g_last_error[256] = {0};
 
+#ifdef BSS_TRACE
+long long* g_trace_buf = nullptr;
+int g_trace_cta = 0;
+#endif
+
 void set_error(const char* where, cudaError_t e) {
   snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
 }
@@ -94,6 +99,28 @@ attn_status_t make_map(CUtensorMap* map, const void* ptr, int B, int H, long lon
   return ATTN_OK;
 }
 
+// The fp32 dQ accumulator [B, H, L, d] as a 4-D tensor (d, L, H, B) with boxes
+// of 32 fp32 (128 bytes, swizzled) by 128 rows, the target of the backward's
+// bulk reduce-adds (rows past L are never written).
+attn_status_t make_map_f32(CUtensorMap* map, void* ptr, int B, int H, long long L, int d) {
+  if (L < 1) L = 1;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(L) * d * 4,
+                           static_cast<cuuint64_t>(H) * L * d * 4};
+  cuuint32_t box[4] = {32, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_last_error, sizeof(g_last_error), "cuTensorMapEncodeTiled (fp32) failed (%d)",
+             static_cast<int>(r));
+    return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -136,6 +163,10 @@ attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int
   p.k_offset = k_offset;
   p.causal = causal ? 1 : 0;
   p.n_pairs = (Lq + 255) / 256;
+#ifdef BSS_TRACE
+  p.trace = g_trace_buf;
+  p.trace_cta = g_trace_cta;
+#endif
   return cuda_status("attn fwd launch",
                      launch_fwd(d, causal != 0, sparse, partial, tq, tk, tv, p,
                                 static_cast<cudaStream_t>(stream)));
@@ -318,11 +349,12 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   if ((s = get_encoder()) != ATTN_OK) return s;
   BwdParams p{};
   if ((s = status_word(&p.err)) != ATTN_OK) return s;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   if ((s = make_map(&tq, q, B, H, L, d)) != ATTN_OK) return s;
   if ((s = make_map(&tk, k, B, H, L, d)) != ATTN_OK) return s;
   if ((s = make_map(&tv, v, B, H, L, d)) != ATTN_OK) return s;
   if ((s = make_map(&tdo, dout, B, H, L, d)) != ATTN_OK) return s;
+  if ((s = make_map_f32(&tdq, workspace, B, H, L, d)) != ATTN_OK) return s;
   p.B = B;
   p.H = H;
   p.L = L;
@@ -337,8 +369,12 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
+#ifdef BSS_TRACE
+  p.trace = g_trace_buf;
+  p.trace_cta = g_trace_cta;
+#endif
   return cuda_status("attn_bwd launch",
-                     launch_bwd(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream)));
+                     launch_bwd(d, tq, tk, tv, tdo, tdq, p, static_cast<cudaStream_t>(stream)));
 }
 
 attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
@@ -385,5 +421,15 @@ attn_status_t attn_watchdog_selftest(unsigned long long timeout_cycles, void* st
   return cuda_status("watchdog selftest launch",
                      launch_watchdog_selftest(timeout_cycles, err, static_cast<cudaStream_t>(stream)));
 }
+
+#ifdef BSS_TRACE
+// Trace builds only: register a device buffer of kTraceRoles * kTraceEvents
+// int64 for the pipeline events of CTA `cta` (linear block index) of the
+// following launches; NULL switches tracing off.
+void attn_trace_set(void* dev_buf, int cta) {
+  g_trace_buf = static_cast<long long*>(dev_buf);
+  g_trace_cta = cta;
+}
+#endif
 
 }  // extern "C"

@@ -16,13 +16,14 @@
 // while the query tiles stream past.  Everything is computed transposed
 // (TMEM lane = key), so that one thread owns one key row:
 //   S^T  = K_j Q_i^T   and   dP^T = V_j dO_i^T         (SS MMAs, M = 128 keys)
-//   the "softmax" warpgroup turns them into P^T and dS^T (bf16), written back
-//   into the lower halves of the same TMEM columns (tensor-memory A operands)
-//   and dS^T also into shared memory in the layout the dQ MMA reads;
+//   two warpgroups (64 query columns each) turn them into P^T and dS^T
+//   (bf16), written back into the lower halves of the same TMEM columns
+//   (tensor-memory A operands), and dS also into shared memory in the layout
+//   the dQ MMA reads;
 //   dV  += P^T dO_i,  dK += dS^T Q_i                   (TS MMAs)
-//   dQ_i = dS K_j     (SS, M = 128 queries) into the freed upper halves of the
-//   S^T and dP^T columns; a second warpgroup reads it and adds it into the
-//   fp32 accumulator in global memory with vector atomics.
+//   dQ_i = dS K_j     (SS, M = 128 queries, N = d) into S^T's columns once P^T
+//   has been consumed; four more warps stage it in shared memory and add it
+//   into the fp32 accumulator in global memory with bulk tensor reduce-adds.
 // Causal: only query tiles i >= j are visited and the element mask is applied
 // on the diagonal tile and on the ragged tail.
 #include "common.cuh"
@@ -35,43 +36,71 @@ struct BwdCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = kTileM * 128;
   static constexpr int kTileBytes = kTileM * D * 2;
-  static constexpr int kStages = (D == 64) ? 2 : 1;       // Q_i / dO_i ring depth
+  static constexpr int kStagesQ = 2;                     // Q_i ring depth
+  static constexpr int kStagesDO = (D == 128) ? 1 : 2;    // dO_i ring depth (room for dQ staging)
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;
-  static constexpr int kDOOff = kQOff + kStages * kTileBytes;
-  static constexpr int kDSOff = kDOOff + kStages * kTileBytes;   // dS, 128 x 128 bf16
+  static constexpr int kDOOff = kQOff + kStagesQ * kTileBytes;
+  static constexpr int kDSOff = kDOOff + kStagesDO * kTileBytes;  // dS, 128 x 128 bf16
   static constexpr int kDSBytes = kTileM * kTileN * 2;
-  static constexpr int kStatOff = kDSOff + kDSBytes;             // 2 x (lse2[128], delta[128])
+  static constexpr int kStageOff = kDSOff + kDSBytes;    // dQ staging: 128 rows x 64 fp32
+  static constexpr int kStageBytes = kTileM * 64 * 4;
+  static constexpr int kStatOff = kStageOff + kStageBytes;   // 2 x (lse2[128], delta[128])
   static constexpr int kBarOff = kStatOff + 2 * 2 * 128 * 4;
   static constexpr int kBarKV = 0;
   static constexpr int kBarQFull = 1;
-  static constexpr int kBarQEmpty = kBarQFull + kStages;
-  static constexpr int kBarSFull = kBarQEmpty + kStages;
+  static constexpr int kBarQEmpty = kBarQFull + kStagesQ;
+  static constexpr int kBarDOFull = kBarQEmpty + kStagesQ;
+  static constexpr int kBarDOEmpty = kBarDOFull + kStagesDO;
+  static constexpr int kBarSFull = kBarDOEmpty + kStagesDO;
   static constexpr int kBarDSReady = kBarSFull + 1;
   static constexpr int kBarDQFull = kBarDSReady + 1;
   static constexpr int kBarDQFree = kBarDQFull + 1;
   static constexpr int kBarDKVFull = kBarDQFree + 1;
   static constexpr int kBarMmaDone = kBarDKVFull + 1;
-  static constexpr int kBarStat = kBarMmaDone + 1;   // [2]: LSE/D of a query tile staged
-  static constexpr int kNumBars = kBarStat + 2;
+  static constexpr int kBarStat = kBarMmaDone + 1;     // [2]: LSE/D of a query tile staged
+  static constexpr int kBarStaged = kBarStat + 2;      // dQ round written to the staging buffer
+  static constexpr int kBarStageFree = kBarStaged + 1; // staging buffer read by the reduce
+  static constexpr int kNumBars = kBarStageFree + 1;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  // Alignment slack for the 1024-byte aligned layout.  At d=128 the layout
+  // leaves less than 1024 bytes: the kernel then relies on the dynamic shared
+  // memory base being 1024-aligned and checks that before touching it.
+  static constexpr int kPayload = kMiscOff + 16;
+  static constexpr int kSlack = (kPayload + 1024 <= 232448) ? 1024 : 232448 - kPayload;
+  static constexpr int kSmemBytes = kPayload + kSlack;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColST = 0;      // S^T (fp32, 128); P^T bf16 in [0,64); dQ half 0 in [64,128)
-  static constexpr uint32_t kColDPT = 128;   // dP^T (fp32, 128); dS^T bf16 in [128,192); dQ half 1 in [192,256)
+  // TMEM columns: S^T (fp32) at [0,128) and dP^T at [128,256).  Half X of the
+  // P^T/dS^T warpgroups (query columns [64X, 64X+64)) writes its P^T (bf16
+  // pairs, 32 columns) to S^T columns [64X, 64X+32) and its dS^T to dP^T
+  // columns [64X, 64X+32): inside the range it has itself already read.  dV and
+  // dK follow.  dQ of a query tile has its own columns at d=64 ([384,448)); at
+  // d=128 it reuses S^T's columns, issued after the dV MMA that reads P^T.
+  static constexpr uint32_t kColST = 0;
+  static constexpr uint32_t kColDPT = 128;
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
-  static constexpr int kThreads = 384;
+  static constexpr uint32_t kColDQ = (D == 128) ? 0 : 384;
+  // A operand address of query k-step kk (16 queries) inside P^T / dS^T
+  static __device__ __forceinline__ uint32_t pcol(int kk) { return 64 * (kk >> 2) + 8 * (kk & 3); }
+  static constexpr int kThreads = 448;
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(448, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                         const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
+  {
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    if (pad > static_cast<uint32_t>(C::kSlack)) {     // layout would not fit: report, touch nothing
+      if (threadIdx.x == 0) record_error(p.err, ATTN_ERR_UNSUPPORTED);
+      return;
+    }
+  }
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -83,6 +112,8 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
   const int tid = static_cast<int>(threadIdx.x);
+  const bool tr = BSS_TRACE_ON(p, blockIdx.y * gridDim.x + blockIdx.x);
+  (void)tr;
   if (*reinterpret_cast<volatile int*>(p.err) == ATTN_ERR_TIMEOUT) return;
 
   const int bh = blockIdx.x;
@@ -96,18 +127,24 @@ __global__ void __launch_bounds__(384, 1)
 
   if (tid == 0) {
     mbar_init(bar(C::kBarKV), 1);
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < C::kStagesQ; ++s) {
       mbar_init(bar(C::kBarQFull + s), 1);
       mbar_init(bar(C::kBarQEmpty + s), 1);
     }
+    for (int s = 0; s < C::kStagesDO; ++s) {
+      mbar_init(bar(C::kBarDOFull + s), 1);
+      mbar_init(bar(C::kBarDOEmpty + s), 1);
+    }
     mbar_init(bar(C::kBarSFull), 1);
-    mbar_init(bar(C::kBarDSReady), 128);
+    mbar_init(bar(C::kBarDSReady), 256);
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQFree), 128);
     mbar_init(bar(C::kBarDKVFull), 1);
     mbar_init(bar(C::kBarMmaDone), 1);
     mbar_init(bar(C::kBarStat + 0), 128);
     mbar_init(bar(C::kBarStat + 1), 128);
+    mbar_init(bar(C::kBarStaged), 128);
+    mbar_init(bar(C::kBarStageFree), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -130,41 +167,56 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_4d(sbase + C::kKOff + c * C::kChunkBytes, &tmK, bar(C::kBarKV), c * 64, j * kTileN, h, b);
         tma_load_4d(sbase + C::kVOff + c * C::kChunkBytes, &tmV, bar(C::kBarKV), c * 64, j * kTileN, h, b);
       }
-      int it = 0;
-      for (; it < n_it; ++it) {
-        const int s = it % C::kStages;
-        if (it >= C::kStages &&
-            !wait_bar(bar(C::kBarQEmpty + s), ((it / C::kStages) & 1) ^ 1, abort_flag, p.err))
-          break;
+      int nq_ld = 0, ndo_ld = 0;
+      for (int it = 0; it < n_it; ++it) {
         const int row = (i0 + it) * kTileM;
-        mbar_arrive_expect_tx(bar(C::kBarQFull + s), 2 * C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_4d(sbase + C::kQOff + s * C::kTileBytes + c * C::kChunkBytes, &tmQ,
-                      bar(C::kBarQFull + s), c * 64, row, h, b);
-          tma_load_4d(sbase + C::kDOOff + s * C::kTileBytes + c * C::kChunkBytes, &tmDO,
-                      bar(C::kBarQFull + s), c * 64, row, h, b);
-        }
+        const int sq = it % C::kStagesQ;
+        if (it >= C::kStagesQ &&
+            !wait_bar(bar(C::kBarQEmpty + sq), ((it / C::kStagesQ) & 1) ^ 1, abort_flag, p.err))
+          break;
+        mbar_arrive_expect_tx(bar(C::kBarQFull + sq), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(sbase + C::kQOff + sq * C::kTileBytes + c * C::kChunkBytes, &tmQ,
+                      bar(C::kBarQFull + sq), c * 64, row, h, b);
+        ++nq_ld;
+        const int sd = it % C::kStagesDO;
+        if (it >= C::kStagesDO &&
+            !wait_bar(bar(C::kBarDOEmpty + sd), ((it / C::kStagesDO) & 1) ^ 1, abort_flag, p.err))
+          break;
+        mbar_arrive_expect_tx(bar(C::kBarDOFull + sd), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(sbase + C::kDOOff + sd * C::kTileBytes + c * C::kChunkBytes, &tmDO,
+                      bar(C::kBarDOFull + sd), c * 64, row, h, b);
+        ++ndo_ld;
       }
+      // Drain: every load issued has landed before the CTA may exit.
       const long long drain = 1ll << 26;
       wait_bar(bar(C::kBarKV), 0, abort_flag, p.err, drain);
-      for (int x = max(0, it - C::kStages); x < it; ++x)
-        wait_bar(bar(C::kBarQFull + x % C::kStages), (x / C::kStages) & 1, abort_flag, p.err, drain);
+      for (int x = max(0, nq_ld - C::kStagesQ); x < nq_ld; ++x)
+        wait_bar(bar(C::kBarQFull + x % C::kStagesQ), (x / C::kStagesQ) & 1, abort_flag, p.err, drain);
+      for (int x = max(0, ndo_ld - C::kStagesDO); x < ndo_ld; ++x)
+        wait_bar(bar(C::kBarDOFull + x % C::kStagesDO), (x / C::kStagesDO) & 1, abort_flag, p.err, drain);
     }
   } else if (warp == 1) {
     // =================== MMA issuer ===================
     if (lane == 0) {
       constexpr uint32_t kIdescT = idesc_bf16_f32(kTileM, kTileN, false, false);  // S^T, dP^T
       constexpr uint32_t kIdescKV = idesc_bf16_f32(kTileM, D, false, true);       // dV, dK
-      constexpr uint32_t kIdescQ = idesc_bf16_f32(kTileM, 64, true, true);        // dQ halves
+      constexpr uint32_t kIdescQ = idesc_bf16_f32(kTileM, D, true, true);         // dQ
       bool ok = wait_bar(bar(C::kBarKV), 0, abort_flag, p.err);
       const uint32_t ka = sbase + C::kKOff, va = sbase + C::kVOff, dsa = sbase + C::kDSOff;
       for (int it = 0; it < n_it && ok; ++it) {
-        const int s = it % C::kStages;
-        const uint32_t qa = sbase + C::kQOff + s * C::kTileBytes;
-        const uint32_t doa = sbase + C::kDOOff + s * C::kTileBytes;
-        if (!wait_bar(bar(C::kBarQFull + s), (it / C::kStages) & 1, abort_flag, p.err)) break;
-        // S^T and dP^T reuse the columns that held dQ of the previous tile
-        if (it > 0 && !wait_bar(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p.err)) break;
+        const int sq = it % C::kStagesQ;
+        const int sd = it % C::kStagesDO;
+        const uint32_t qa = sbase + C::kQOff + sq * C::kTileBytes;
+        const uint32_t doa = sbase + C::kDOOff + sd * C::kTileBytes;
+        if (!wait_bar(bar(C::kBarQFull + sq), (it / C::kStagesQ) & 1, abort_flag, p.err)) break;
+        BSS_TRACE_EV(p, tr, 1, 5 * it);
+        // at d=128, S^T reuses the columns that held dQ of the previous tile
+        if (C::kColDQ == C::kColST && it > 0 &&
+            !wait_bar(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p.err))
+          break;
+        BSS_TRACE_EV(p, tr, 1, 5 * it + 1);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -172,6 +224,8 @@ __global__ void __launch_bounds__(384, 1)
           mma_ss(tmem + C::kColST, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
                  kIdescT, kk > 0 ? 1u : 0u);
         }
+        if (!wait_bar(bar(C::kBarDOFull + sd), (it / C::kStagesDO) & 1, abort_flag, p.err)) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
@@ -179,41 +233,50 @@ __global__ void __launch_bounds__(384, 1)
                  sdesc_sw128(doa + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBarSFull));
+        BSS_TRACE_EV(p, tr, 1, 5 * it + 2);
         if (!wait_bar(bar(C::kBarDSReady), it & 1, abort_flag, p.err)) break;
+        BSS_TRACE_EV(p, tr, 1, 5 * it + 3);
         tc_fence_after();
-        // dV += P^T dO_i ; dK += dS^T Q_i   (K dimension = the 128 queries)
+        // dV += P^T dO_i  (K dimension = the 128 queries); dO_i is free afterwards
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk) {
-          mma_ts(tmem + C::kColDV, tmem + C::kColST + kk * 8,
+          mma_ts(tmem + C::kColDV, tmem + C::kColST + C::pcol(kk),
                  sdesc_sw128(doa + kk * 2048, C::kChunkBytes, 1024), kIdescKV,
                  (it > 0 || kk > 0) ? 1u : 0u);
         }
+        mma_commit(bar(C::kBarDOEmpty + sd));
+        // dK += dS^T Q_i; Q_i is free afterwards
 #pragma unroll
         for (int kk = 0; kk < kTileM / 16; ++kk) {
-          mma_ts(tmem + C::kColDK, tmem + C::kColDPT + kk * 8,
+          mma_ts(tmem + C::kColDK, tmem + C::kColDPT + C::pcol(kk),
                  sdesc_sw128(qa + kk * 2048, C::kChunkBytes, 1024), kIdescKV,
                  (it > 0 || kk > 0) ? 1u : 0u);
         }
-        // dQ_i = dS K_j  (M = queries, K dimension = the 128 keys), one N=64 MMA per d-half
+        mma_commit(bar(C::kBarQEmpty + sq));
+        // dQ_i = dS K_j  (M = queries, N = d, K dimension = the 128 keys); at
+        // d=64 its own columns are reused once the previous dQ has been read
+        if (C::kColDQ != C::kColST && it > 0 &&
+            !wait_bar(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p.err))
+          break;
 #pragma unroll
-        for (int hh = 0; hh < C::kChunks; ++hh) {
-          const uint32_t dcol = hh == 0 ? C::kColST + 64 : C::kColDPT + 64;
-#pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk) {
-            mma_ss(tmem + dcol, sdesc_sw128(dsa + kk * 2048, C::kChunkBytes, 1024),
-                   sdesc_sw128(ka + hh * C::kChunkBytes + kk * 2048, C::kChunkBytes, 1024), kIdescQ,
-                   kk > 0 ? 1u : 0u);
-          }
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          mma_ss(tmem + C::kColDQ, sdesc_sw128(dsa + kk * 2048, C::kChunkBytes, 1024),
+                 sdesc_sw128(ka + kk * 2048, C::kChunkBytes, 1024), kIdescQ, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBarDQFull));
-        mma_commit(bar(C::kBarQEmpty + s));
+        BSS_TRACE_EV(p, tr, 1, 5 * it + 4);
       }
       mma_commit(bar(C::kBarDKVFull));
       mma_commit(bar(C::kBarMmaDone));
       wait_bar(bar(C::kBarMmaDone), 0, abort_flag, p.err);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // =================== P^T / dS^T warpgroup (thread = key row) ===================
+  } else if (warp < 10) {
+    // =================== P^T / dS^T: two warpgroups, thread = key row ===================
+    // Warpgroup X (warps 2-5: X = 0, warps 6-9: X = 1) handles query columns
+    // [64X, 64X + 64) of S^T and dP^T, 16 at a time; the bf16 results of chunk
+    // c go to columns [64X + 8c, 64X + 8c + 8), which this half has already
+    // read, so the halves never touch each other's columns.
+    const int X = (warp - 2) >> 2;
     const int wq = warp & 3;
     const int kr = wq * 32 + lane;
     const int key = j * kTileN + kr;
@@ -230,183 +293,201 @@ __global__ void __launch_bounds__(384, 1)
       if (i < nq && q < L) {
         const float lse = __ldg(p.lse + stat_base + q);
         l2 = (lse == -INF) ? INF : lse * kLog2e;      // an empty row contributes nothing
-        dl = __ldg(p.delta + stat_base + q);
+        dl = __ldg(p.delta + stat_base + q) * scale;
       } else {
         l2 = INF;
         dl = 0.f;
       }
     };
-    {
+    if (X == 0) {
       float l2, dl;
       load_stats(i0, l2, dl);
       stats[kr] = l2;
       stats[128 + kr] = dl;
       mbar_arrive(bar(C::kBarStat + 0));
     }
-    // Buffer (it & 1) holds the statistics of query tile i0 + it.  It is
-    // rewritten (for tile it + 2) only after S^T of tile it + 1 is ready, which
-    // implies every thread has finished reading it for tile it.
+    // Buffer (it & 1) holds the statistics of query tile i0 + it (LSE in
+    // log2 units, scale * D).  It is rewritten (for tile it + 2) only after S^T
+    // of tile it + 1 is ready, which implies every thread has finished reading
+    // it for tile it.
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int i = i0 + it;
-      const float* lse2 = stats + (it & 1) * 256;
+      const float* lse2 = stats + (it & 1) * 256 + 64 * X;
       const float* dlt = lse2 + 128;
-      float l2n, dln;
-      load_stats(i + 1, l2n, dln);
+      float l2n = 0.f, dln = 0.f;
+      if (X == 0) load_stats(i + 1, l2n, dln);
       if (!wait_bar(bar(C::kBarSFull), it & 1, abort_flag, p.err) ||
           !wait_bar(bar(C::kBarStat + (it & 1)), (it >> 1) & 1, abort_flag, p.err)) {
         ok = false;
         break;
       }
+      const bool trw = tr && kr == 0 && X == 0;
+      BSS_TRACE_EV(p, trw, 2, 3 * it);
       tc_fence_after();
       const bool key_ok = key < L;
-      // element mask: diagonal tile (query < key) or ragged tail (query >= L: its
-      // lse2 is +inf, so P is 0 there already)
+      // element mask: diagonal tile (query < key); the ragged tail (query >= L)
+      // has lse2 = +inf, so P is 0 there already
       const bool diag = CAUSAL && (i == j);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tST + c * 32, sv);
-        tmem_ld32(tDPT + c * 32, dv);
-        tmem_ld_wait(sv);
-        tmem_ld_wait(dv);
-        uint32_t pk[16], dk[16];
-        float dsv[32];
+      // four chunks of 16 query columns; the TMEM loads of chunk c+1 are in
+      // flight while chunk c is computed
+      uint32_t sv[2][16], dv[2][16];
+      tmem_ld16(tST + 64 * X, sv[0]);
+      tmem_ld16(tDPT + 64 * X, dv[0]);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int ql = c * 32 + e;                       // query within the tile
-          float pv = ex2(fmaf(__uint_as_float(sv[e]), sl2, -lse2[ql]));
-          if (!key_ok || (diag && ql < kr)) pv = 0.f;
-          const float ds = pv * (__uint_as_float(dv[e]) - dlt[ql]) * scale;
-          dsv[e] = ds;
-          if (e & 1) {
-            pk[e >> 1] = pack_bf16(__uint_as_float(sv[e - 1]), pv);
-          } else {
-            sv[e] = __float_as_uint(pv);
+      for (int c = 0; c < 4; ++c) {
+        const int cur = c & 1;
+        const int col = 64 * X + 16 * c;                   // first query of the chunk
+        tmem_ld_wait16(sv[cur]);
+        tmem_ld_wait16(dv[cur]);
+        if (c + 1 < 4) {
+          tmem_ld16(tST + col + 16, sv[cur ^ 1]);
+          tmem_ld16(tDPT + col + 16, dv[cur ^ 1]);
+        }
+        float ds[16];
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + 16 * c + e);
+          const float4 d4 = *reinterpret_cast<const float4*>(dlt + 16 * c + e);
+          const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int ql = col + e + u;
+            float pv = ex2(fmaf(__uint_as_float(sv[cur][e + u]), sl2, -la[u]));
+            if (!key_ok || (diag && ql < kr)) pv = 0.f;
+            ds[e + u] = pv * fmaf(__uint_as_float(dv[cur][e + u]), scale, -da[u]);
+            sv[cur][e + u] = __float_as_uint(pv);
           }
         }
+        uint32_t pk[8], dk[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) dk[e] = pack_bf16(dsv[2 * e], dsv[2 * e + 1]);
-        // P^T -> columns [16c, 16c+16) of S^T (already read); dS^T likewise in dP^T
-        uint32_t lo[32];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          lo[e] = pk[e];
-          lo[16 + e] = dk[e];
+        for (int e = 0; e < 8; ++e) {
+          pk[e] = pack_bf16(__uint_as_float(sv[cur][2 * e]), __uint_as_float(sv[cur][2 * e + 1]));
+          dk[e] = pack_bf16(ds[2 * e], ds[2 * e + 1]);
         }
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
-            "%10, %11, %12, %13, %14, %15, %16};" ::"r"(tST + c * 16),
-            "r"(lo[0]), "r"(lo[1]), "r"(lo[2]), "r"(lo[3]), "r"(lo[4]), "r"(lo[5]), "r"(lo[6]),
-            "r"(lo[7]), "r"(lo[8]), "r"(lo[9]), "r"(lo[10]), "r"(lo[11]), "r"(lo[12]), "r"(lo[13]),
-            "r"(lo[14]), "r"(lo[15])
-            : "memory");
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, "
-            "%10, %11, %12, %13, %14, %15, %16};" ::"r"(tDPT + c * 16),
-            "r"(lo[16]), "r"(lo[17]), "r"(lo[18]), "r"(lo[19]), "r"(lo[20]), "r"(lo[21]),
-            "r"(lo[22]), "r"(lo[23]), "r"(lo[24]), "r"(lo[25]), "r"(lo[26]), "r"(lo[27]),
-            "r"(lo[28]), "r"(lo[29]), "r"(lo[30]), "r"(lo[31])
-            : "memory");
+        tmem_st8(tST + 64 * X + 8 * c, pk);
+        tmem_st8(tDPT + 64 * X + 8 * c, dk);
         // dS into shared memory as the M-major A operand of the dQ MMA: queries
-        // 64*mc .. 64*mc+63 form chunk mc, one 128-byte row per key, 16-byte
-        // units swizzled by the row index.
+        // 64*mc .. 64*mc+63 form chunk mc (= X here), one 128-byte row per key,
+        // 16-byte units (8 queries) swizzled by the row index.
 #pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {
-          const int mc = c >> 1;
-          const int unit = (c & 1) * 4 + u4;
-          uint4 w = make_uint4(dk[u4 * 4 + 0], dk[u4 * 4 + 1], dk[u4 * 4 + 2], dk[u4 * 4 + 3]);
-          *reinterpret_cast<uint4*>(ds_smem + mc * C::kChunkBytes + kr * 128 + ((unit ^ (kr & 7)) * 16)) = w;
+        for (int u2 = 0; u2 < 2; ++u2) {
+          const int unit = 2 * c + u2;
+          uint4 w = make_uint4(dk[4 * u2 + 0], dk[4 * u2 + 1], dk[4 * u2 + 2], dk[4 * u2 + 3]);
+          *reinterpret_cast<uint4*>(ds_smem + X * C::kChunkBytes + kr * 128 + ((unit ^ (kr & 7)) * 16)) = w;
         }
       }
+      BSS_TRACE_EV(p, trw, 2, 3 * it + 1);
       tmem_st_wait();
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::kBarDSReady));
-      // statistics of the next query tile
-      float* nxt = stats + ((it + 1) & 1) * 256;
-      nxt[kr] = l2n;
-      nxt[128 + kr] = dln;
-      mbar_arrive(bar(C::kBarStat + ((it + 1) & 1)));
+      BSS_TRACE_EV(p, trw, 2, 3 * it + 2);
+      if (X == 0) {
+        // statistics of the next query tile
+        float* nxt = stats + ((it + 1) & 1) * 256;
+        nxt[kr] = l2n;
+        nxt[128 + kr] = dln;
+        mbar_arrive(bar(C::kBarStat + ((it + 1) & 1)));
+      }
     }
-    // ---- epilogue: dK, dV rows of this key tile ----
+    // ---- epilogue: half 0 stores dK rows, half 1 stores dV rows ----
     if (ok) ok = wait_bar(bar(C::kBarDKVFull), 0, abort_flag, p.err);
     tc_fence_after();
     if (ok) {
       const size_t row_g = static_cast<size_t>(bh) * L + (key < L ? key : 0);
+      const uint32_t tsrc = tmem + lane_base + (X == 0 ? C::kColDK : C::kColDV);
+      __nv_bfloat16* dst = (X == 0 ? p.dk : p.dv) + row_g * D;
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t tsrc = tmem + lane_base + (which == 0 ? C::kColDK : C::kColDV);
-        __nv_bfloat16* dst = (which == 0 ? p.dk : p.dv) + row_g * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          if (n_it > 0) {
-            tmem_ld32(tsrc + c * 32, o);
-            tmem_ld_wait(o);
-          } else {
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        if (n_it > 0) {
+          tmem_ld32(tsrc + c * 32, o);
+          tmem_ld_wait(o);
+        } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = 0u;
-          }
-          if (key < L) {
+          for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (key < L) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 w;
-              w.x = pack_bf16(__uint_as_float(o[e + 0]), __uint_as_float(o[e + 1]));
-              w.y = pack_bf16(__uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
-              w.z = pack_bf16(__uint_as_float(o[e + 4]), __uint_as_float(o[e + 5]));
-              w.w = pack_bf16(__uint_as_float(o[e + 6]), __uint_as_float(o[e + 7]));
-              *reinterpret_cast<uint4*>(dst + c * 32 + e) = w;
-            }
+          for (int e = 0; e < 32; e += 8) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(o[e + 0]), __uint_as_float(o[e + 1]));
+            w.y = pack_bf16(__uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
+            w.z = pack_bf16(__uint_as_float(o[e + 4]), __uint_as_float(o[e + 5]));
+            w.w = pack_bf16(__uint_as_float(o[e + 6]), __uint_as_float(o[e + 7]));
+            *reinterpret_cast<uint4*>(dst + c * 32 + e) = w;
           }
         }
       }
     }
-  } else if (warp >= 8) {
-    // =================== dQ accumulation warpgroup (thread = query row) ===================
+  } else {
+    // =================== dQ: warps 10-13, thread = query row ===================
+    // Each round moves 64 d-columns of the tile's dQ from TMEM to a
+    // 128-byte-swizzled fp32 staging buffer (two TMA boxes of 32 columns);
+    // one thread then adds the boxes into the fp32 accumulator in global
+    // memory with bulk tensor reduce-adds.  The atomic traffic of a per-thread
+    // scheme never reaches the load/store path.
     const int wq = warp & 3;
     const int qr = wq * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    for (int it = 0; it < n_it; ++it) {
-      if (!wait_bar(bar(C::kBarDQFull), it & 1, abort_flag, p.err)) break;
+    const uint32_t tDQ = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::kColDQ;
+    const uint32_t stage = sbase + C::kStageOff;
+    uint8_t* stage_ptr = smem + C::kStageOff;
+    constexpr int kRounds = D / 64;
+    constexpr int kBoxBytes = kTileM * 32 * 4;    // one TMA box: 128 rows x 32 fp32
+    static_assert(2 * kBoxBytes == C::kStageBytes, "two boxes fill the staging buffer");
+    bool ok = true;
+    int g = 0;                                    // global round counter
+    for (int it = 0; it < n_it && ok; ++it) {
+      if (!wait_bar_relaxed(bar(C::kBarDQFull), it & 1, abort_flag, p.err)) break;
+      BSS_TRACE_EV(p, tr && qr == 0, 3, 3 * it);
       tc_fence_after();
-      uint32_t a[32], c2[32];
-      tmem_ld32(tmem + lane_base + C::kColST + 64, a);
-      tmem_ld32(tmem + lane_base + C::kColST + 96, c2);
-      tmem_ld_wait(a);
-      tmem_ld_wait(c2);
-      uint32_t e2[32], f2[32];
-      if (D == 128) {
-        tmem_ld32(tmem + lane_base + C::kColDPT + 64, e2);
-        tmem_ld32(tmem + lane_base + C::kColDPT + 96, f2);
-        tmem_ld_wait(e2);
-        tmem_ld_wait(f2);
-      }
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarDQFree));
-      const int q = (i0 + it) * kTileM + qr;
-      if (q < L) {
-        float4* dst = reinterpret_cast<float4*>(p.dq_acc + (static_cast<size_t>(bh) * L + q) * D);
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          atomicAdd(dst + e / 4, make_float4(__uint_as_float(a[e]), __uint_as_float(a[e + 1]),
-                                             __uint_as_float(a[e + 2]), __uint_as_float(a[e + 3])));
-#pragma unroll
-        for (int e = 0; e < 32; e += 4)
-          atomicAdd(dst + 8 + e / 4, make_float4(__uint_as_float(c2[e]), __uint_as_float(c2[e + 1]),
-                                                 __uint_as_float(c2[e + 2]), __uint_as_float(c2[e + 3])));
-        if (D == 128) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            atomicAdd(dst + 16 + e / 4, make_float4(__uint_as_float(e2[e]), __uint_as_float(e2[e + 1]),
-                                                    __uint_as_float(e2[e + 2]), __uint_as_float(e2[e + 3])));
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            atomicAdd(dst + 24 + e / 4, make_float4(__uint_as_float(f2[e]), __uint_as_float(f2[e + 1]),
-                                                    __uint_as_float(f2[e + 2]), __uint_as_float(f2[e + 3])));
+      for (int r = 0; r < kRounds; ++r, ++g) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tDQ + 64 * r, v0);
+        tmem_ld32(tDQ + 64 * r + 32, v1);
+        tmem_ld_wait(v0);
+        tmem_ld_wait(v1);
+        if (r == kRounds - 1) {
+          tc_fence_before();
+          mbar_arrive(bar(C::kBarDQFree));          // every TMEM read of this tile is done
+          BSS_TRACE_EV(p, tr && qr == 0, 3, 3 * it + 1);
         }
+        // the previous round's reduce has finished reading the staging buffer
+        if (g > 0 && !wait_bar(bar(C::kBarStageFree), (g - 1) & 1, abort_flag, p.err)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {               // box 0: columns 0..31 of the round
+          *reinterpret_cast<uint4*>(stage_ptr + qr * 128 + ((u ^ (qr & 7)) * 16)) =
+              make_uint4(v0[4 * u], v0[4 * u + 1], v0[4 * u + 2], v0[4 * u + 3]);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {               // box 1: columns 32..63
+          *reinterpret_cast<uint4*>(stage_ptr + kBoxBytes + qr * 128 + ((u ^ (qr & 7)) * 16)) =
+              make_uint4(v1[4 * u], v1[4 * u + 1], v1[4 * u + 2], v1[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(C::kBarStaged));
+        if (qr == 0) {
+          if (!wait_bar(bar(C::kBarStaged), g & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          const int row = (i0 + it) * kTileM;
+          tma_reduce_add_4d(&tmDQ, stage, 64 * r, row, h, b);
+          tma_reduce_add_4d(&tmDQ, stage + kBoxBytes, 64 * r + 32, row, h, b);
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(bar(C::kBarStageFree));
+        }
+        __syncwarp();                               // reconverge before the next TMEM load
       }
+      BSS_TRACE_EV(p, tr && qr == 0, 3, 3 * it + 2);
     }
+    if (qr == 0) bulk_wait_all();                   // every reduction has landed
   }
 
   tc_fence_before();
@@ -469,7 +550,8 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_convert_kernel(const float* a
 
 template <int D, bool CAUSAL>
 cudaError_t launch_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        const CUtensorMap& tdo, const BwdParams& p, cudaStream_t st) {
+                        const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                        cudaStream_t st) {
   using C = BwdCfg<D>;
   auto kern = attn_bwd_main_kernel<D, CAUSAL>;
   static bool configured = false;
@@ -479,7 +561,7 @@ cudaError_t launch_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     configured = true;
   }
   dim3 grid(p.B * p.H, (p.L + kTileN - 1) / kTileN);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, p);
+  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 
@@ -494,7 +576,8 @@ unsigned grid_for(long long work, int per_block) {
 }  // namespace
 
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, cudaStream_t st) {
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                       cudaStream_t st) {
   const long long rows = static_cast<long long>(p.B) * p.H * p.L;
   cudaError_t e;
   if (d == 64) {
@@ -506,9 +589,11 @@ cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (d == 64)
-    e = p.causal ? launch_main<64, true>(tq, tk, tv, tdo, p, st) : launch_main<64, false>(tq, tk, tv, tdo, p, st);
+    e = p.causal ? launch_main<64, true>(tq, tk, tv, tdo, tdq, p, st)
+                 : launch_main<64, false>(tq, tk, tv, tdo, tdq, p, st);
   else
-    e = p.causal ? launch_main<128, true>(tq, tk, tv, tdo, p, st) : launch_main<128, false>(tq, tk, tv, tdo, p, st);
+    e = p.causal ? launch_main<128, true>(tq, tk, tv, tdo, tdq, p, st)
+                 : launch_main<128, false>(tq, tk, tv, tdo, tdq, p, st);
   if (e != cudaSuccess) return e;
   const long long n8 = rows * d / 8;
   attn_bwd_dq_convert_kernel<<<grid_for(n8, 256), 256, 0, st>>>(p.dq_acc, p.dq, n8);

@@ -44,6 +44,43 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// Optional pipeline trace for performance work.  Off unless the library is
+// built with -DBSS_TRACE: then the roles of one chosen CTA record clock64()
+// timestamps of their pipeline events into trace[role * kTraceEvents + i]
+// (a device buffer registered with attn_trace_set, trace builds only).  The
+// default build compiles every trace point away.
+constexpr int kTraceRoles = 8;
+constexpr int kTraceEvents = 1024;
+#ifdef BSS_TRACE
+#define BSS_TRACE_ON(p, cta_linear) ((p).trace != nullptr && static_cast<int>(cta_linear) == (p).trace_cta)
+#define BSS_TRACE_EV(p, on, role, idx)                                                  \
+  do {                                                                                  \
+    if ((on) && (idx) < kTraceEvents) (p).trace[(role) * kTraceEvents + (idx)] = clock64(); \
+  } while (0)
+#else
+#define BSS_TRACE_ON(p, cta_linear) false
+#define BSS_TRACE_EV(p, on, role, idx) ((void)0)
+#endif
+
+// Bounded wait for roles off the critical path: polls with a short sleep in
+// between so that waiting warps leave the issue slots to the computing ones.
+__device__ __forceinline__ bool wait_bar_relaxed(uint32_t bar, uint32_t parity,
+                                                 volatile int* abort_flag, int* err,
+                                                 long long limit = kWaitLimitCycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    __nanosleep(256);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      *abort_flag = 1;
+      record_error(err, ATTN_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 struct FwdParams {
   int B, H, Lq, Lk;
   float scale_log2;        // scale * log2(e): scores are exponentiated in base 2
@@ -62,6 +99,8 @@ struct FwdParams {
   int n_qblk, nnz;
   int n_pairs;             // CTAs along x: ceil(Lq / 256)
   int* err;
+  long long* trace;        // trace builds only (nullptr otherwise)
+  int trace_cta;
 };
 
 struct MergeParams {
@@ -87,6 +126,8 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int* err;
+  long long* trace;        // trace builds only (nullptr otherwise)
+  int trace_cta;
 };
 
 }  // namespace bss
@@ -98,6 +139,7 @@ cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUte
                        cudaStream_t st);
 cudaError_t launch_merge(int d, const MergeParams& p, int* err, cudaStream_t st);
 cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, cudaStream_t st);
+                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                       cudaStream_t st);
 cudaError_t launch_watchdog_selftest(unsigned long long cycles, int* err, cudaStream_t st);
 }  // namespace bss

@@ -12,8 +12,9 @@
 //     a single K/V stream: each K/V tile is loaded once for 256 query rows;
 //   * warp 0 issues TMA loads (128-byte swizzled boxes of 128 rows x 64 d) into
 //     a ring of K and V stages; warp 1 (one thread) issues every tcgen05.mma;
-//     warpgroups 1 and 2 run the online softmax of tile 0 and tile 1, one
-//     thread per query row (TMEM lane = row);
+//     warpgroups 1 and 2 (warps 4-7, 8-11) run the online softmax of tile 0
+//     and tile 1, one thread per query row (TMEM lane = row), with a larger
+//     register budget handed over from warpgroup 0 (setmaxnreg);
 //   * TMEM (512 columns): S0 | S1 | O0 | O1.  S = Q K^T is written by an SS
 //     MMA; the softmax warpgroup reads its row, writes P (bf16) back into the
 //     upper half of the same S columns, and P V accumulates into O by a TS MMA
@@ -40,7 +41,7 @@ struct FwdCfg {
   static constexpr int kChunkBytes = kTileM * 128;         // 128 rows x 128 bytes
   static constexpr int kTileBytes = kTileM * D * 2;
   static constexpr int kStagesK = (D == 128) ? 2 : 4;
-  static constexpr int kStagesV = (D == 128) ? 2 : 4;
+  static constexpr int kStagesV = (D == 128) ? 3 : 4;   // V is consumed last: deeper prefetch
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kStagesK * kTileBytes;
@@ -65,6 +66,14 @@ struct FwdCfg {
   static constexpr uint32_t kColP = 64;                     // P_t at S_t + 64 (bf16 pairs)
   static constexpr uint32_t kColO = 256;                    // O_t at 256 + t*D
   static constexpr int kThreads = 384;
+  // Register split per warpgroup (setmaxnreg): warpgroup 0 (TMA, MMA, two idle
+  // warps) keeps kRegsLow, the two softmax warpgroups get kRegsHigh.  Each SM
+  // sub-partition holds one warp of every warpgroup: 88 + 2 * 200 = 488 <= 512
+  // registers per lane there, and the whole split 128*88 + 256*200 = 62464 fits
+  // the 384 * R registers the launch holds for any ptxas assignment R >= 163
+  // (the build asserts R = 168).
+  static constexpr uint32_t kRegsLow = 88;
+  static constexpr uint32_t kRegsHigh = 200;
 };
 
 // The ordered list of key blocks this CTA visits and which of its two tiles
@@ -118,6 +127,8 @@ __global__ void __launch_bounds__(384, 1)
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
   const int tid = static_cast<int>(threadIdx.x);
+  const bool tr = BSS_TRACE_ON(p, blockIdx.y * gridDim.x + blockIdx.x);
+  (void)tr;
   // A launch whose earlier CTAs already timed out stops at once instead of
   // timing out CTA by CTA.
   if (*reinterpret_cast<volatile int*>(p.err) == ATTN_ERR_TIMEOUT) return;
@@ -170,6 +181,7 @@ __global__ void __launch_bounds__(384, 1)
     tmem_alloc(sbase + C::kMiscOff, C::kTmemCols);
     tmem_relinquish();
   }
+  BSS_TRACE_EV(p, tr && tid == 0, 6, 0);
   if (SPARSE) {
     for (int i = tid; i < 2 * C::kBitmapWords; i += C::kThreads) bitmap[i] = 0u;
     __syncthreads();
@@ -204,6 +216,8 @@ __global__ void __launch_bounds__(384, 1)
   sch.bm0 = SPARSE ? bitmap : nullptr;
   sch.bm1 = SPARSE ? bitmap + C::kBitmapWords : nullptr;
 
+  if (warp < 4) {
+  regs_dec<C::kRegsLow>();
   if (warp == 0) {
     // =================== TMA producer ===================
     if (lane == 0) {
@@ -232,6 +246,7 @@ __global__ void __launch_bounds__(384, 1)
           ok = false;
           break;
         }
+        BSS_TRACE_EV(p, tr, 0, 2 * i);
         const uint32_t ks = sbase + C::kKOff + sk * C::kTileBytes;
         mbar_arrive_expect_tx(bar(C::kBarKFull + sk), C::kTileBytes);
 #pragma unroll
@@ -244,6 +259,7 @@ __global__ void __launch_bounds__(384, 1)
           ok = false;
           break;
         }
+        BSS_TRACE_EV(p, tr, 0, 2 * i + 1);
         const uint32_t vs = sbase + C::kVOff + sv * C::kTileBytes;
         mbar_arrive_expect_tx(bar(C::kBarVFull + sv), C::kTileBytes);
 #pragma unroll
@@ -315,6 +331,7 @@ __global__ void __launch_bounds__(384, 1)
         const int sv = i % C::kStagesV;
         const int skn = (i + 1) % C::kStagesK;
         if (!wait_bar(bar(C::kBarVFull + sv), (i / C::kStagesV) & 1, abort_flag, p.err)) break;
+        BSS_TRACE_EV(p, tr, 1, 4 * i);
         tc_fence_after();
         bool kready = false;
         for (int t = 0; t < 2 && ok; ++t) {
@@ -324,6 +341,7 @@ __global__ void __launch_bounds__(384, 1)
               break;
             }
             ++pcount[t];
+            BSS_TRACE_EV(p, tr, 1, 4 * i + 1 + t);
             tc_fence_after();
             issue_pv(t, sv);
           }
@@ -340,6 +358,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         if (!ok) break;
+        BSS_TRACE_EV(p, tr, 1, 4 * i + 3);
         mma_commit(bar(C::kBarVEmpty + sv));
         if (nkb >= 0) mma_commit(bar(C::kBarKEmpty + skn));
         kb = nkb;
@@ -351,8 +370,10 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(bar(C::kBarMmaDone));
       wait_bar(bar(C::kBarMmaDone), 0, abort_flag, p.err);
     }
-  } else if (warp >= 4) {
-    // =================== softmax warpgroups ===================
+  }
+  } else {
+    regs_inc<C::kRegsHigh>();
+    // =================== softmax warpgroups (warps 4-7: tile 0, 8-11: tile 1) ===================
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;                      // TMEM lane quarter of this warp
     const int row_in_tile = wq * 32 + lane;
@@ -375,6 +396,8 @@ __global__ void __launch_bounds__(384, 1)
         ok = false;
         break;
       }
+      const bool trw = tr && lane == 0 && wq == 0;
+      BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt);
       tc_fence_after();
       uint32_t s[4][32];
 #pragma unroll
@@ -397,15 +420,19 @@ __global__ void __launch_bounds__(384, 1)
           for (int j = 0; j < 32; ++j)
             if (c * 32 + j > jl) s[c][j] = __float_as_uint(NEG_INF);
       }
-      float mx0 = NEG_INF, mx1 = NEG_INF;
+      // row max over 8 independent chains (short dependency chains)
+      float mx[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(s[0][u]);
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          mx0 = fmaxf(mx0, __uint_as_float(s[c][j]));
-          mx1 = fmaxf(mx1, __uint_as_float(s[c][j + 1]));
-        }
-      const float mblk = fmaxf(mx0, mx1) * sl2;
+        for (int j = (c == 0 ? 8 : 0); j < 32; j += 8)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(s[c][j + u]));
+      const float mblk =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+      BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt + 1);
       mt = fmaxf(mt, mblk);
       float alpha = 1.f;
       bool moved = false;
@@ -415,7 +442,9 @@ __global__ void __launch_bounds__(384, 1)
         moved = true;
       }
       const float mu = (m2 == NEG_INF) ? 0.f : m2;
-      float rs0 = 0.f, rs1 = 0.f;
+      float rs[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) rs[u] = 0.f;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
@@ -426,14 +455,14 @@ __global__ void __launch_bounds__(384, 1)
           for (int j = 0; j < 32; j += 2) {
             const float p0 = ex2(fmaf(__uint_as_float(s[c][j]), sl2, -mu));
             const float p1 = ex2(fmaf(__uint_as_float(s[c][j + 1]), sl2, -mu));
-            rs0 += p0;
-            rs1 += p1;
+            rs[(j >> 1) & 3] += p0 + p1;
             pk[c2 * 16 + j / 2] = pack_bf16(p0, p1);
           }
         }
         tmem_st32(tP + half * 32, pk);
       }
-      l = l * alpha + (rs0 + rs1);
+      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+      BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt + 2);
       // rescale O when this row's reference max moved and O already holds data
       const bool fix = moved && cnt > 0;
       if (__any_sync(0xFFFFFFFFu, fix)) {
@@ -451,6 +480,7 @@ __global__ void __launch_bounds__(384, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::kBarPFull + t));
+      BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt + 3);
       ++cnt;
     }
 
@@ -459,23 +489,21 @@ __global__ void __launch_bounds__(384, 1)
       ok = wait_bar(bar(C::kBarOFull + t), 0, abort_flag, p.err);
       tc_fence_after();
     }
+    BSS_TRACE_EV(p, tr && lane == 0 && wq == 0, 4 + t, 0);
     if (ok) {
       const bool inb = row < p.Lq;
       const size_t row_g = static_cast<size_t>(bh) * p.Lq + (inb ? row : 0);
       if (PARTIAL) {
+        // An empty state (m = -inf) is fully described by m and l; its acc row
+        // is not written (a merge never reads it).
         const float factor = (mt == NEG_INF || cnt == 0) ? 0.f : ex2(m2 - mt);
         float* dst = p.acc_out + row_g * D;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 32 && cnt > 0; ++c) {
           uint32_t o[32];
-          if (cnt > 0) {
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait(o);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = 0u;
-          }
-          if (inb) {
+          tmem_ld32(tO + c * 32, o);
+          tmem_ld_wait(o);
+          if (inb && mt != NEG_INF) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
               float4 v4 = make_float4(__uint_as_float(o[j]) * factor, __uint_as_float(o[j + 1]) * factor,
@@ -518,6 +546,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   }
 
+  if (warp >= 4) BSS_TRACE_EV(p, tr && lane == 0 && (warp & 3) == 0, 4 + ((warp - 4) >> 2), 1);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {

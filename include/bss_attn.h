@@ -77,7 +77,9 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  * invariant) and section 4 (one Ring-Attention step on a KV block).
  *   Writes, per query row, m = max allowed scaled logit (natural-log units),
  *   l = sum exp(s - m), acc = sum exp(s - m) V over the keys of this chunk.
- *   Rows with no allowed key get the empty state m = -inf, l = 0, acc = 0.
+ *   Rows with no allowed key get the empty state m = -inf, l = 0; their acc
+ *   row is left untouched (an empty state is identified by m = -inf and is
+ *   never read by attn_merge_states).
  *   m, l: fp32 [B,H,Lq]; acc: fp32 [B,H,Lq,d].  Other arguments as attn_fwd;
  *   k_offset is the absolute position of the chunk's first key.
  */

@@ -58,8 +58,8 @@ struct BwdCfg {
   static constexpr int kBarDQFull = kBarDSReady + 1;
   static constexpr int kBarDQFree = kBarDQFull + 1;
   static constexpr int kBarDKVFull = kBarDQFree + 1;
-  static constexpr int kBarMmaDone = kBarDKVFull + 1;
-  static constexpr int kBarStat = kBarMmaDone + 1;     // [2]: LSE/D of a query tile staged
+  static constexpr int kBarMmaDone = kBarDKVFull + 1;  // [2], one per MMA issuer
+  static constexpr int kBarStat = kBarMmaDone + 2;     // [2]: LSE/D of a query tile staged
   static constexpr int kBarStaged = kBarStat + 2;      // dQ round written to the staging buffer
   static constexpr int kBarStageFree = kBarStaged + 1; // staging buffer read by the reduce
   static constexpr int kNumBars = kBarStageFree + 1;
@@ -84,11 +84,15 @@ struct BwdCfg {
   static constexpr uint32_t kColDQ = (D == 128) ? 0 : 384;
   // A operand address of query k-step kk (16 queries) inside P^T / dS^T
   static __device__ __forceinline__ uint32_t pcol(int kk) { return 64 * (kk >> 2) + 8 * (kk & 3); }
-  static constexpr int kThreads = 448;
+  // Two MMA issuers pay off at d=64, where each MMA is short; at d=128 one
+  // issuer measured faster.
+  static constexpr bool kTwoIssuers = (D == 64);
+  static constexpr int kIssuers = kTwoIssuers ? 2 : 1;
+  static constexpr int kThreads = kTwoIssuers ? 512 : 448;
 };
 
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(448, 1)
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
@@ -127,20 +131,23 @@ __global__ void __launch_bounds__(448, 1)
 
   if (tid == 0) {
     mbar_init(bar(C::kBarKV), 1);
+    // Two MMA issuers: A (S^T, dV, dQ) and B (dP^T, dK); barriers that both
+    // release or fill count two arrivals.
     for (int s = 0; s < C::kStagesQ; ++s) {
       mbar_init(bar(C::kBarQFull + s), 1);
-      mbar_init(bar(C::kBarQEmpty + s), 1);
+      mbar_init(bar(C::kBarQEmpty + s), C::kIssuers);
     }
     for (int s = 0; s < C::kStagesDO; ++s) {
       mbar_init(bar(C::kBarDOFull + s), 1);
-      mbar_init(bar(C::kBarDOEmpty + s), 1);
+      mbar_init(bar(C::kBarDOEmpty + s), C::kIssuers);
     }
-    mbar_init(bar(C::kBarSFull), 1);
+    mbar_init(bar(C::kBarSFull), C::kIssuers);
     mbar_init(bar(C::kBarDSReady), 256);
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQFree), 128);
-    mbar_init(bar(C::kBarDKVFull), 1);
-    mbar_init(bar(C::kBarMmaDone), 1);
+    mbar_init(bar(C::kBarDKVFull), C::kIssuers);
+    mbar_init(bar(C::kBarMmaDone + 0), 1);
+    mbar_init(bar(C::kBarMmaDone + 1), 1);
     mbar_init(bar(C::kBarStat + 0), 128);
     mbar_init(bar(C::kBarStat + 1), 128);
     mbar_init(bar(C::kBarStaged), 128);
@@ -197,9 +204,17 @@ __global__ void __launch_bounds__(448, 1)
       for (int x = max(0, ndo_ld - C::kStagesDO); x < ndo_ld; ++x)
         wait_bar(bar(C::kBarDOFull + x % C::kStagesDO), (x / C::kStagesDO) & 1, abort_flag, p.err, drain);
     }
-  } else if (warp == 1) {
-    // =================== MMA issuer ===================
+  } else if (warp == 1 || (C::kTwoIssuers && warp == 14)) {
+    // =================== MMA issuers ===================
+    // With two issuers, A (warp 1) issues S^T, dV, dQ and B (warp 14) issues
+    // dP^T, dK; with one, warp 1 issues everything.  Each issuer overwrites only
+    // TMEM columns that its own earlier MMAs read (S^T over P^T after dV, dQ
+    // over P^T after dV at d=128; dP^T over dS^T after dK), so issue order
+    // within one issuer keeps them safe.
     if (lane == 0) {
+      const bool A = (warp == 1);
+      const bool doA = A;                          // S^T, dV, dQ
+      const bool doB = !A || !C::kTwoIssuers;      // dP^T, dK
       constexpr uint32_t kIdescT = idesc_bf16_f32(kTileM, kTileN, false, false);  // S^T, dP^T
       constexpr uint32_t kIdescKV = idesc_bf16_f32(kTileM, D, false, true);       // dV, dK
       constexpr uint32_t kIdescQ = idesc_bf16_f32(kTileM, D, true, true);         // dQ
@@ -210,65 +225,90 @@ __global__ void __launch_bounds__(448, 1)
         const int sd = it % C::kStagesDO;
         const uint32_t qa = sbase + C::kQOff + sq * C::kTileBytes;
         const uint32_t doa = sbase + C::kDOOff + sd * C::kTileBytes;
-        if (!wait_bar(bar(C::kBarQFull + sq), (it / C::kStagesQ) & 1, abort_flag, p.err)) break;
-        BSS_TRACE_EV(p, tr, 1, 5 * it);
-        // at d=128, S^T reuses the columns that held dQ of the previous tile
-        if (C::kColDQ == C::kColST && it > 0 &&
-            !wait_bar(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p.err))
-          break;
-        BSS_TRACE_EV(p, tr, 1, 5 * it + 1);
+        if (doA) {
+          if (!wait_bar(bar(C::kBarQFull + sq), (it / C::kStagesQ) & 1, abort_flag, p.err)) break;
+          BSS_TRACE_EV(p, tr, 1, 5 * it);
+          // at d=128, S^T reuses the columns that held dQ of the previous tile
+          if (C::kColDQ == C::kColST && it > 0 &&
+              !wait_bar(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p.err))
+            break;
+          BSS_TRACE_EV(p, tr, 1, 5 * it + 1);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+            mma_ss(tmem + C::kColST, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
+                   kIdescT, kk > 0 ? 1u : 0u);
+          }
+          if (C::kTwoIssuers) {
+            mma_commit(bar(C::kBarSFull));
+            mma_commit(bar(C::kBarQEmpty + sq));
+          }
+        }
+        if (doB) {
+          if (!wait_bar(bar(C::kBarDOFull + sd), (it / C::kStagesDO) & 1, abort_flag, p.err)) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+            mma_ss(tmem + C::kColDPT, sdesc_sw128(va + off, 16, 1024),
+                   sdesc_sw128(doa + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(C::kBarSFull));
+          if (C::kTwoIssuers) mma_commit(bar(C::kBarDOEmpty + sd));
+        }
+        BSS_TRACE_EV(p, tr && A, 1, 5 * it + 2);
+        // the P/dS warps run for a while: poll gently so that the issue slots
+        // they share with this warp stay theirs
+        if (!wait_bar_relaxed<64>(bar(C::kBarDSReady), it & 1, abort_flag, p.err)) break;
+        BSS_TRACE_EV(p, tr && A, 1, 5 * it + 3);
         tc_fence_after();
+        if (doA) {
+          // dV += P^T dO_i  (K dimension = the 128 queries)
+          if (C::kTwoIssuers &&
+              !wait_bar(bar(C::kBarDOFull + sd), (it / C::kStagesDO) & 1, abort_flag, p.err))
+            break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColST, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
-                 kIdescT, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kTileM / 16; ++kk) {
+            mma_ts(tmem + C::kColDV, tmem + C::kColST + C::pcol(kk),
+                   sdesc_sw128(doa + kk * 2048, C::kChunkBytes, 1024), kIdescKV,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(C::kBarDOEmpty + sd));
         }
-        if (!wait_bar(bar(C::kBarDOFull + sd), (it / C::kStagesDO) & 1, abort_flag, p.err)) break;
-        tc_fence_after();
+        if (doB) {
+          // dK += dS^T Q_i
+          if (C::kTwoIssuers &&
+              !wait_bar(bar(C::kBarQFull + sq), (it / C::kStagesQ) & 1, abort_flag, p.err))
+            break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColDPT, sdesc_sw128(va + off, 16, 1024),
-                 sdesc_sw128(doa + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kTileM / 16; ++kk) {
+            mma_ts(tmem + C::kColDK, tmem + C::kColDPT + C::pcol(kk),
+                   sdesc_sw128(qa + kk * 2048, C::kChunkBytes, 1024), kIdescKV,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(bar(C::kBarQEmpty + sq));
         }
-        mma_commit(bar(C::kBarSFull));
-        BSS_TRACE_EV(p, tr, 1, 5 * it + 2);
-        if (!wait_bar(bar(C::kBarDSReady), it & 1, abort_flag, p.err)) break;
-        BSS_TRACE_EV(p, tr, 1, 5 * it + 3);
-        tc_fence_after();
-        // dV += P^T dO_i  (K dimension = the 128 queries); dO_i is free afterwards
+        if (doA) {
+          // dQ_i = dS K_j  (M = queries, N = d, K dimension = the 128 keys); at
+          // d=64 its own columns are reused once the previous dQ has been read
+          if (C::kColDQ != C::kColST && it > 0 &&
+              !wait_bar(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p.err))
+            break;
 #pragma unroll
-        for (int kk = 0; kk < kTileM / 16; ++kk) {
-          mma_ts(tmem + C::kColDV, tmem + C::kColST + C::pcol(kk),
-                 sdesc_sw128(doa + kk * 2048, C::kChunkBytes, 1024), kIdescKV,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kTileN / 16; ++kk) {
+            mma_ss(tmem + C::kColDQ, sdesc_sw128(dsa + kk * 2048, C::kChunkBytes, 1024),
+                   sdesc_sw128(ka + kk * 2048, C::kChunkBytes, 1024), kIdescQ, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(C::kBarDQFull));
         }
-        mma_commit(bar(C::kBarDOEmpty + sd));
-        // dK += dS^T Q_i; Q_i is free afterwards
-#pragma unroll
-        for (int kk = 0; kk < kTileM / 16; ++kk) {
-          mma_ts(tmem + C::kColDK, tmem + C::kColDPT + C::pcol(kk),
-                 sdesc_sw128(qa + kk * 2048, C::kChunkBytes, 1024), kIdescKV,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(C::kBarQEmpty + sq));
-        // dQ_i = dS K_j  (M = queries, N = d, K dimension = the 128 keys); at
-        // d=64 its own columns are reused once the previous dQ has been read
-        if (C::kColDQ != C::kColST && it > 0 &&
-            !wait_bar(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p.err))
-          break;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          mma_ss(tmem + C::kColDQ, sdesc_sw128(dsa + kk * 2048, C::kChunkBytes, 1024),
-                 sdesc_sw128(ka + kk * 2048, C::kChunkBytes, 1024), kIdescQ, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(C::kBarDQFull));
-        BSS_TRACE_EV(p, tr, 1, 5 * it + 4);
+        BSS_TRACE_EV(p, tr && A, 1, 5 * it + 4);
       }
       mma_commit(bar(C::kBarDKVFull));
-      mma_commit(bar(C::kBarMmaDone));
-      wait_bar(bar(C::kBarMmaDone), 0, abort_flag, p.err);
+      mma_commit(bar(C::kBarMmaDone + (A ? 0 : 1)));
+      wait_bar(bar(C::kBarMmaDone + (A ? 0 : 1)), 0, abort_flag, p.err);
     }
   } else if (warp < 10) {
     // =================== P^T / dS^T: two warpgroups, thread = key row ===================
@@ -422,7 +462,7 @@ __global__ void __launch_bounds__(448, 1)
         }
       }
     }
-  } else {
+  } else if (warp >= 10 && warp < 14) {
     // =================== dQ: warps 10-13, thread = query row ===================
     // Each round moves 64 d-columns of the tile's dQ from TMEM to a
     // 128-byte-swizzled fp32 staging buffer (two TMA boxes of 32 columns);
@@ -454,10 +494,19 @@ __global__ void __launch_bounds__(448, 1)
           mbar_arrive(bar(C::kBarDQFree));          // every TMEM read of this tile is done
           BSS_TRACE_EV(p, tr && qr == 0, 3, 3 * it + 1);
         }
-        // the previous round's reduce has finished reading the staging buffer
-        if (g > 0 && !wait_bar(bar(C::kBarStageFree), (g - 1) & 1, abort_flag, p.err)) {
-          ok = false;
-          break;
+        // The reduce of the previous round must have read the staging buffer
+        // before it is rewritten.  The issuing thread waits for that only now,
+        // after this round's TMEM reads, so those (and dq_free) never queue
+        // behind a bulk reduce.
+        if (g > 0) {
+          if (qr == 0) {
+            bulk_wait_read_all();
+            mbar_arrive(bar(C::kBarStageFree));
+          }
+          if (!wait_bar(bar(C::kBarStageFree), (g - 1) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {               // box 0: columns 0..31 of the round
@@ -480,8 +529,6 @@ __global__ void __launch_bounds__(448, 1)
           tma_reduce_add_4d(&tmDQ, stage, 64 * r, row, h, b);
           tma_reduce_add_4d(&tmDQ, stage + kBoxBytes, 64 * r + 32, row, h, b);
           bulk_commit_group();
-          bulk_wait_read_all();
-          mbar_arrive(bar(C::kBarStageFree));
         }
         __syncwarp();                               // reconverge before the next TMEM load
       }

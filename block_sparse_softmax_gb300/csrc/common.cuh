@@ -64,13 +64,14 @@ constexpr int kTraceEvents = 1024;
 
 // Bounded wait for roles off the critical path: polls with a short sleep in
 // between so that waiting warps leave the issue slots to the computing ones.
+template <unsigned kSleepNs = 256>
 __device__ __forceinline__ bool wait_bar_relaxed(uint32_t bar, uint32_t parity,
                                                  volatile int* abort_flag, int* err,
                                                  long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    __nanosleep(256);
+    __nanosleep(kSleepNs);
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {

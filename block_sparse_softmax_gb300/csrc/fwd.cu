@@ -156,6 +156,29 @@ __global__ void __launch_bounds__(384, 1)
     }
   }
 
+  // A dense-mode CTA whose rows see no key (all rows before a chunk's first
+  // key, or past the end) writes the empty state of its rows and leaves
+  // without setting anything up.
+  if (!SPARSE && kbmax[0] < 0 && kbmax[1] < 0) {
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const int nrows = max(0, min(2 * kTileM, p.Lq - r0[0]));
+    const size_t row0 = static_cast<size_t>(bh) * p.Lq + r0[0];
+    for (int r = tid; r < nrows; r += C::kThreads) {
+      if (PARTIAL) {
+        p.m_out[row0 + r] = NEG_INF;
+        p.l_out[row0 + r] = 0.f;
+      } else {
+        p.lse[row0 + r] = NEG_INF;
+      }
+    }
+    if (!PARTIAL) {
+      uint4* o4 = reinterpret_cast<uint4*>(p.o + row0 * D);
+      const int n16 = nrows * D / 8;
+      for (int x = tid; x < n16; x += C::kThreads) o4[x] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    return;
+  }
+
   // ---- set-up: barriers, tensor memory, block-sparse bitmaps -------------
   if (tid == 0) {
     mbar_init(bar(C::kBarQFull + 0), 1);

@@ -129,7 +129,8 @@ attn_status_t check_common(int B, int H, long long Lq, long long Lk, int d, floa
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
-  if ((Lq + 255) / 256 > 65535) return ATTN_ERR_UNSUPPORTED;
+  if ((Lq + 127) / 128 > 65535) return ATTN_ERR_UNSUPPORTED;   // grid y of the backward
+  if (static_cast<long long>(B) * H * ((Lq + 255) / 256) > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
 
@@ -163,6 +164,7 @@ attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int
   p.k_offset = k_offset;
   p.causal = causal ? 1 : 0;
   p.n_pairs = (Lq + 255) / 256;
+  p.n_items = B * H * p.n_pairs;
 #ifdef BSS_TRACE
   p.trace = g_trace_buf;
   p.trace_cta = g_trace_cta;

@@ -44,6 +44,19 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// Bounded wait used while unwinding: ignores the abort flag so that copies
+// and MMAs already in flight land before the CTA releases its shared and
+// tensor memory.  Gives up silently after `limit` cycles.
+__device__ __forceinline__ bool drain_bar(uint32_t bar, uint32_t parity,
+                                          long long limit = 1ll << 26) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (clock64() - t0 <= limit) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  return false;
+}
+
 // Optional pipeline trace for performance work.  Off unless the library is
 // built with -DBSS_TRACE: then the roles of one chosen CTA record clock64()
 // timestamps of their pipeline events into trace[role * kTraceEvents + i]
@@ -98,7 +111,8 @@ struct FwdParams {
   const int* row_ptr;
   const int* col_idx;
   int n_qblk, nnz;
-  int n_pairs;             // CTAs along x: ceil(Lq / 256)
+  int n_pairs;             // query-row pairs per head: ceil(Lq / 256)
+  int n_items;             // work items (= CTAs launched): B * H * n_pairs
   int* err;
   long long* trace;        // trace builds only (nullptr otherwise)
   int trace_cta;

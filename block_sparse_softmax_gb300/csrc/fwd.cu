@@ -8,13 +8,18 @@
 // running state (m, l, A) and discarded, so S and P never reach HBM.
 //
 // How it is laid out on the SM (a GB300 design, not the pages' Triton one):
-//   * one CTA owns TWO consecutive 128-row query tiles of one (b, h) that share
-//     a single K/V stream: each K/V tile is loaded once for 256 query rows;
+//   * a work item is TWO consecutive 128-row query tiles of one (b, h) that
+//     share a single K/V stream: each K/V tile is loaded once for 256 rows;
+//   * the kernel is persistent: one CTA per SM takes item after item, handed
+//     out greedily by the hardware's cluster launch control (the CTA cancels a
+//     not-yet-started CTA of the grid and does its item), so set-up is paid
+//     once and one item's epilogue overlaps the next item's loads and MMAs;
 //   * warp 0 issues TMA loads (128-byte swizzled boxes of 128 rows x 64 d) into
-//     a ring of K and V stages; warp 1 (one thread) issues every tcgen05.mma;
-//     warpgroups 1 and 2 (warps 4-7, 8-11) run the online softmax of tile 0
-//     and tile 1, one thread per query row (TMEM lane = row), with a larger
-//     register budget handed over from warpgroup 0 (setmaxnreg);
+//     a ring of K and V stages and schedules items; warp 1 (one thread) issues
+//     every tcgen05.mma; warpgroups 1 and 2 (warps 4-7, 8-11) run the online
+//     softmax and the epilogue of tile 0 and tile 1, one thread per query row
+//     (TMEM lane = row), with a larger register budget handed over from
+//     warpgroup 0 (setmaxnreg);
 //   * TMEM (512 columns): S0 | S1 | O0 | O1.  S = Q K^T is written by an SS
 //     MMA; the softmax warpgroup reads its row, writes P (bf16) back into the
 //     upper half of the same S columns, and P V accumulates into O by a TS MMA
@@ -46,42 +51,107 @@ struct FwdCfg {
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kStagesK * kTileBytes;
   static constexpr int kBarOff = kVOff + kStagesV * kTileBytes;
-  // q_full[2] k_full[SK] k_empty[SK] v_full[SV] v_empty[SV] s_full[2] p_full[2] o_full[2] mma_done
+  // q_full[2] q_empty[2] k_full[SK] k_empty[SK] v_full[SV] v_empty[SV] s_full[2]
+  // p_full[2] o_full[2] o_empty[2] item_full[2] item_empty[2] clc mma_done
   static constexpr int kBarQFull = 0;
-  static constexpr int kBarKFull = 2;
+  static constexpr int kBarQEmpty = 2;
+  static constexpr int kBarKFull = 4;
   static constexpr int kBarKEmpty = kBarKFull + kStagesK;
   static constexpr int kBarVFull = kBarKEmpty + kStagesK;
   static constexpr int kBarVEmpty = kBarVFull + kStagesV;
   static constexpr int kBarSFull = kBarVEmpty + kStagesV;
   static constexpr int kBarPFull = kBarSFull + 2;
   static constexpr int kBarOFull = kBarPFull + 2;
-  static constexpr int kBarMmaDone = kBarOFull + 2;
+  static constexpr int kBarOEmpty = kBarOFull + 2;
+  static constexpr int kBarItemFull = kBarOEmpty + 2;
+  static constexpr int kBarItemEmpty = kBarItemFull + 2;
+  static constexpr int kBarClc = kBarItemEmpty + 2;
+  static constexpr int kBarMmaDone = kBarClc + 1;
   static constexpr int kNumBars = kBarMmaDone + 1;
-  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  // 16-byte aligned: cancel answer (16) | TMEM base | abort flag | next item [2]
+  static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;
+  static constexpr int kClcOff = kMiscOff;
+  static constexpr int kTmemSlotOff = kMiscOff + 16;
+  static constexpr int kAbortOff = kMiscOff + 20;
+  static constexpr int kNextItemOff = kMiscOff + 24;
   static constexpr int kBitmapWords = kMaxKBlocks / 32;
-  static constexpr int kBitmapOff = kMiscOff + 16;
+  static constexpr int kBitmapOff = kMiscOff + 32;
   static constexpr int kSmemBytes = kBitmapOff + 2 * kBitmapWords * 4 + 1024;
+  static_assert(kSmemBytes <= 232448, "forward shared memory exceeds the 227 KB a CTA may use");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;                      // S_t at t*128
   static constexpr uint32_t kColP = 64;                     // P_t at S_t + 64 (bf16 pairs)
   static constexpr uint32_t kColO = 256;                    // O_t at 256 + t*D
   static constexpr int kThreads = 384;
-  // Register split per warpgroup (setmaxnreg): warpgroup 0 (TMA, MMA, two idle
-  // warps) keeps kRegsLow, the two softmax warpgroups get kRegsHigh.  Each SM
-  // sub-partition holds one warp of every warpgroup: 88 + 2 * 200 = 488 <= 512
-  // registers per lane there, and the whole split 128*88 + 256*200 = 62464 fits
-  // the 384 * R registers the launch holds for any ptxas assignment R >= 163
-  // (the build asserts R = 168).
-  static constexpr uint32_t kRegsLow = 88;
-  static constexpr uint32_t kRegsHigh = 200;
+  // Readers of each next-item slot: the MMA thread and one lane of each of the
+  // eight softmax warps.
+  static constexpr int kItemReaders = 1 + 8;
 };
 
-// The ordered list of key blocks this CTA visits and which of its two tiles
+// Register split per warpgroup (setmaxnreg): warpgroup 0 (TMA and scheduler,
+// MMA, two idle warps) gets kLow registers a thread, the two softmax warpgroups
+// kHigh.  Each SM sub-partition holds one warp of every warpgroup, so
+// kLow + 2 kHigh must stay within its 512 registers a lane, and the whole
+// split within the 384 * 168 registers the launch holds (launch_one refuses
+// to launch if ptxas gave the kernel fewer than 168 a thread, which would
+// leave setmaxnreg.inc waiting for registers that never come).  The
+// block-sparse schedule needs more registers in warpgroup 0.
+template <bool SPARSE>
+struct FwdRegs {
+  static constexpr uint32_t kLow = SPARSE ? 152 : 136;
+  static constexpr uint32_t kHigh = SPARSE ? 176 : 184;
+  static constexpr int kLaunchRegs = 168;
+  static_assert(kLow + 2 * kHigh <= 512, "register split exceeds an SM sub-partition");
+  static_assert(128 * kLow + 256 * kHigh <= 384 * kLaunchRegs, "register split exceeds the launch");
+};
+
+// One work item: two consecutive 128-row query tiles of one (b, h), which
+// share a single K/V stream.  Items are numbered row-pair-major with every
+// head of a pair side by side; under a causal mask the last pair (whose rows
+// see the most keys) comes first, so that the longest items start first.
+struct FwdItem {
+  int b, h, bh;
+  int r0[2];       // first query row of each tile
+  int kbmax[2];    // last key block each tile can see (-1: none)
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ FwdItem fwd_item(int item, const FwdParams& p) {
+  FwdItem it;
+  const int BH = p.B * p.H;
+  const int rank = item / BH;
+  it.bh = item - rank * BH;
+  it.b = it.bh / p.H;
+  it.h = it.bh - it.b * p.H;
+  const int pair = CAUSAL ? (p.n_pairs - 1 - rank) : rank;
+  it.r0[0] = pair * 2 * kTileM;
+  it.r0[1] = it.r0[0] + kTileM;
+  const int nk = (p.Lk + kTileN - 1) / kTileN;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    if (it.r0[t] >= p.Lq) {
+      it.kbmax[t] = -1;
+    } else if (CAUSAL) {
+      const long long r_last = min(it.r0[t] + kTileM - 1, p.Lq - 1);
+      const long long lim = r_last + p.q_offset - p.k_offset;
+      it.kbmax[t] = lim < 0 ? -1 : static_cast<int>(lim / kTileN < nk - 1 ? lim / kTileN : nk - 1);
+    } else {
+      it.kbmax[t] = nk - 1;
+    }
+  }
+  return it;
+}
+
+// The ordered list of key blocks an item visits and which of its two tiles
 // takes part in each.  Every role walks it identically.
 struct Schedule {
   int kbmax0, kbmax1;          // last block a tile can see (-1: none)
   const uint32_t* bm0;         // block-sparse bitmaps (nullptr: dense prefix)
   const uint32_t* bm1;
+
+  __device__ __forceinline__ Schedule(const FwdItem& it, const uint32_t* bitmap, int words)
+      : kbmax0(it.kbmax[0]), kbmax1(it.kbmax[1]), bm0(bitmap),
+        bm1(bitmap ? bitmap + words : nullptr) {}
 
   __device__ __forceinline__ int member(int kb) const {
     int m = 0;
@@ -107,8 +177,74 @@ struct Schedule {
     }
     return -1;
   }
+  // The last block tile t computes (-1: none).
+  __device__ __forceinline__ int last(int t) const {
+    const int lim = t ? kbmax1 : kbmax0;
+    const uint32_t* bm = t ? bm1 : bm0;
+    if (bm == nullptr || lim < 0) return lim;
+    for (int w = lim >> 5; w >= 0; --w) {
+      uint32_t bits = bm[w];
+      if (w == (lim >> 5)) bits &= (2u << (lim & 31)) - 1u;
+      if (bits) return (w << 5) + 31 - __clz(bits);
+    }
+    return -1;
+  }
 };
 
+// Row-per-thread to line-coalesced stores.  In the epilogue lane l of a warp
+// holds row l of the warp's 32 rows; a store of 16 bytes per lane would touch
+// 32 cache lines per instruction.  An in-register 8x8 transpose of 16-byte
+// segments inside each lane octet (8g..8g+7) turns that around: before it,
+// lane 8g+i holds segments 0..7 (v[4s..4s+3]) of one 128-byte line of its own
+// row; after it, the same lane holds segment i of that line of rows 8g+0..7
+// (row 8g+k at v[4k..4k+3]).  Each of the three butterfly stages swaps one
+// bit between the row and the segment index.
+__device__ __forceinline__ void transpose_octets(uint32_t (&v)[32], int lane) {
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      if (s & m) continue;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t a = v[4 * s + r];
+        const uint32_t b = v[4 * (s | m) + r];
+        const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, hi ? a : b, m);
+        v[4 * s + r] = hi ? recv : a;
+        v[4 * (s | m) + r] = hi ? b : recv;
+      }
+    }
+  }
+}
+
+// Store one 128-byte line per row for the warp's 32 rows after
+// transpose_octets: each instruction writes 4 whole lines.  `base` points at
+// byte `line_off` of the warp's first row, rows are `row_bytes` apart, and
+// only rows whose bit is set in `valid` are written.
+__device__ __forceinline__ void store_octet_lines(const uint32_t (&v)[32], uint8_t* base,
+                                                  size_t row_bytes, uint32_t valid, int lane) {
+  const int g = lane >> 3;
+  const int i = lane & 7;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int r = 8 * g + k;
+    if ((valid >> r) & 1u)
+      *reinterpret_cast<uint4*>(base + r * row_bytes + 16 * i) =
+          make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  }
+}
+
+// Persistent over work items.  The grid holds one CTA per item, but a running
+// CTA does not exit after its own item: when its producer has issued the loads
+// of an item's last key block it asks the hardware (cluster launch control) to
+// cancel a CTA that has not started yet and takes over that CTA's item.  So
+// one CTA per SM streams item after item, with set-up paid once, the next
+// item's Q and K loads and S = Q K^T overlapping the previous item's epilogue,
+// and the items handed out greedily in order (longest first under a causal
+// mask).  The producer passes each next item index to the other roles through
+// a two-slot ring in shared memory.  A block-sparse launch runs one item per
+// CTA (its bitmaps are built per item at set-up).
 template <int D, bool CAUSAL, bool SPARSE, bool PARTIAL>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -120,69 +256,33 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bars = sbase + C::kBarOff;
   auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
-  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::kMiscOff);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + C::kTmemSlotOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
+  volatile int* next_item = reinterpret_cast<volatile int*>(smem + C::kNextItemOff);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + C::kBitmapOff);
+  const uint32_t* sched_bm = SPARSE ? bitmap : nullptr;
 
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
   const int tid = static_cast<int>(threadIdx.x);
-  const bool tr = BSS_TRACE_ON(p, blockIdx.y * gridDim.x + blockIdx.x);
+  const bool tr = BSS_TRACE_ON(p, blockIdx.x);
   (void)tr;
   // A launch whose earlier CTAs already timed out stops at once instead of
   // timing out CTA by CTA.
   if (*reinterpret_cast<volatile int*>(p.err) == ATTN_ERR_TIMEOUT) return;
 
-  const int bh = blockIdx.x;
-  const int b = bh / p.H;
-  const int h = bh - b * p.H;
-  const int pair = CAUSAL ? (p.n_pairs - 1 - static_cast<int>(blockIdx.y)) : static_cast<int>(blockIdx.y);
-  const int r0_0 = pair * 2 * kTileM;
-  const int r0[2] = {r0_0, r0_0 + kTileM};
-  const int nk = (p.Lk + kTileN - 1) / kTileN;
-
-  // Last key block each tile can see.
-  int kbmax[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    if (r0[t] >= p.Lq) {
-      kbmax[t] = -1;
-    } else if (CAUSAL) {
-      const long long r_last = min(r0[t] + kTileM - 1, p.Lq - 1);
-      const long long lim = r_last + p.q_offset - p.k_offset;
-      kbmax[t] = lim < 0 ? -1 : static_cast<int>(lim / kTileN < nk - 1 ? lim / kTileN : nk - 1);
-    } else {
-      kbmax[t] = nk - 1;
-    }
-  }
-
-  // A dense-mode CTA whose rows see no key (all rows before a chunk's first
-  // key, or past the end) writes the empty state of its rows and leaves
-  // without setting anything up.
-  if (!SPARSE && kbmax[0] < 0 && kbmax[1] < 0) {
-    const float NEG_INF = -__int_as_float(0x7f800000);
-    const int nrows = max(0, min(2 * kTileM, p.Lq - r0[0]));
-    const size_t row0 = static_cast<size_t>(bh) * p.Lq + r0[0];
-    for (int r = tid; r < nrows; r += C::kThreads) {
-      if (PARTIAL) {
-        p.m_out[row0 + r] = NEG_INF;
-        p.l_out[row0 + r] = 0.f;
-      } else {
-        p.lse[row0 + r] = NEG_INF;
-      }
-    }
-    if (!PARTIAL) {
-      uint4* o4 = reinterpret_cast<uint4*>(p.o + row0 * D);
-      const int n16 = nrows * D / 8;
-      for (int x = tid; x < n16; x += C::kThreads) o4[x] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    return;
-  }
-
   // ---- set-up: barriers, tensor memory, block-sparse bitmaps -------------
   if (tid == 0) {
-    mbar_init(bar(C::kBarQFull + 0), 1);
-    mbar_init(bar(C::kBarQFull + 1), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kBarQFull + t), 1);
+      mbar_init(bar(C::kBarQEmpty + t), 1);
+      mbar_init(bar(C::kBarSFull + t), 1);
+      mbar_init(bar(C::kBarPFull + t), 4 * 32);
+      mbar_init(bar(C::kBarOFull + t), 1);
+      mbar_init(bar(C::kBarOEmpty + t), 4 * 32);
+      mbar_init(bar(C::kBarItemFull + t), 1);
+      mbar_init(bar(C::kBarItemEmpty + t), C::kItemReaders);
+    }
     for (int s = 0; s < C::kStagesK; ++s) {
       mbar_init(bar(C::kBarKFull + s), 1);
       mbar_init(bar(C::kBarKEmpty + s), 1);
@@ -191,27 +291,25 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::kBarVFull + s), 1);
       mbar_init(bar(C::kBarVEmpty + s), 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(bar(C::kBarSFull + t), 1);
-      mbar_init(bar(C::kBarPFull + t), 4 * 32);
-      mbar_init(bar(C::kBarOFull + t), 1);
-    }
+    mbar_init(bar(C::kBarClc), 1);
     mbar_init(bar(C::kBarMmaDone), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0) {
-    tmem_alloc(sbase + C::kMiscOff, C::kTmemCols);
+    tmem_alloc(sbase + C::kTmemSlotOff, C::kTmemCols);
     tmem_relinquish();
   }
   BSS_TRACE_EV(p, tr && tid == 0, 6, 0);
   if (SPARSE) {
+    const FwdItem it0 = fwd_item<CAUSAL>(blockIdx.x, p);
+    const int nk = (p.Lk + kTileN - 1) / kTileN;
     for (int i = tid; i < 2 * C::kBitmapWords; i += C::kThreads) bitmap[i] = 0u;
     __syncthreads();
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const int qb = r0[t] / kTileM;
-      if (r0[t] >= p.Lq || qb >= p.n_qblk) continue;
+      const int qb = it0.r0[t] / kTileM;
+      if (it0.r0[t] >= p.Lq || qb >= p.n_qblk) continue;
       const int beg = __ldg(p.row_ptr + qb);
       const int end = __ldg(p.row_ptr + qb + 1);
       if (beg < 0 || end < beg || end > p.nnz) {
@@ -233,306 +331,426 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  Schedule sch;
-  sch.kbmax0 = kbmax[0];
-  sch.kbmax1 = kbmax[1];
-  sch.bm0 = SPARSE ? bitmap : nullptr;
-  sch.bm1 = SPARSE ? bitmap + C::kBitmapWords : nullptr;
-
   if (warp < 4) {
-  regs_dec<C::kRegsLow>();
+  regs_dec<FwdRegs<SPARSE>::kLow>();
   if (warp == 0) {
-    // =================== TMA producer ===================
+    // =================== TMA producer and item scheduler ===================
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      bool qloaded[2] = {false, false};
-      int i = 0;
+      int item = static_cast<int>(blockIdx.x);
+      int n = 0;              // items finished
+      int ik = 0, iv = 0;     // K and V tiles loaded (over all items)
+      int qn[2] = {0, 0};     // Q tiles loaded into each tile slot
+      int clc_k = 0;          // cancel requests answered
+      bool clc_live = !SPARSE;
+      bool clc_out = false;   // a cancel request is in flight
       bool ok = true;
-      for (int kb = sch.next(-1); kb >= 0 && ok; kb = sch.next(kb), ++i) {
-        const int mask = sch.member(kb);
+      auto request_item = [&]() {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar(C::kBarClc), 16);
+        clc_try_cancel(sbase + C::kClcOff, bar(C::kBarClc));
+        clc_out = true;
+      };
+      while (ok) {
+        const FwdItem it = fwd_item<CAUSAL>(item, p);
+        const Schedule sch(it, sched_bm, C::kBitmapWords);
+        bool qloaded[2] = {false, false};
+        for (int kb = sch.next(-1); kb >= 0;) {
+          const int nkb = sch.next(kb);
+          // The next item is asked for as this item's last block is loaded.
+          if (nkb < 0 && clc_live) request_item();
+          const int mask = sch.member(kb);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (((mask >> t) & 1) && !qloaded[t]) {
-            const uint32_t qs = sbase + C::kQOff + t * C::kTileBytes;
-            mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
+          for (int t = 0; t < 2; ++t) {
+            if (((mask >> t) & 1) && !qloaded[t] && ok) {
+              if (qn[t] > 0 &&
+                  !wait_bar(bar(C::kBarQEmpty + t), (qn[t] - 1) & 1, abort_flag, p.err)) {
+                ok = false;
+                break;
+              }
+              const uint32_t qs = sbase + C::kQOff + t * C::kTileBytes;
+              mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
 #pragma unroll
-            for (int c = 0; c < C::kChunks; ++c)
-              tma_load_4d(qs + c * C::kChunkBytes, &tmQ, bar(C::kBarQFull + t), c * 64, r0[t], h, b);
-            qloaded[t] = true;
+              for (int c = 0; c < C::kChunks; ++c)
+                tma_load_4d(qs + c * C::kChunkBytes, &tmQ, bar(C::kBarQFull + t), c * 64, it.r0[t],
+                            it.h, it.b);
+              ++qn[t];
+              qloaded[t] = true;
+            }
+          }
+          if (!ok) break;
+          const int sk = ik % C::kStagesK;
+          if (ik >= C::kStagesK &&
+              !wait_bar(bar(C::kBarKEmpty + sk), ((ik / C::kStagesK) & 1) ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          BSS_TRACE_EV(p, tr, 0, 2 * ik);
+          const uint32_t ks = sbase + C::kKOff + sk * C::kTileBytes;
+          mbar_arrive_expect_tx(bar(C::kBarKFull + sk), C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(ks + c * C::kChunkBytes, &tmK, bar(C::kBarKFull + sk), c * 64, kb * kTileN,
+                        it.h, it.b);
+          ++ik;
+          const int sv = iv % C::kStagesV;
+          if (iv >= C::kStagesV &&
+              !wait_bar(bar(C::kBarVEmpty + sv), ((iv / C::kStagesV) & 1) ^ 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          BSS_TRACE_EV(p, tr, 0, 2 * iv + 1);
+          const uint32_t vs = sbase + C::kVOff + sv * C::kTileBytes;
+          mbar_arrive_expect_tx(bar(C::kBarVFull + sv), C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(vs + c * C::kChunkBytes, &tmV, bar(C::kBarVFull + sv), c * 64, kb * kTileN,
+                        it.h, it.b);
+          ++iv;
+          kb = nkb;
+        }
+        if (!ok) break;
+        if (clc_live && !clc_out) request_item();   // an item without blocks
+        int next = -1;
+        if (clc_out) {
+          if (!wait_bar(bar(C::kBarClc), clc_k & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          clc_out = false;
+          ++clc_k;
+          int x = -1;
+          if (clc_query(sbase + C::kClcOff, x)) {
+            if (x >= 0 && x < p.n_items) {
+              next = x;
+            } else {
+              record_error(p.err, ATTN_ERR_CUDA);   // not an index of this grid
+              clc_live = false;
+            }
+          } else {
+            clc_live = false;                        // nothing left to take
           }
         }
-        const int sk = i % C::kStagesK;
-        if (i >= C::kStagesK &&
-            !wait_bar(bar(C::kBarKEmpty + sk), ((i / C::kStagesK) & 1) ^ 1, abort_flag, p.err)) {
+        const int s = n & 1;
+        if (n >= 2 &&
+            !wait_bar(bar(C::kBarItemEmpty + s), ((n >> 1) & 1) ^ 1, abort_flag, p.err)) {
           ok = false;
           break;
         }
-        BSS_TRACE_EV(p, tr, 0, 2 * i);
-        const uint32_t ks = sbase + C::kKOff + sk * C::kTileBytes;
-        mbar_arrive_expect_tx(bar(C::kBarKFull + sk), C::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(ks + c * C::kChunkBytes, &tmK, bar(C::kBarKFull + sk), c * 64, kb * kTileN, h, b);
-        const int sv = i % C::kStagesV;
-        if (i >= C::kStagesV &&
-            !wait_bar(bar(C::kBarVEmpty + sv), ((i / C::kStagesV) & 1) ^ 1, abort_flag, p.err)) {
-          ++i;  // the K load of this step is in flight
-          ok = false;
-          break;
-        }
-        BSS_TRACE_EV(p, tr, 0, 2 * i + 1);
-        const uint32_t vs = sbase + C::kVOff + sv * C::kTileBytes;
-        mbar_arrive_expect_tx(bar(C::kBarVFull + sv), C::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(vs + c * C::kChunkBytes, &tmV, bar(C::kBarVFull + sv), c * 64, kb * kTileN, h, b);
+        next_item[s] = next;
+        mbar_arrive(bar(C::kBarItemFull + s));
+        ++n;
+        if (next < 0) break;
+        item = next;
       }
-      // Drain: every load issued has landed before the CTA may exit (in the
+      // Drain: every copy issued has landed before the CTA may exit (on the
       // normal path these waits return at once).
-      const long long drain = 1ll << 26;
-      for (int j = max(0, i - C::kStagesK); j < i; ++j)
-        wait_bar(bar(C::kBarKFull + j % C::kStagesK), (j / C::kStagesK) & 1, abort_flag, p.err, drain);
-      for (int j = max(0, i - C::kStagesV); j < i; ++j)
-        wait_bar(bar(C::kBarVFull + j % C::kStagesV), (j / C::kStagesV) & 1, abort_flag, p.err, drain);
+      for (int j = max(0, ik - C::kStagesK); j < ik; ++j)
+        drain_bar(bar(C::kBarKFull + j % C::kStagesK), (j / C::kStagesK) & 1);
+      for (int j = max(0, iv - C::kStagesV); j < iv; ++j)
+        drain_bar(bar(C::kBarVFull + j % C::kStagesV), (j / C::kStagesV) & 1);
       for (int t = 0; t < 2; ++t)
-        if (qloaded[t]) wait_bar(bar(C::kBarQFull + t), 0, abort_flag, p.err, drain);
+        if (qn[t] > 0) drain_bar(bar(C::kBarQFull + t), (qn[t] - 1) & 1);
+      if (clc_out) drain_bar(bar(C::kBarClc), clc_k & 1);
     }
   } else if (warp == 1) {
     // =================== MMA issuer (one thread) ===================
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(kTileM, kTileN, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileM, D, false, true);
-      bool qready[2] = {false, false};
-      bool ostarted[2] = {false, false};
-      int pcount[2] = {0, 0};
+      int item = static_cast<int>(blockIdx.x);
+      int n = 0;                // items finished
+      int i = 0;                // key blocks consumed (over all items)
+      int qn[2] = {0, 0};       // Q tiles consumed per tile slot
+      int pcount[2] = {0, 0};   // P tiles consumed per tile
+      int on[2] = {0, 0};       // O accumulations handed to the epilogue per tile
       bool ok = true;
+      while (ok) {
+        const FwdItem it = fwd_item<CAUSAL>(item, p);
+        const Schedule sch(it, sched_bm, C::kBitmapWords);
+        const int lastkb[2] = {sch.last(0), sch.last(1)};
+        bool qready[2] = {false, false};
+        bool ostarted[2] = {false, false};
 
-      auto issue_qk = [&](int t, int sk) -> bool {
-        if (!qready[t]) {
-          if (!wait_bar(bar(C::kBarQFull + t), 0, abort_flag, p.err)) return false;
-          qready[t] = true;
-        }
-        const uint32_t qa = sbase + C::kQOff + t * C::kTileBytes;
-        const uint32_t ka = sbase + C::kKOff + sk * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + C::kColS + t * 128, sdesc_sw128(qa + off, 16, 1024),
-                 sdesc_sw128(ka + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(bar(C::kBarSFull + t));
-        return true;
-      };
-      auto issue_pv = [&](int t, int sv) {
-        const uint32_t va = sbase + C::kVOff + sv * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kTileN / 16; ++kk) {
-          mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * 128 + C::kColP + kk * 8,
-                 sdesc_sw128(va + kk * 16 * 128, C::kChunkBytes, 1024), kIdescPV,
-                 (ostarted[t] || kk > 0) ? 1u : 0u);
-        }
-        ostarted[t] = true;
-      };
-
-      int kb = sch.next(-1);
-      int mask = kb >= 0 ? sch.member(kb) : 0;
-      if (kb >= 0) {
-        ok = wait_bar(bar(C::kBarKFull + 0), 0, abort_flag, p.err);
-        if (ok) {
-          tc_fence_after();
-          for (int t = 0; t < 2 && ok; ++t)
-            if ((mask >> t) & 1) ok = issue_qk(t, 0);
-          mma_commit(bar(C::kBarKEmpty + 0));
-        }
-      }
-      int i = 0;
-      while (kb >= 0 && ok) {
-        const int nkb = sch.next(kb);
-        const int nmask = nkb >= 0 ? sch.member(nkb) : 0;
-        const int sv = i % C::kStagesV;
-        const int skn = (i + 1) % C::kStagesK;
-        if (!wait_bar(bar(C::kBarVFull + sv), (i / C::kStagesV) & 1, abort_flag, p.err)) break;
-        BSS_TRACE_EV(p, tr, 1, 4 * i);
-        tc_fence_after();
-        bool kready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if ((mask >> t) & 1) {
-            if (!wait_bar(bar(C::kBarPFull + t), pcount[t] & 1, abort_flag, p.err)) {
-              ok = false;
-              break;
-            }
-            ++pcount[t];
-            BSS_TRACE_EV(p, tr, 1, 4 * i + 1 + t);
-            tc_fence_after();
-            issue_pv(t, sv);
+        auto issue_qk = [&](int t, int sk, int kb) -> bool {
+          if (!qready[t]) {
+            if (!wait_bar(bar(C::kBarQFull + t), qn[t] & 1, abort_flag, p.err)) return false;
+            qready[t] = true;
           }
-          if ((nmask >> t) & 1) {
-            if (!kready) {
-              if (!wait_bar(bar(C::kBarKFull + skn), ((i + 1) / C::kStagesK) & 1, abort_flag, p.err)) {
+          const uint32_t qa = sbase + C::kQOff + t * C::kTileBytes;
+          const uint32_t ka = sbase + C::kKOff + sk * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+            mma_ss(tmem + C::kColS + t * 128, sdesc_sw128(qa + off, 16, 1024),
+                   sdesc_sw128(ka + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(bar(C::kBarSFull + t));
+          // Q of this tile is free for the next item once its last S lands.
+          if (kb == lastkb[t]) mma_commit(bar(C::kBarQEmpty + t));
+          return true;
+        };
+        auto issue_pv = [&](int t, int sv) -> bool {
+          if (!ostarted[t] && on[t] > 0) {
+            // O_t still holds the previous item's result until its epilogue read it
+            if (!wait_bar(bar(C::kBarOEmpty + t), (on[t] - 1) & 1, abort_flag, p.err)) return false;
+            tc_fence_after();
+          }
+          const uint32_t va = sbase + C::kVOff + sv * C::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < kTileN / 16; ++kk) {
+            mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * 128 + C::kColP + kk * 8,
+                   sdesc_sw128(va + kk * 16 * 128, C::kChunkBytes, 1024), kIdescPV,
+                   (ostarted[t] || kk > 0) ? 1u : 0u);
+          }
+          ostarted[t] = true;
+          return true;
+        };
+
+        int kb = sch.next(-1);
+        int mask = kb >= 0 ? sch.member(kb) : 0;
+        if (kb >= 0) {
+          const int sk = i % C::kStagesK;
+          ok = wait_bar(bar(C::kBarKFull + sk), (i / C::kStagesK) & 1, abort_flag, p.err);
+          if (ok) {
+            tc_fence_after();
+            for (int t = 0; t < 2 && ok; ++t)
+              if ((mask >> t) & 1) ok = issue_qk(t, sk, kb);
+            if (ok) mma_commit(bar(C::kBarKEmpty + sk));
+          }
+        }
+        while (kb >= 0 && ok) {
+          const int nkb = sch.next(kb);
+          const int nmask = nkb >= 0 ? sch.member(nkb) : 0;
+          const int sv = i % C::kStagesV;
+          const int skn = (i + 1) % C::kStagesK;
+          if (!wait_bar(bar(C::kBarVFull + sv), (i / C::kStagesV) & 1, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          BSS_TRACE_EV(p, tr, 1, 4 * i);
+          tc_fence_after();
+          bool kready = false;
+          for (int t = 0; t < 2 && ok; ++t) {
+            if ((mask >> t) & 1) {
+              if (!wait_bar(bar(C::kBarPFull + t), pcount[t] & 1, abort_flag, p.err)) {
                 ok = false;
                 break;
               }
+              ++pcount[t];
+              BSS_TRACE_EV(p, tr, 1, 4 * i + 1 + t);
               tc_fence_after();
-              kready = true;
+              if (!issue_pv(t, sv)) {
+                ok = false;
+                break;
+              }
             }
-            ok = issue_qk(t, skn);
+            if ((nmask >> t) & 1) {
+              if (!kready) {
+                if (!wait_bar(bar(C::kBarKFull + skn), ((i + 1) / C::kStagesK) & 1, abort_flag, p.err)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                kready = true;
+              }
+              ok = issue_qk(t, skn, nkb);
+            }
           }
+          if (!ok) break;
+          BSS_TRACE_EV(p, tr, 1, 4 * i + 3);
+          mma_commit(bar(C::kBarVEmpty + sv));
+          if (nkb >= 0) mma_commit(bar(C::kBarKEmpty + skn));
+          kb = nkb;
+          mask = nmask;
+          ++i;
         }
         if (!ok) break;
-        BSS_TRACE_EV(p, tr, 1, 4 * i + 3);
-        mma_commit(bar(C::kBarVEmpty + sv));
-        if (nkb >= 0) mma_commit(bar(C::kBarKEmpty + skn));
-        kb = nkb;
-        mask = nmask;
-        ++i;
+        for (int t = 0; t < 2; ++t) {
+          if (ostarted[t]) {
+            mma_commit(bar(C::kBarOFull + t));
+            ++on[t];
+          }
+          if (qready[t]) ++qn[t];
+        }
+        const int s = n & 1;
+        if (!wait_bar(bar(C::kBarItemFull + s), (n >> 1) & 1, abort_flag, p.err)) break;
+        const int next = next_item[s];
+        mbar_arrive(bar(C::kBarItemEmpty + s));
+        ++n;
+        if (next < 0) break;
+        item = next;
       }
-      for (int t = 0; t < 2; ++t)
-        if (ostarted[t]) mma_commit(bar(C::kBarOFull + t));
+      // every MMA issued has completed before tensor memory is released
       mma_commit(bar(C::kBarMmaDone));
-      wait_bar(bar(C::kBarMmaDone), 0, abort_flag, p.err);
+      drain_bar(bar(C::kBarMmaDone), 0);
     }
   }
   } else {
-    regs_inc<C::kRegsHigh>();
+    regs_inc<FwdRegs<SPARSE>::kHigh>();
     // =================== softmax warpgroups (warps 4-7: tile 0, 8-11: tile 1) ===================
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;                      // TMEM lane quarter of this warp
     const int row_in_tile = wq * 32 + lane;
-    const int row = r0[t] + row_in_tile;
     const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + C::kColS + t * 128;
     const uint32_t tP = tS + C::kColP;
     const uint32_t tO = tmem + lane_base + C::kColO + t * D;
     const float sl2 = p.scale_log2;
     const float NEG_INF = -__int_as_float(0x7f800000);
+    const bool trw = tr && lane == 0 && wq == 0;
+    (void)trw;
 
-    float m2 = NEG_INF;     // reference max (log2 units), moved only by > 8
-    float mt = NEG_INF;     // exact running max (log2 units)
-    float l = 0.f;
-    int cnt = 0;
+    int item = static_cast<int>(blockIdx.x);
+    int n = 0;          // items finished
+    int cnt = 0;        // S tiles consumed (over all items)
+    int on = 0;         // O accumulations read back
     bool ok = true;
-    for (int kb = sch.next(-1); kb >= 0; kb = sch.next(kb)) {
-      if (!((sch.member(kb) >> t) & 1)) continue;
-      if (!wait_bar(bar(C::kBarSFull + t), cnt & 1, abort_flag, p.err)) {
-        ok = false;
-        break;
-      }
-      const bool trw = tr && lane == 0 && wq == 0;
-      BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt);
-      tc_fence_after();
-      uint32_t s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+    while (ok) {
+      const FwdItem it = fwd_item<CAUSAL>(item, p);
+      const Schedule sch(it, sched_bm, C::kBitmapWords);
+      const int r0 = it.r0[t];
+      const int row = r0 + row_in_tile;
 
-      // element mask: only where the block crosses the diagonal or the end
-      const int kstart = kb * kTileN;
-      const bool edge = (kstart + kTileN > p.Lk) ||
-                        (CAUSAL && (static_cast<long long>(kstart) + kTileN - 1 + p.k_offset >
-                                    static_cast<long long>(r0[t]) + p.q_offset));
-      if (edge) {
-        long long lim = static_cast<long long>(p.Lk) - 1 - kstart;
-        if (CAUSAL) lim = min(lim, static_cast<long long>(row) + p.q_offset - p.k_offset - kstart);
-        const int jl = static_cast<int>(max(-1ll, min(127ll, lim)));
+      float m2 = NEG_INF;     // reference max (log2 units), moved only by > 8
+      float mt = NEG_INF;     // exact running max (log2 units)
+      float l = 0.f;
+      int ci = 0;             // blocks of this item
+      for (int kb = sch.next(-1); kb >= 0; kb = sch.next(kb)) {
+        if (!((sch.member(kb) >> t) & 1)) continue;
+        // warp-uniform outcome: the loads below are warp-collective
+        if (!__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarSFull + t), cnt & 1, abort_flag, p.err))) {
+          ok = false;
+          break;
+        }
+        BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt);
+        tc_fence_after();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + c * 32, s[c]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+
+        // element mask: only where the block crosses the diagonal or the end
+        const int kstart = kb * kTileN;
+        const bool edge = (kstart + kTileN > p.Lk) ||
+                          (CAUSAL && (static_cast<long long>(kstart) + kTileN - 1 + p.k_offset >
+                                      static_cast<long long>(r0) + p.q_offset));
+        if (edge) {
+          long long lim = static_cast<long long>(p.Lk) - 1 - kstart;
+          if (CAUSAL) lim = min(lim, static_cast<long long>(row) + p.q_offset - p.k_offset - kstart);
+          const int jl = static_cast<int>(max(-1ll, min(127ll, lim)));
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (c * 32 + j > jl) s[c][j] = __float_as_uint(NEG_INF);
+        }
+        // row max over 8 independent chains (short dependency chains)
+        float mx[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(s[0][u]);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c * 32 + j > jl) s[c][j] = __float_as_uint(NEG_INF);
-      }
-      // row max over 8 independent chains (short dependency chains)
-      float mx[8];
+          for (int j = (c == 0 ? 8 : 0); j < 32; j += 8)
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(s[0][u]);
+            for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(s[c][j + u]));
+        const float mblk = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+        BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt + 1);
+        mt = fmaxf(mt, mblk);
+        float alpha = 1.f;
+        bool moved = false;
+        if (mblk > m2 + 8.f) {
+          alpha = ex2(m2 - mblk);
+          m2 = mblk;
+          moved = true;
+        }
+        const float mu = (m2 == NEG_INF) ? 0.f : m2;
+        float rs[4];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+        for (int u = 0; u < 4; ++u) rs[u] = 0.f;
 #pragma unroll
-        for (int j = (c == 0 ? 8 : 0); j < 32; j += 8)
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(s[c][j + u]));
-      const float mblk =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
-      BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt + 1);
-      mt = fmaxf(mt, mblk);
-      float alpha = 1.f;
-      bool moved = false;
-      if (mblk > m2 + 8.f) {
-        alpha = ex2(m2 - mblk);
-        m2 = mblk;
-        moved = true;
-      }
-      const float mu = (m2 == NEG_INF) ? 0.f : m2;
-      float rs[4];
+          for (int c2 = 0; c2 < 2; ++c2) {
+            const int c = half * 2 + c2;
 #pragma unroll
-      for (int u = 0; u < 4; ++u) rs[u] = 0.f;
+            for (int j = 0; j < 32; j += 2) {
+              const float p0 = ex2(fmaf(__uint_as_float(s[c][j]), sl2, -mu));
+              const float p1 = ex2(fmaf(__uint_as_float(s[c][j + 1]), sl2, -mu));
+              rs[(j >> 1) & 3] += p0 + p1;
+              pk[c2 * 16 + j / 2] = pack_bf16(p0, p1);
+            }
+          }
+          tmem_st32(tP + half * 32, pk);
+        }
+        l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+        BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt + 2);
+        // rescale O when this row's reference max moved and O already holds data
+        const bool fix = moved && ci > 0;
+        if (__any_sync(0xFFFFFFFFu, fix)) {
+          const float a = fix ? alpha : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait(o);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int c = half * 2 + c2;
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(s[c][j]), sl2, -mu));
-            const float p1 = ex2(fmaf(__uint_as_float(s[c][j + 1]), sl2, -mu));
-            rs[(j >> 1) & 3] += p0 + p1;
-            pk[c2 * 16 + j / 2] = pack_bf16(p0, p1);
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * a);
+            tmem_st32(tO + c * 32, o);
           }
         }
-        tmem_st32(tP + half * 32, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::kBarPFull + t));
+        BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt + 3);
+        ++cnt;
+        ++ci;
       }
-      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
-      BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt + 2);
-      // rescale O when this row's reference max moved and O already holds data
-      const bool fix = moved && cnt > 0;
-      if (__any_sync(0xFFFFFFFFu, fix)) {
-        const float a = fix ? alpha : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * a);
-          tmem_st32(tO + c * 32, o);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(C::kBarPFull + t));
-      BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt + 3);
-      ++cnt;
-    }
+      if (!ok) break;
 
-    // ---- epilogue ----
-    if (ok && cnt > 0) {
-      ok = wait_bar(bar(C::kBarOFull + t), 0, abort_flag, p.err);
-      tc_fence_after();
-    }
-    BSS_TRACE_EV(p, tr && lane == 0 && wq == 0, 4 + t, 0);
-    if (ok) {
-      const bool inb = row < p.Lq;
-      const size_t row_g = static_cast<size_t>(bh) * p.Lq + (inb ? row : 0);
-      if (PARTIAL) {
-        // An empty state (m = -inf) is fully described by m and l; its acc row
-        // is not written (a merge never reads it).
-        const float factor = (mt == NEG_INF || cnt == 0) ? 0.f : ex2(m2 - mt);
-        float* dst = p.acc_out + row_g * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32 && cnt > 0; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait(o);
-          if (inb && mt != NEG_INF) {
+      // ---- epilogue: O_t is read out of TMEM at once and released to the
+      // next item's P V before the global stores ----
+      uint32_t o[D / 32][32];
+      if (ci > 0) {
+        if (!__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarOFull + t), on & 1, abort_flag, p.err))) break;
+        tc_fence_after();
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              float4 v4 = make_float4(__uint_as_float(o[j]) * factor, __uint_as_float(o[j + 1]) * factor,
-                                      __uint_as_float(o[j + 2]) * factor, __uint_as_float(o[j + 3]) * factor);
-              *reinterpret_cast<float4*>(dst + c * 32 + j) = v4;
-            }
+        for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, o[c]);
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
+        tc_fence_before();
+        mbar_arrive(bar(C::kBarOEmpty + t));
+        ++on;
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[c][j] = 0u;
+      }
+      BSS_TRACE_EV(p, trw, 4 + t, 2 * n);
+      const bool inb = row < p.Lq;
+      const size_t row_g = static_cast<size_t>(it.bh) * p.Lq + (inb ? row : 0);
+      // first row of this warp (rows past Lq are masked out of `valid`)
+      const size_t wrow0 = static_cast<size_t>(it.bh) * p.Lq + (r0 + wq * 32);
+      if (PARTIAL) {
+        // An empty state (m = -inf) is fully described by m and l; its acc
+        // row is not written (a merge never reads it).
+        const float factor = (mt == NEG_INF || ci == 0) ? 0.f : ex2(m2 - mt);
+        const uint32_t valid = __ballot_sync(0xFFFFFFFFu, inb && ci > 0 && mt != NEG_INF);
+        if (valid) {
+          uint8_t* base = reinterpret_cast<uint8_t*>(p.acc_out + wrow0 * D);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[c][j] = __float_as_uint(__uint_as_float(o[c][j]) * factor);
+            transpose_octets(o[c], lane);
+            store_octet_lines(o[c], base + c * 128, D * 4, valid, lane);
           }
         }
         if (inb) {
@@ -541,35 +759,37 @@ __global__ void __launch_bounds__(384, 1)
         }
       } else {
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* dst = p.o + row_g * D;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          if (cnt > 0) {
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait(o);
-          } else {
+        const uint32_t valid = __ballot_sync(0xFFFFFFFFu, inb);
+        uint8_t* base = reinterpret_cast<uint8_t*>(p.o + wrow0 * D);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = 0u;
-          }
-          if (inb) {
+        for (int g2 = 0; g2 < D / 64; ++g2) {
+          // line g2 of a row: columns 64 g2 .. 64 g2 + 63 as 32 bf16 pairs
+          uint32_t w[32];
 #pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-              uint4 w;
-              w.x = pack_bf16(__uint_as_float(o[j + 0]) * inv, __uint_as_float(o[j + 1]) * inv);
-              w.y = pack_bf16(__uint_as_float(o[j + 2]) * inv, __uint_as_float(o[j + 3]) * inv);
-              w.z = pack_bf16(__uint_as_float(o[j + 4]) * inv, __uint_as_float(o[j + 5]) * inv);
-              w.w = pack_bf16(__uint_as_float(o[j + 6]) * inv, __uint_as_float(o[j + 7]) * inv);
-              *reinterpret_cast<uint4*>(dst + c * 32 + j) = w;
-            }
+          for (int k = 0; k < 32; ++k) {
+            const int c = 2 * g2 + k / 16;
+            const int j = (2 * k) % 32;
+            w[k] = pack_bf16(__uint_as_float(o[c][j]) * inv, __uint_as_float(o[c][j + 1]) * inv);
           }
+          transpose_octets(w, lane);
+          store_octet_lines(w, base + g2 * 128, D * 2, valid, lane);
         }
         if (inb) p.lse[row_g] = l > 0.f ? (m2 + __log2f(l)) * kLn2 : NEG_INF;
       }
+      BSS_TRACE_EV(p, trw, 4 + t, 2 * n + 1);
+      // ---- next item ----
+      const int s = n & 1;
+      if (!__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarItemFull + s), (n >> 1) & 1, abort_flag, p.err)))
+        break;
+      const int next = next_item[s];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::kBarItemEmpty + s));
+      ++n;
+      if (next < 0) break;
+      item = next;
     }
   }
 
-  if (warp >= 4) BSS_TRACE_EV(p, tr && lane == 0 && (warp & 3) == 0, 4 + ((warp - 4) >> 2), 1);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -584,14 +804,21 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<D>;
   auto kern = attn_fwd_kernel<D, CAUSAL, SPARSE, PARTIAL>;
-  static bool configured = false;  // per-process; the attribute is per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  constexpr int kMaxDev = 64;
+  static bool configured[kMaxDev] = {};  // the attribute is per device and function
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    if (fa.numRegs < FwdRegs<SPARSE>::kLaunchRegs) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
-  dim3 grid(p.B * p.H, p.n_pairs);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, p);
+  kern<<<p.n_items, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 

@@ -45,6 +45,42 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // ----------------------------------------------------------------------------
+// Cluster launch control: work stealing between the CTAs of one grid
+// ----------------------------------------------------------------------------
+// Ask the hardware to cancel one CTA of this grid that has not started yet.
+// The 16-byte answer is written to shared memory at `resp` (16-byte aligned)
+// and completes `bar`, which must expect 16 transaction bytes.  After an
+// answer that cancelled nothing, no further request may be made.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128"
+      " [%0], [%1];" ::"r"(resp), "r"(bar)
+      : "memory");
+}
+// Read an answer: returns true and the cancelled CTA's x index when a CTA was
+// cancelled (its work now belongs to the caller), false when none was left.
+__device__ __forceinline__ bool clc_query(uint32_t resp, int& x) {
+  uint32_t cx, cy, cz, cw, ok;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t.reg .b64 lo, hi;\n\t"
+      "ld.shared.v2.b64 {lo, hi}, [%5];\n\t"
+      "mov.b128 r, {lo, hi};\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %4, 1, 0, p;\n\t"
+      "mov.u32 %0, 0;\n\tmov.u32 %1, 0;\n\tmov.u32 %2, 0;\n\tmov.u32 %3, 0;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%0, %1, %2, %3}, r;\n\t"
+      "}"
+      : "=r"(cx), "=r"(cy), "=r"(cz), "=r"(cw), "=r"(ok)
+      : "r"(resp)
+      : "memory");
+  (void)cy;
+  (void)cz;
+  (void)cw;
+  x = static_cast<int>(cx);
+  return ok != 0;
+}
+
+// ----------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), tile mode, completion on an mbarrier
 // ----------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

@@ -129,8 +129,7 @@ attn_status_t check_common(int B, int H, long long Lq, long long Lk, int d, floa
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * H > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
-  if ((Lq + 127) / 128 > 65535) return ATTN_ERR_UNSUPPORTED;   // grid y of the backward
-  if (static_cast<long long>(B) * H * ((Lq + 255) / 256) > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H * ((Lq + 127) / 128) > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
 
@@ -371,6 +370,16 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
+  // Heads launched together: about 2 groups run at once, each head holding
+  // Q, dO (bf16) and the dQ accumulator (fp32), 8 L d bytes; keep the pair of
+  // groups near 64 MiB, well inside L2.
+  {
+    const long long per_head = 8ll * L * d;
+    long long g = (64ll << 20) / (2 * per_head);
+    if (g < 1) g = 1;
+    if (g > static_cast<long long>(B) * H) g = static_cast<long long>(B) * H;
+    p.head_group = static_cast<int>(g);
+  }
 #ifdef BSS_TRACE
   p.trace = g_trace_buf;
   p.trace_cta = g_trace_cta;

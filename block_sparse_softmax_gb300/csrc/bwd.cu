@@ -13,17 +13,27 @@
 // Main kernel design (the KV-owned traversal of section 3, 'The ownership
 // conflict between dQ and dK, dV'): one CTA owns a 128-key tile of one (b, h)
 // and keeps K_j, V_j in shared memory and dK_j, dV_j accumulating in TMEM
-// while the query tiles stream past.  Everything is computed transposed
-// (TMEM lane = key), so that one thread owns one key row:
+// while the query tiles stream past.  Scores are computed transposed (TMEM
+// lane = key), so that one thread owns one key row:
 //   S^T  = K_j Q_i^T   and   dP^T = V_j dO_i^T         (SS MMAs, M = 128 keys)
-//   two warpgroups (64 query columns each) turn them into P^T and dS^T
-//   (bf16), written back into the lower halves of the same TMEM columns
-//   (tensor-memory A operands), and dS also into shared memory in the layout
-//   the dQ MMA reads;
-//   dV  += P^T dO_i,  dK += dS^T Q_i                   (TS MMAs)
-//   dQ_i = dS K_j     (SS, M = 128 queries, N = d) into S^T's columns once P^T
-//   has been consumed; four more warps stage it in shared memory and add it
-//   into the fp32 accumulator in global memory with bulk tensor reduce-adds.
+//   two warpgroups (64 query columns each) first turn S^T into P^T (bf16,
+//   written back into the lower halves of S^T's own columns as the
+//   tensor-memory A operand of dV), then, once dP^T is there, form dS and
+//   store it (bf16) in shared memory in the 128-byte-swizzled layout of a
+//   K-major tile with one key per row;
+//   dV  += P^T dO_i                                     (TS MMA)
+//   dK  += dS^T Q_i   (dS^T is that tile read K-major) (SS MMA)
+//   dQ_i = dS K_j     (the same tile read M-major)      (SS MMA, M = queries)
+//   four more warps move dQ_i out of TMEM through a shared staging buffer and
+//   add it into the fp32 accumulator in global memory with bulk tensor
+//   reduce-adds.
+// One thread issues every MMA, in the order
+//   dV(i), S^T(i+1), dQ(i), dK(i), dP^T(i+1)
+// so that the tensor core works on dV(i) and S^T(i+1) while dS(i) is formed
+// and on dK(i) while dQ(i) is drained: the chain that sets the pace is
+// dQ(i) -> drain -> dP^T(i+1) -> dS(i+1) -> dQ(i+1), and the other MMAs fill
+// its gaps.  dQ_i is written into dP^T's columns at d=128 (they are free once
+// dS(i) has been formed) and into columns of its own at d=64.
 // Causal: only query tiles i >= j are visited and the element mask is applied
 // on the diagonal tile and on the ragged tail.
 #include "common.cuh"
@@ -36,13 +46,13 @@ struct BwdCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = kTileM * 128;
   static constexpr int kTileBytes = kTileM * D * 2;
-  static constexpr int kStagesQ = 2;                     // Q_i ring depth
+  static constexpr int kStagesQ = 2;                     // Q_i ring depth (S^T(i+1) and dK(i) overlap)
   static constexpr int kStagesDO = (D == 128) ? 1 : 2;    // dO_i ring depth (room for dQ staging)
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
   static constexpr int kQOff = kVOff + kTileBytes;
   static constexpr int kDOOff = kQOff + kStagesQ * kTileBytes;
-  static constexpr int kDSOff = kDOOff + kStagesDO * kTileBytes;  // dS, 128 x 128 bf16
+  static constexpr int kDSOff = kDOOff + kStagesDO * kTileBytes;  // dS, 128 keys x 128 queries bf16
   static constexpr int kDSBytes = kTileM * kTileN * 2;
   static constexpr int kStageOff = kDSOff + kDSBytes;    // dQ staging: 128 rows x 64 fp32
   static constexpr int kStageBytes = kTileM * 64 * 4;
@@ -53,13 +63,15 @@ struct BwdCfg {
   static constexpr int kBarQEmpty = kBarQFull + kStagesQ;
   static constexpr int kBarDOFull = kBarQEmpty + kStagesQ;
   static constexpr int kBarDOEmpty = kBarDOFull + kStagesDO;
-  static constexpr int kBarSFull = kBarDOEmpty + kStagesDO;
-  static constexpr int kBarDSReady = kBarSFull + 1;
+  static constexpr int kBarSFull = kBarDOEmpty + kStagesDO;   // S^T of a query tile in TMEM
+  static constexpr int kBarDPFull = kBarSFull + 1;            // dP^T in TMEM
+  static constexpr int kBarPReady = kBarDPFull + 1;           // P^T written (S^T read)
+  static constexpr int kBarDSReady = kBarPReady + 1;          // dS in shared memory (dP^T read)
   static constexpr int kBarDQFull = kBarDSReady + 1;
   static constexpr int kBarDQFree = kBarDQFull + 1;
   static constexpr int kBarDKVFull = kBarDQFree + 1;
-  static constexpr int kBarMmaDone = kBarDKVFull + 1;  // [2], one per MMA issuer
-  static constexpr int kBarStat = kBarMmaDone + 2;     // [2]: LSE/D of a query tile staged
+  static constexpr int kBarMmaDone = kBarDKVFull + 1;
+  static constexpr int kBarStat = kBarMmaDone + 1;     // [2]: LSE/D of a query tile staged
   static constexpr int kBarStaged = kBarStat + 2;      // dQ round written to the staging buffer
   static constexpr int kBarStageFree = kBarStaged + 1; // staging buffer read by the reduce
   static constexpr int kNumBars = kBarStageFree + 1;
@@ -70,25 +82,39 @@ struct BwdCfg {
   static constexpr int kPayload = kMiscOff + 16;
   static constexpr int kSlack = (kPayload + 1024 <= 232448) ? 1024 : 232448 - kPayload;
   static constexpr int kSmemBytes = kPayload + kSlack;
+  static_assert(kPayload <= 232448, "backward shared memory exceeds the 227 KB a CTA may use");
   static constexpr uint32_t kTmemCols = 512;
   // TMEM columns: S^T (fp32) at [0,128) and dP^T at [128,256).  Half X of the
-  // P^T/dS^T warpgroups (query columns [64X, 64X+64)) writes its P^T (bf16
-  // pairs, 32 columns) to S^T columns [64X, 64X+32) and its dS^T to dP^T
-  // columns [64X, 64X+32): inside the range it has itself already read.  dV and
-  // dK follow.  dQ of a query tile has its own columns at d=64 ([384,448)); at
-  // d=128 it reuses S^T's columns, issued after the dV MMA that reads P^T.
+  // P^T/dS warpgroups (query columns [64X, 64X+64)) writes its P^T (bf16
+  // pairs, 32 columns) to S^T columns [64X, 64X+32), inside the range it has
+  // itself already read.  dV and dK follow.  dQ of a query tile takes dP^T's
+  // columns at d=128 and columns of its own, [384,448), at d=64.
   static constexpr uint32_t kColST = 0;
   static constexpr uint32_t kColDPT = 128;
   static constexpr uint32_t kColDV = 256;
   static constexpr uint32_t kColDK = 256 + D;
-  static constexpr uint32_t kColDQ = (D == 128) ? 0 : 384;
-  // A operand address of query k-step kk (16 queries) inside P^T / dS^T
+  static constexpr uint32_t kColDQ = (D == 128) ? kColDPT : 384;
+  static constexpr bool kDQOverDP = (kColDQ == kColDPT);
+  // A operand address of query k-step kk (16 queries) inside P^T
   static __device__ __forceinline__ uint32_t pcol(int kk) { return 64 * (kk >> 2) + 8 * (kk & 3); }
-  // Two MMA issuers pay off at d=64, where each MMA is short; at d=128 one
-  // issuer measured faster.
-  static constexpr bool kTwoIssuers = (D == 64);
-  static constexpr int kIssuers = kTwoIssuers ? 2 : 1;
-  static constexpr int kThreads = kTwoIssuers ? 512 : 448;
+  static constexpr int kThreads = 512;
+};
+
+// Register split per warpgroup (setmaxnreg): warpgroup 0 (TMA, MMA, two idle
+// warps) kLow, the P/dS warpgroups 1-2 kMid (each thread keeps 64 fp32 P
+// values between its two phases), the dQ warpgroup 3 kHigh.  Each SM
+// sub-partition holds one warp of every warpgroup: kLow + 2 kMid + kHigh <= 512
+// registers a lane, and the split fits the 512 * 128 registers the launch
+// holds (launch_main refuses to launch if ptxas gave the kernel fewer than 128
+// a thread).
+template <int D>
+struct BwdRegs {
+  static constexpr uint32_t kLow = 72;
+  static constexpr uint32_t kMid = 160;
+  static constexpr uint32_t kHigh = 120;
+  static constexpr uint32_t kLaunchRegs = 128;
+  static_assert(kLow + 2 * kMid + kHigh <= 512, "register split exceeds an SM sub-partition");
+  static_assert(128 * (kLow + 2 * kMid + kHigh) <= 512 * kLaunchRegs, "register split exceeds the launch");
 };
 
 template <int D, bool CAUSAL>
@@ -116,38 +142,46 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
   const int tid = static_cast<int>(threadIdx.x);
-  const bool tr = BSS_TRACE_ON(p, blockIdx.y * gridDim.x + blockIdx.x);
+  const bool tr = BSS_TRACE_ON(p, blockIdx.x);
   (void)tr;
   if (*reinterpret_cast<volatile int*>(p.err) == ATTN_ERR_TIMEOUT) return;
 
-  const int bh = blockIdx.x;
-  const int b = bh / p.H;
-  const int h = bh - b * p.H;
-  const int j = blockIdx.y;                       // key tile owned by this CTA
+  // CTA order: heads in groups of p.head_group, and inside a group key tile
+  // major (under a causal mask the first key tiles have the most query tiles,
+  // so they start first).  The CTAs running at any moment then belong to a
+  // few heads, whose Q, dO and fp32 dQ accumulator stay in L2, so the dQ
+  // reduce-adds are read-modify-writes in L2 rather than in DRAM.
   const int L = p.L;
   const int nq = (L + kTileM - 1) / kTileM;
+  const int BH = p.B * p.H;
+  const int grp = static_cast<int>(blockIdx.x) / (p.head_group * nq);
+  const int gsz = min(p.head_group, BH - grp * p.head_group);
+  const int within = static_cast<int>(blockIdx.x) - grp * p.head_group * nq;
+  const int j = within / gsz;                     // key tile owned by this CTA
+  const int bh = grp * p.head_group + (within - j * gsz);
+  const int b = bh / p.H;
+  const int h = bh - b * p.H;
   const int i0 = CAUSAL ? j : 0;                  // first query tile that sees these keys
   const int n_it = nq - i0;
 
   if (tid == 0) {
     mbar_init(bar(C::kBarKV), 1);
-    // Two MMA issuers: A (S^T, dV, dQ) and B (dP^T, dK); barriers that both
-    // release or fill count two arrivals.
     for (int s = 0; s < C::kStagesQ; ++s) {
       mbar_init(bar(C::kBarQFull + s), 1);
-      mbar_init(bar(C::kBarQEmpty + s), C::kIssuers);
+      mbar_init(bar(C::kBarQEmpty + s), 1);
     }
     for (int s = 0; s < C::kStagesDO; ++s) {
       mbar_init(bar(C::kBarDOFull + s), 1);
-      mbar_init(bar(C::kBarDOEmpty + s), C::kIssuers);
+      mbar_init(bar(C::kBarDOEmpty + s), 1);
     }
-    mbar_init(bar(C::kBarSFull), C::kIssuers);
+    mbar_init(bar(C::kBarSFull), 1);
+    mbar_init(bar(C::kBarDPFull), 1);
+    mbar_init(bar(C::kBarPReady), 256);
     mbar_init(bar(C::kBarDSReady), 256);
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQFree), 128);
-    mbar_init(bar(C::kBarDKVFull), C::kIssuers);
-    mbar_init(bar(C::kBarMmaDone + 0), 1);
-    mbar_init(bar(C::kBarMmaDone + 1), 1);
+    mbar_init(bar(C::kBarDKVFull), 1);
+    mbar_init(bar(C::kBarMmaDone), 1);
     mbar_init(bar(C::kBarStat + 0), 128);
     mbar_init(bar(C::kBarStat + 1), 128);
     mbar_init(bar(C::kBarStaged), 128);
@@ -164,6 +198,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < 4) {
+  regs_set<BwdRegs<D>::kLow, BwdRegs<D>::kLaunchRegs>();
   if (warp == 0) {
     // =================== TMA producer ===================
     if (lane == 0) {
@@ -197,126 +233,122 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         ++ndo_ld;
       }
       // Drain: every load issued has landed before the CTA may exit.
-      const long long drain = 1ll << 26;
-      wait_bar(bar(C::kBarKV), 0, abort_flag, p.err, drain);
+      drain_bar(bar(C::kBarKV), 0);
       for (int x = max(0, nq_ld - C::kStagesQ); x < nq_ld; ++x)
-        wait_bar(bar(C::kBarQFull + x % C::kStagesQ), (x / C::kStagesQ) & 1, abort_flag, p.err, drain);
+        drain_bar(bar(C::kBarQFull + x % C::kStagesQ), (x / C::kStagesQ) & 1);
       for (int x = max(0, ndo_ld - C::kStagesDO); x < ndo_ld; ++x)
-        wait_bar(bar(C::kBarDOFull + x % C::kStagesDO), (x / C::kStagesDO) & 1, abort_flag, p.err, drain);
+        drain_bar(bar(C::kBarDOFull + x % C::kStagesDO), (x / C::kStagesDO) & 1);
     }
-  } else if (warp == 1 || (C::kTwoIssuers && warp == 14)) {
-    // =================== MMA issuers ===================
-    // With two issuers, A (warp 1) issues S^T, dV, dQ and B (warp 14) issues
-    // dP^T, dK; with one, warp 1 issues everything.  Each issuer overwrites only
-    // TMEM columns that its own earlier MMAs read (S^T over P^T after dV, dQ
-    // over P^T after dV at d=128; dP^T over dS^T after dK), so issue order
-    // within one issuer keeps them safe.
+  } else if (warp == 1) {
+    // =================== MMA issuer (one thread) ===================
+    // Issue order per query tile i: dV(i), S^T(i+1), dQ(i), dK(i), dP^T(i+1).
+    // Every overwrite of TMEM or shared memory is ordered behind the MMAs that
+    // read the old contents by issue order (the tensor core executes one
+    // thread's MMAs in order) or by the barrier it waits on:
+    //   S^T(i+1) over P^T(i): after dV(i);  P^T(i+1) written after S^T(i+1)
+    //   completes; dQ(i) over dP^T(i): after ds_ready(i) (dP^T read);
+    //   dP^T(i+1) over dQ(i): after dq_free(i); dS(i+1) written after
+    //   dP^T(i+1) completes, so after dQ(i) and dK(i) read dS(i).
     if (lane == 0) {
-      const bool A = (warp == 1);
-      const bool doA = A;                          // S^T, dV, dQ
-      const bool doB = !A || !C::kTwoIssuers;      // dP^T, dK
       constexpr uint32_t kIdescT = idesc_bf16_f32(kTileM, kTileN, false, false);  // S^T, dP^T
       constexpr uint32_t kIdescKV = idesc_bf16_f32(kTileM, D, false, true);       // dV, dK
       constexpr uint32_t kIdescQ = idesc_bf16_f32(kTileM, D, true, true);         // dQ
-      bool ok = wait_bar(bar(C::kBarKV), 0, abort_flag, p.err);
       const uint32_t ka = sbase + C::kKOff, va = sbase + C::kVOff, dsa = sbase + C::kDSOff;
+      auto qaddr = [&](int it) { return sbase + C::kQOff + (it % C::kStagesQ) * C::kTileBytes; };
+      auto doaddr = [&](int it) { return sbase + C::kDOOff + (it % C::kStagesDO) * C::kTileBytes; };
+      // S^T(it) = K_j Q^T
+      auto issue_s = [&](int it) -> bool {
+        if (!wait_bar(bar(C::kBarQFull + it % C::kStagesQ), (it / C::kStagesQ) & 1, abort_flag, p.err))
+          return false;
+        tc_fence_after();
+        const uint32_t qa = qaddr(it);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::kColST, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
+                 kIdescT, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBarSFull));
+        return true;
+      };
+      // dP^T(it) = V_j dO^T
+      auto issue_dp = [&](int it) -> bool {
+        if (!wait_bar(bar(C::kBarDOFull + it % C::kStagesDO), (it / C::kStagesDO) & 1, abort_flag, p.err))
+          return false;
+        tc_fence_after();
+        const uint32_t doa = doaddr(it);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::kColDPT, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(doa + off, 16, 1024),
+                 kIdescT, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBarDPFull));
+        return true;
+      };
+      bool ok = wait_bar(bar(C::kBarKV), 0, abort_flag, p.err);
+      if (ok && n_it > 0) ok = issue_s(0) && issue_dp(0);
       for (int it = 0; it < n_it && ok; ++it) {
-        const int sq = it % C::kStagesQ;
-        const int sd = it % C::kStagesDO;
-        const uint32_t qa = sbase + C::kQOff + sq * C::kTileBytes;
-        const uint32_t doa = sbase + C::kDOOff + sd * C::kTileBytes;
-        if (doA) {
-          if (!wait_bar(bar(C::kBarQFull + sq), (it / C::kStagesQ) & 1, abort_flag, p.err)) break;
-          BSS_TRACE_EV(p, tr, 1, 5 * it);
-          // at d=128, S^T reuses the columns that held dQ of the previous tile
-          if (C::kColDQ == C::kColST && it > 0 &&
-              !wait_bar(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p.err))
-            break;
-          BSS_TRACE_EV(p, tr, 1, 5 * it + 1);
-          tc_fence_after();
+        // dV += P^T dO_i  (K dimension = the 128 queries)
+        if (!wait_bar(bar(C::kBarPReady), it & 1, abort_flag, p.err)) break;
+        BSS_TRACE_EV(p, tr, 1, 4 * it);
+        tc_fence_after();
+        const uint32_t doa = doaddr(it);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-            mma_ss(tmem + C::kColST, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
-                   kIdescT, kk > 0 ? 1u : 0u);
-          }
-          if (C::kTwoIssuers) {
-            mma_commit(bar(C::kBarSFull));
-            mma_commit(bar(C::kBarQEmpty + sq));
-          }
+        for (int kk = 0; kk < kTileM / 16; ++kk) {
+          mma_ts(tmem + C::kColDV, tmem + C::kColST + C::pcol(kk),
+                 sdesc_sw128(doa + kk * 2048, C::kChunkBytes, 1024), kIdescKV,
+                 (it > 0 || kk > 0) ? 1u : 0u);
         }
-        if (doB) {
-          if (!wait_bar(bar(C::kBarDOFull + sd), (it / C::kStagesDO) & 1, abort_flag, p.err)) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-            mma_ss(tmem + C::kColDPT, sdesc_sw128(va + off, 16, 1024),
-                   sdesc_sw128(doa + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(C::kBarSFull));
-          if (C::kTwoIssuers) mma_commit(bar(C::kBarDOEmpty + sd));
-        }
-        BSS_TRACE_EV(p, tr && A, 1, 5 * it + 2);
+        mma_commit(bar(C::kBarDOEmpty + it % C::kStagesDO));   // dP^T(it) and dV(it) read dO_i
+        if (it + 1 < n_it && !issue_s(it + 1)) break;
         // the P/dS warps run for a while: poll gently so that the issue slots
         // they share with this warp stay theirs
         if (!wait_bar_relaxed<64>(bar(C::kBarDSReady), it & 1, abort_flag, p.err)) break;
-        BSS_TRACE_EV(p, tr && A, 1, 5 * it + 3);
+        BSS_TRACE_EV(p, tr, 1, 4 * it + 1);
         tc_fence_after();
-        if (doA) {
-          // dV += P^T dO_i  (K dimension = the 128 queries)
-          if (C::kTwoIssuers &&
-              !wait_bar(bar(C::kBarDOFull + sd), (it / C::kStagesDO) & 1, abort_flag, p.err))
-            break;
-          tc_fence_after();
+        // dQ_i = dS K_j  (M = queries, N = d, K dimension = the 128 keys); with
+        // columns of its own, only after the previous dQ has been read
+        if (!C::kDQOverDP && it > 0 && !wait_bar(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p.err))
+          break;
 #pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk) {
-            mma_ts(tmem + C::kColDV, tmem + C::kColST + C::pcol(kk),
-                   sdesc_sw128(doa + kk * 2048, C::kChunkBytes, 1024), kIdescKV,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(C::kBarDOEmpty + sd));
+        for (int kk = 0; kk < kTileN / 16; ++kk) {
+          mma_ss(tmem + C::kColDQ, sdesc_sw128(dsa + kk * 2048, C::kChunkBytes, 1024),
+                 sdesc_sw128(ka + kk * 2048, C::kChunkBytes, 1024), kIdescQ, kk > 0 ? 1u : 0u);
         }
-        if (doB) {
-          // dK += dS^T Q_i
-          if (C::kTwoIssuers &&
-              !wait_bar(bar(C::kBarQFull + sq), (it / C::kStagesQ) & 1, abort_flag, p.err))
-            break;
-          tc_fence_after();
+        mma_commit(bar(C::kBarDQFull));
+        // dK += dS^T Q_i  (dS^T: the same tile read K-major; K dimension = queries)
+        const uint32_t qa = qaddr(it);
 #pragma unroll
-          for (int kk = 0; kk < kTileM / 16; ++kk) {
-            mma_ts(tmem + C::kColDK, tmem + C::kColDPT + C::pcol(kk),
-                   sdesc_sw128(qa + kk * 2048, C::kChunkBytes, 1024), kIdescKV,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(C::kBarQEmpty + sq));
+        for (int kk = 0; kk < kTileM / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::kColDK, sdesc_sw128(dsa + off, 16, 1024),
+                 sdesc_sw128(qa + kk * 2048, C::kChunkBytes, 1024), kIdescKV,
+                 (it > 0 || kk > 0) ? 1u : 0u);
         }
-        if (doA) {
-          // dQ_i = dS K_j  (M = queries, N = d, K dimension = the 128 keys); at
-          // d=64 its own columns are reused once the previous dQ has been read
-          if (C::kColDQ != C::kColST && it > 0 &&
-              !wait_bar(bar(C::kBarDQFree), (it - 1) & 1, abort_flag, p.err))
-            break;
-#pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk) {
-            mma_ss(tmem + C::kColDQ, sdesc_sw128(dsa + kk * 2048, C::kChunkBytes, 1024),
-                   sdesc_sw128(ka + kk * 2048, C::kChunkBytes, 1024), kIdescQ, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(C::kBarDQFull));
+        mma_commit(bar(C::kBarQEmpty + it % C::kStagesQ));
+        BSS_TRACE_EV(p, tr, 1, 4 * it + 2);
+        if (it + 1 < n_it) {
+          // dP^T(i+1) over dQ(i): only once dQ(i) has been read out
+          if (C::kDQOverDP && !wait_bar(bar(C::kBarDQFree), it & 1, abort_flag, p.err)) break;
+          BSS_TRACE_EV(p, tr, 1, 4 * it + 3);
+          if (!issue_dp(it + 1)) break;
         }
-        BSS_TRACE_EV(p, tr && A, 1, 5 * it + 4);
       }
       mma_commit(bar(C::kBarDKVFull));
-      mma_commit(bar(C::kBarMmaDone + (A ? 0 : 1)));
-      wait_bar(bar(C::kBarMmaDone + (A ? 0 : 1)), 0, abort_flag, p.err);
+      mma_commit(bar(C::kBarMmaDone));
+      drain_bar(bar(C::kBarMmaDone), 0);   // every MMA issued has completed
     }
-  } else if (warp < 10) {
-    // =================== P^T / dS^T: two warpgroups, thread = key row ===================
-    // Warpgroup X (warps 2-5: X = 0, warps 6-9: X = 1) handles query columns
-    // [64X, 64X + 64) of S^T and dP^T, 16 at a time; the bf16 results of chunk
-    // c go to columns [64X + 8c, 64X + 8c + 8), which this half has already
-    // read, so the halves never touch each other's columns.
-    const int X = (warp - 2) >> 2;
+  }
+  } else if (warp < 12) {
+    regs_set<BwdRegs<D>::kMid, BwdRegs<D>::kLaunchRegs>();
+    // =================== P^T / dS: two warpgroups, thread = key row ===================
+    // Warpgroup X (warps 4-7: X = 0, warps 8-11: X = 1) handles query columns
+    // [64X, 64X + 64), 16 at a time.  Phase 1 turns S^T into P (kept in fp32
+    // registers) and writes P^T (bf16) to columns [64X + 8c, 64X + 8c + 8) of
+    // chunk c, which this half has already read; phase 2 forms dS from P and
+    // dP^T and stores it in shared memory.
+    const int X = (warp - 4) >> 2;
     const int wq = warp & 3;
     const int kr = wq * 32 + lane;
     const int key = j * kTileN + kr;
@@ -327,7 +359,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const float scale = p.scale;
     const float INF = __int_as_float(0x7f800000);
     const size_t stat_base = static_cast<size_t>(bh) * L;
-    uint8_t* ds_smem = smem + C::kDSOff;
+    uint8_t* ds_row = smem + C::kDSOff + X * C::kChunkBytes + kr * 128;   // this key's dS row
     auto load_stats = [&](int i, float& l2, float& dl) {
       const int q = i * kTileM + kr;
       if (i < nq && q < L) {
@@ -346,10 +378,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       stats[128 + kr] = dl;
       mbar_arrive(bar(C::kBarStat + 0));
     }
-    // Buffer (it & 1) holds the statistics of query tile i0 + it (LSE in
-    // log2 units, scale * D).  It is rewritten (for tile it + 2) only after S^T
-    // of tile it + 1 is ready, which implies every thread has finished reading
-    // it for tile it.
+    // Buffer (it & 1) holds the statistics of query tile i0 + it (LSE in log2
+    // units, scale * D).  It is rewritten (for tile it + 2) at the end of tile
+    // it + 1 by half 0; by then dP^T(it + 1) has been issued, which waited for
+    // dS(it) of both halves, so nobody reads it for tile it any more.
     bool ok = true;
     for (int it = 0; it < n_it; ++it) {
       const int i = i0 + it;
@@ -363,67 +395,87 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         break;
       }
       const bool trw = tr && kr == 0 && X == 0;
-      BSS_TRACE_EV(p, trw, 2, 3 * it);
+      (void)trw;
+      BSS_TRACE_EV(p, trw, 2, 4 * it);
       tc_fence_after();
       const bool key_ok = key < L;
       // element mask: diagonal tile (query < key); the ragged tail (query >= L)
       // has lse2 = +inf, so P is 0 there already
       const bool diag = CAUSAL && (i == j);
-      // four chunks of 16 query columns; the TMEM loads of chunk c+1 are in
-      // flight while chunk c is computed
-      uint32_t sv[2][16], dv[2][16];
-      tmem_ld16(tST + 64 * X, sv[0]);
-      tmem_ld16(tDPT + 64 * X, dv[0]);
+      // ---- phase 1: P (four chunks of 16 queries; chunk c+1's TMEM load is in
+      // flight while chunk c is computed) ----
+      float pf[4][16];
+      {
+        uint32_t sv[2][16];
+        tmem_ld16(tST + 64 * X, sv[0]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int cur = c & 1;
-        const int col = 64 * X + 16 * c;                   // first query of the chunk
-        tmem_ld_wait16(sv[cur]);
-        tmem_ld_wait16(dv[cur]);
-        if (c + 1 < 4) {
-          tmem_ld16(tST + col + 16, sv[cur ^ 1]);
-          tmem_ld16(tDPT + col + 16, dv[cur ^ 1]);
-        }
-        float ds[16];
+        for (int c = 0; c < 4; ++c) {
+          const int cur = c & 1;
+          const int col = 64 * X + 16 * c;                 // first query of the chunk
+          tmem_ld_wait16(sv[cur]);
+          if (c + 1 < 4) tmem_ld16(tST + col + 16, sv[cur ^ 1]);
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + 16 * c + e);
-          const float4 d4 = *reinterpret_cast<const float4*>(dlt + 16 * c + e);
-          const float la[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+          for (int e = 0; e < 16; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2 + 16 * c + e);
+            const float la[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int ql = col + e + u;
-            float pv = ex2(fmaf(__uint_as_float(sv[cur][e + u]), sl2, -la[u]));
-            if (!key_ok || (diag && ql < kr)) pv = 0.f;
-            ds[e + u] = pv * fmaf(__uint_as_float(dv[cur][e + u]), scale, -da[u]);
-            sv[cur][e + u] = __float_as_uint(pv);
+            for (int u = 0; u < 4; ++u) {
+              float pv = ex2(fmaf(__uint_as_float(sv[cur][e + u]), sl2, -la[u]));
+              if (!key_ok || (diag && col + e + u < kr)) pv = 0.f;
+              pf[c][e + u] = pv;
+            }
           }
-        }
-        uint32_t pk[8], dk[8];
+          uint32_t pk[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          pk[e] = pack_bf16(__uint_as_float(sv[cur][2 * e]), __uint_as_float(sv[cur][2 * e + 1]));
-          dk[e] = pack_bf16(ds[2 * e], ds[2 * e + 1]);
-        }
-        tmem_st8(tST + 64 * X + 8 * c, pk);
-        tmem_st8(tDPT + 64 * X + 8 * c, dk);
-        // dS into shared memory as the M-major A operand of the dQ MMA: queries
-        // 64*mc .. 64*mc+63 form chunk mc (= X here), one 128-byte row per key,
-        // 16-byte units (8 queries) swizzled by the row index.
-#pragma unroll
-        for (int u2 = 0; u2 < 2; ++u2) {
-          const int unit = 2 * c + u2;
-          uint4 w = make_uint4(dk[4 * u2 + 0], dk[4 * u2 + 1], dk[4 * u2 + 2], dk[4 * u2 + 3]);
-          *reinterpret_cast<uint4*>(ds_smem + X * C::kChunkBytes + kr * 128 + ((unit ^ (kr & 7)) * 16)) = w;
+          for (int e = 0; e < 8; ++e) pk[e] = pack_bf16(pf[c][2 * e], pf[c][2 * e + 1]);
+          tmem_st8(tST + 64 * X + 8 * c, pk);
         }
       }
-      BSS_TRACE_EV(p, trw, 2, 3 * it + 1);
       tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::kBarPReady));
+      BSS_TRACE_EV(p, trw, 2, 4 * it + 1);
+      // ---- phase 2: dS = P o (dP - D), into shared memory ----
+      if (!wait_bar(bar(C::kBarDPFull), it & 1, abort_flag, p.err)) {
+        ok = false;
+        break;
+      }
+      BSS_TRACE_EV(p, trw, 2, 4 * it + 2);
+      tc_fence_after();
+      {
+        uint32_t dv[2][16];
+        tmem_ld16(tDPT + 64 * X, dv[0]);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int cur = c & 1;
+          const int col = 64 * X + 16 * c;
+          tmem_ld_wait16(dv[cur]);
+          if (c + 1 < 4) tmem_ld16(tDPT + col + 16, dv[cur ^ 1]);
+          uint32_t dk[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dlt + 16 * c + e);
+            const float da[4] = {d4.x, d4.y, d4.z, d4.w};
+            float ds[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) ds[u] = pf[c][e + u] * fmaf(__uint_as_float(dv[cur][e + u]), scale, -da[u]);
+            dk[e / 2] = pack_bf16(ds[0], ds[1]);
+            dk[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
+          }
+          // one 128-byte row per key (queries 64X .. 64X+63), 16-byte units of
+          // 8 queries swizzled by the row index: the K-major tile layout
+#pragma unroll
+          for (int u2 = 0; u2 < 2; ++u2) {
+            const int unit = 2 * c + u2;
+            *reinterpret_cast<uint4*>(ds_row + ((unit ^ (kr & 7)) * 16)) =
+                make_uint4(dk[4 * u2 + 0], dk[4 * u2 + 1], dk[4 * u2 + 2], dk[4 * u2 + 3]);
+          }
+        }
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(C::kBarDSReady));
-      BSS_TRACE_EV(p, trw, 2, 3 * it + 2);
+      BSS_TRACE_EV(p, trw, 2, 4 * it + 3);
       if (X == 0) {
         // statistics of the next query tile
         float* nxt = stats + ((it + 1) & 1) * 256;
@@ -462,13 +514,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
       }
     }
-  } else if (warp >= 10 && warp < 14) {
-    // =================== dQ: warps 10-13, thread = query row ===================
+  } else {
+    regs_set<BwdRegs<D>::kHigh, BwdRegs<D>::kLaunchRegs>();
+    // =================== dQ: warps 12-15, thread = query row ===================
     // Each round moves 64 d-columns of the tile's dQ from TMEM to a
     // 128-byte-swizzled fp32 staging buffer (two TMA boxes of 32 columns);
     // one thread then adds the boxes into the fp32 accumulator in global
-    // memory with bulk tensor reduce-adds.  The atomic traffic of a per-thread
-    // scheme never reaches the load/store path.
+    // memory with bulk tensor reduce-adds.  dQ's TMEM columns are handed back
+    // after the last round's reads.  (On the bench shapes, handing them back
+    // before any staging, streaming 16 KB boxes through two slots, or vector
+    // red.global from registers all measured slower: the reduce stream, not
+    // the TMEM hand-back, sets the pace.)
     const int wq = warp & 3;
     const int qr = wq * 32 + lane;
     const uint32_t tDQ = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::kColDQ;
@@ -495,9 +551,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           BSS_TRACE_EV(p, tr && qr == 0, 3, 3 * it + 1);
         }
         // The reduce of the previous round must have read the staging buffer
-        // before it is rewritten.  The issuing thread waits for that only now,
-        // after this round's TMEM reads, so those (and dq_free) never queue
-        // behind a bulk reduce.
+        // before it is rewritten.
         if (g > 0) {
           if (qr == 0) {
             bulk_wait_read_all();
@@ -601,14 +655,22 @@ cudaError_t launch_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
                         cudaStream_t st) {
   using C = BwdCfg<D>;
   auto kern = attn_bwd_main_kernel<D, CAUSAL>;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  constexpr int kMaxDev = 64;
+  static bool configured[kMaxDev] = {};  // the attribute is per device and function
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    if (fa.numRegs < static_cast<int>(BwdRegs<D>::kLaunchRegs)) return cudaErrorInvalidConfiguration;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev] = true;
   }
-  dim3 grid(p.B * p.H, (p.L + kTileN - 1) / kTileN);
-  kern<<<grid, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
+  const int n_cta = p.B * p.H * ((p.L + kTileN - 1) / kTileN);
+  kern<<<n_cta, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }
 

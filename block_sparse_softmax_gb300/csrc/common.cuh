@@ -44,6 +44,50 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// Row-per-thread to line-coalesced stores.  In the epilogue lane l of a warp
+// holds row l of the warp's 32 rows; a store of 16 bytes per lane would touch
+// 32 cache lines per instruction.  An in-register 8x8 transpose of 16-byte
+// segments inside each lane octet (8g..8g+7) turns that around: before it,
+// lane 8g+i holds segments 0..7 (v[4s..4s+3]) of one 128-byte line of its own
+// row; after it, the same lane holds segment i of that line of rows 8g+0..7
+// (row 8g+k at v[4k..4k+3]).  Each of the three butterfly stages swaps one
+// bit between the row and the segment index.
+__device__ __forceinline__ void transpose_octets(uint32_t (&v)[32], int lane) {
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      if (s & m) continue;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t a = v[4 * s + r];
+        const uint32_t b = v[4 * (s | m) + r];
+        const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, hi ? a : b, m);
+        v[4 * s + r] = hi ? recv : a;
+        v[4 * (s | m) + r] = hi ? b : recv;
+      }
+    }
+  }
+}
+
+// Store one 128-byte line per row for the warp's 32 rows after
+// transpose_octets: each instruction writes 4 whole lines.  `base` points at
+// byte `line_off` of the warp's first row, rows are `row_bytes` apart, and
+// only rows whose bit is set in `valid` are written.
+__device__ __forceinline__ void store_octet_lines(const uint32_t (&v)[32], uint8_t* base,
+                                                  size_t row_bytes, uint32_t valid, int lane) {
+  const int g = lane >> 3;
+  const int i = lane & 7;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int r = 8 * g + k;
+    if ((valid >> r) & 1u)
+      *reinterpret_cast<uint4*>(base + r * row_bytes + 16 * i) =
+          make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  }
+}
+
 // Bounded wait used while unwinding: ignores the abort flag so that copies
 // and MMAs already in flight land before the CTA releases its shared and
 // tensor memory.  Gives up silently after `limit` cycles.
@@ -140,6 +184,7 @@ struct BwdParams {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
+  int head_group;          // heads whose key tiles are launched together (see attn_bwd_main_kernel)
   int* err;
   long long* trace;        // trace builds only (nullptr otherwise)
   int trace_cta;

@@ -100,7 +100,7 @@ template <bool SPARSE>
 struct FwdRegs {
   static constexpr uint32_t kLow = SPARSE ? 152 : 136;
   static constexpr uint32_t kHigh = SPARSE ? 176 : 184;
-  static constexpr int kLaunchRegs = 168;
+  static constexpr uint32_t kLaunchRegs = 168;
   static_assert(kLow + 2 * kHigh <= 512, "register split exceeds an SM sub-partition");
   static_assert(128 * kLow + 256 * kHigh <= 384 * kLaunchRegs, "register split exceeds the launch");
 };
@@ -190,50 +190,6 @@ struct Schedule {
     return -1;
   }
 };
-
-// Row-per-thread to line-coalesced stores.  In the epilogue lane l of a warp
-// holds row l of the warp's 32 rows; a store of 16 bytes per lane would touch
-// 32 cache lines per instruction.  An in-register 8x8 transpose of 16-byte
-// segments inside each lane octet (8g..8g+7) turns that around: before it,
-// lane 8g+i holds segments 0..7 (v[4s..4s+3]) of one 128-byte line of its own
-// row; after it, the same lane holds segment i of that line of rows 8g+0..7
-// (row 8g+k at v[4k..4k+3]).  Each of the three butterfly stages swaps one
-// bit between the row and the segment index.
-__device__ __forceinline__ void transpose_octets(uint32_t (&v)[32], int lane) {
-#pragma unroll
-  for (int m = 4; m >= 1; m >>= 1) {
-    const bool hi = (lane & m) != 0;
-#pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      if (s & m) continue;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint32_t a = v[4 * s + r];
-        const uint32_t b = v[4 * (s | m) + r];
-        const uint32_t recv = __shfl_xor_sync(0xFFFFFFFFu, hi ? a : b, m);
-        v[4 * s + r] = hi ? recv : a;
-        v[4 * (s | m) + r] = hi ? b : recv;
-      }
-    }
-  }
-}
-
-// Store one 128-byte line per row for the warp's 32 rows after
-// transpose_octets: each instruction writes 4 whole lines.  `base` points at
-// byte `line_off` of the warp's first row, rows are `row_bytes` apart, and
-// only rows whose bit is set in `valid` are written.
-__device__ __forceinline__ void store_octet_lines(const uint32_t (&v)[32], uint8_t* base,
-                                                  size_t row_bytes, uint32_t valid, int lane) {
-  const int g = lane >> 3;
-  const int i = lane & 7;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int r = 8 * g + k;
-    if ((valid >> r) & 1u)
-      *reinterpret_cast<uint4*>(base + r * row_bytes + 16 * i) =
-          make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-  }
-}
 
 // Persistent over work items.  The grid holds one CTA per item, but a running
 // CTA does not exit after its own item: when its producer has issued the loads
@@ -332,7 +288,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-  regs_dec<FwdRegs<SPARSE>::kLow>();
+  regs_set<FwdRegs<SPARSE>::kLow, FwdRegs<SPARSE>::kLaunchRegs>();
   if (warp == 0) {
     // =================== TMA producer and item scheduler ===================
     if (lane == 0) {
@@ -589,7 +545,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   }
   } else {
-    regs_inc<FwdRegs<SPARSE>::kHigh>();
+    regs_set<FwdRegs<SPARSE>::kHigh, FwdRegs<SPARSE>::kLaunchRegs>();
     // =================== softmax warpgroups (warps 4-7: tile 0, 8-11: tile 1) ===================
     const int t = (warp - 4) >> 2;
     const int wq = warp & 3;                      // TMEM lane quarter of this warp
@@ -813,7 +769,7 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   if (!configured[dev]) {
     cudaFuncAttributes fa;
     if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-    if (fa.numRegs < FwdRegs<SPARSE>::kLaunchRegs) return cudaErrorInvalidConfiguration;
+    if (fa.numRegs < static_cast<int>(FwdRegs<SPARSE>::kLaunchRegs)) return cudaErrorInvalidConfiguration;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured[dev] = true;

@@ -73,10 +73,7 @@ __device__ __forceinline__ bool clc_query(uint32_t resp, int& x) {
       : "=r"(cx), "=r"(cy), "=r"(cz), "=r"(cw), "=r"(ok)
       : "r"(resp)
       : "memory");
-  (void)cy;
-  (void)cz;
-  (void)cw;
-  x = static_cast<int>(cx);
+  x = static_cast<int>(cx + 0u * (cy | cz | cw));   // y, z, w: 1-D grids only
   return ok != 0;
 }
 
@@ -111,6 +108,11 @@ __device__ __forceinline__ void bulk_commit_group() {
 // Wait until the source shared memory of every committed bulk group has been read.
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until the source shared memory of all but the most recent committed
+// bulk group has been read.
+__device__ __forceinline__ void bulk_wait_read_all_but_one() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // Wait until every committed bulk group has completed.
 __device__ __forceinline__ void bulk_wait_all() {
@@ -276,6 +278,19 @@ __device__ __forceinline__ void regs_dec() {
 template <uint32_t N>
 __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+// Move this warp's register budget from the launch's kLaunch registers a
+// thread to N: setmaxnreg.inc may only raise it and .dec only lower it, so the
+// direction is chosen at compile time (nothing is issued when N == kLaunch).
+template <uint32_t N, uint32_t kLaunch>
+__device__ __forceinline__ void regs_set() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg counts are multiples of 8 in [24, 256]");
+  static_assert(kLaunch % 8 == 0, "the launch register count must be a multiple of 8");
+  if constexpr (N > kLaunch) {
+    regs_inc<N>();
+  } else if constexpr (N < kLaunch) {
+    regs_dec<N>();
+  }
 }
 
 // ----------------------------------------------------------------------------

@@ -22,7 +22,8 @@ from . import _lib
 
 __all__ = [
     "AttnError", "attn_fwd", "attn_fwd_partial", "attn_merge_states", "attn_blocklist_normalize",
-    "attn_fwd_blocksparse", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_noalloc",
+    "attn_fwd_blocksparse", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_blocksparse",
+    "attn_bwd_blocksparse_workspace_bytes", "attn_bwd_noalloc",
     "attn_poll_status",
     "attn_watchdog_selftest", "attn_fwd_splitkv", "library",
 ]
@@ -170,6 +171,18 @@ def attn_blocklist_normalize(row_ptr, col_idx, n_kblk: int) -> Tuple[np.ndarray,
     return out_rp, out_ci[:int(nnz[0])].copy()
 
 
+def _csr_on_device(row_ptr, col_idx, device):
+    """int32 CSR on the tensors' device; an empty col_idx gets a one-element
+    placeholder (never read) so that its pointer is valid."""
+    rp = torch.as_tensor(np.asarray(row_ptr, dtype=np.int32) if not torch.is_tensor(row_ptr)
+                         else row_ptr).to(device=device, dtype=torch.int32).contiguous()
+    ci = torch.as_tensor(np.asarray(col_idx, dtype=np.int32) if not torch.is_tensor(col_idx)
+                         else col_idx).to(device=device, dtype=torch.int32).contiguous()
+    if ci.numel() == 0:
+        return rp, torch.zeros(1, device=device, dtype=torch.int32), 0
+    return rp, ci, ci.numel()
+
+
 def attn_fwd_blocksparse(q, k, v, row_ptr, col_idx, *, causal: bool = False,
                          scale: Optional[float] = None, block: int = 128, out=None, lse=None):
     """Attention over per-query-block CSR lists of key blocks (raw form accepted)."""
@@ -177,15 +190,7 @@ def attn_fwd_blocksparse(q, k, v, row_ptr, col_idx, *, causal: bool = False,
     _need(q, "q", torch.bfloat16, (B, H, L, d))
     _need(k, "k", torch.bfloat16, (B, H, L, d))
     _need(v, "v", torch.bfloat16, (B, H, L, d))
-    rp = torch.as_tensor(np.asarray(row_ptr, dtype=np.int32) if not torch.is_tensor(row_ptr)
-                         else row_ptr).to(device=q.device, dtype=torch.int32).contiguous()
-    ci = torch.as_tensor(np.asarray(col_idx, dtype=np.int32) if not torch.is_tensor(col_idx)
-                         else col_idx).to(device=q.device, dtype=torch.int32).contiguous()
-    if ci.numel() == 0:
-        ci = torch.zeros(1, device=q.device, dtype=torch.int32)
-        nnz = 0
-    else:
-        nnz = ci.numel()
+    rp, ci, nnz = _csr_on_device(row_ptr, col_idx, q.device)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, L), device=q.device, dtype=torch.float32) if lse is None else lse
     _need(out, "out", torch.bfloat16, (B, H, L, d))
@@ -222,6 +227,36 @@ def attn_bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: Optional[flo
                               workspace.numel() * workspace.element_size(), B, H, L, d,
                               _scale(scale, d), int(causal), _stream_of(q))
     _check(st, "attn_bwd")
+    return dq, dk, dv, delta
+
+
+def attn_bwd_blocksparse_workspace_bytes(B: int, H: int, L: int, d: int) -> int:
+    return int(_lib.load().attn_bwd_blocksparse_workspace_bytes(B, H, L, d))
+
+
+def attn_bwd_blocksparse(q, k, v, o, lse, dout, row_ptr, col_idx, *, causal: bool = False,
+                         scale: Optional[float] = None, block: int = 128,
+                         workspace: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None,
+                         delta=None):
+    """Gradients of attn_fwd_blocksparse with the same block list (raw CSR accepted)."""
+    B, H, L, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _need(t, name, torch.bfloat16, (B, H, L, d))
+    _need(lse, "lse", torch.float32, (B, H, L))
+    rp, ci, nnz = _csr_on_device(row_ptr, col_idx, q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    delta = torch.empty((B, H, L), device=q.device, dtype=torch.float32) if delta is None else delta
+    nbytes = attn_bwd_blocksparse_workspace_bytes(B, H, L, d)
+    if workspace is None:
+        workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
+    st = _lib.load().attn_bwd_blocksparse(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), B, H, L, d, _scale(scale, d), int(causal),
+        int(block), rp.data_ptr(), ci.data_ptr(), rp.numel() - 1, nnz, _stream_of(q))
+    _check(st, "attn_bwd_blocksparse")
     return dq, dk, dv, delta
 
 

@@ -38,6 +38,14 @@ _SIGNATURES = {
                             _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                             _C.c_void_p, _C.c_size_t, _C.c_int, _C.c_int, _C.c_int, _C.c_int,
                             _C.c_float, _C.c_int, _C.c_void_p]),
+    "attn_bwd_blocksparse_workspace_bytes": (_C.c_size_t, [_C.c_int, _C.c_int, _C.c_int,
+                                                           _C.c_int]),
+    "attn_bwd_blocksparse": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
+                                        _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
+                                        _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_size_t,
+                                        _C.c_int, _C.c_int, _C.c_int, _C.c_int, _C.c_float,
+                                        _C.c_int, _C.c_int, _C.c_void_p, _C.c_void_p, _C.c_int,
+                                        _C.c_int, _C.c_void_p]),
     "attn_bwd_noalloc": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                     _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                     _C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int, _C.c_int,

@@ -212,6 +212,82 @@ attn_status_t noalloc_scratch(float** out) {
   return ATTN_OK;
 }
 
+// Workspace of the block-sparse backward: the fp32 dQ accumulator, then (at a
+// 256-byte boundary) the key-major bitmap of the block list.
+size_t bwd_bitmap_offset(size_t acc_bytes) { return (acc_bytes + 255) & ~static_cast<size_t>(255); }
+size_t bwd_bitmap_bytes(int L) {
+  const size_t nblk = (static_cast<size_t>(L < 0 ? 0 : L) + 127) / 128;
+  return nblk * ((nblk + 31) / 32) * 4;
+}
+
+// The backward of attn_bwd and attn_bwd_blocksparse (row_ptr == nullptr: dense
+// or causal); the workspace size has been checked by the caller.
+attn_status_t bwd_common(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         float* delta, void* workspace, int B, int H, int L, int d, float scale,
+                         int causal, const int32_t* row_ptr, const int32_t* col_idx, int nnz,
+                         void* stream) {
+  attn_status_t s = check_common(B, H, L, L, d, scale);
+  if (s != ATTN_OK) return s;
+  const void* ptrs16[] = {q, k, v, o, dout, dq, dk, dv, workspace};
+  for (const void* ptr : ptrs16)
+    if (!ptr || !aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
+  if (!lse || !delta || !aligned4(lse) || !aligned4(delta)) return ATTN_ERR_INVALID_ARG;
+  if (L == 0) return ATTN_OK;
+  if ((s = get_encoder()) != ATTN_OK) return s;
+  BwdParams p{};
+  if ((s = status_word(&p.err)) != ATTN_OK) return s;
+  CUtensorMap tq, tk, tv, tdo, tdq;
+  if ((s = make_map(&tq, q, B, H, L, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tk, k, B, H, L, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tv, v, B, H, L, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tdo, dout, B, H, L, d)) != ATTN_OK) return s;
+  if ((s = make_map_f32(&tdq, workspace, B, H, L, d)) != ATTN_OK) return s;
+  p.B = B;
+  p.H = H;
+  p.L = L;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal ? 1 : 0;
+  p.o = static_cast<const __nv_bfloat16*>(o);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.lse = lse;
+  p.delta = delta;
+  p.dq_acc = static_cast<float*>(workspace);
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  // Heads launched together: about 2 groups run at once, each head holding
+  // Q, dO (bf16) and the dQ accumulator (fp32), 8 L d bytes; keep the pair of
+  // groups near 64 MiB, well inside L2.
+  {
+    const long long per_head = 8ll * L * d;
+    long long g = (64ll << 20) / (2 * per_head);
+    if (g < 1) g = 1;
+    if (g > static_cast<long long>(B) * H) g = static_cast<long long>(B) * H;
+    p.head_group = static_cast<int>(g);
+  }
+#ifdef BSS_TRACE
+  p.trace = g_trace_buf;
+  p.trace_cta = g_trace_cta;
+#endif
+  const bool sparse = row_ptr != nullptr;
+  if (sparse) {
+    const int nblk = (L + 127) / 128;
+    uint32_t* bm = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) +
+                                               bwd_bitmap_offset(attn_bwd_workspace_bytes(B, H, L, d)));
+    p.col_bitmap = bm;
+    p.col_bitmap_words = (nblk + 31) / 32;
+    s = cuda_status("attn_bwd_blocksparse block-list transpose",
+                    launch_blocklist_columns(row_ptr, col_idx, nblk, nnz, causal, bm,
+                                             p.col_bitmap_words, p.err,
+                                             static_cast<cudaStream_t>(stream)));
+    if (s != ATTN_OK) return s;
+  }
+  return cuda_status("attn_bwd launch", launch_bwd(d, sparse, tq, tk, tv, tdo, tdq, p,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 }  // namespace bss
 
@@ -335,57 +411,37 @@ size_t attn_bwd_workspace_bytes(int B, int H, int L, int d) {
   return static_cast<size_t>(B) * H * static_cast<size_t>(L) * d * sizeof(float);
 }
 
+size_t attn_bwd_blocksparse_workspace_bytes(int B, int H, int L, int d) {
+  const size_t acc = attn_bwd_workspace_bytes(B, H, L, d);
+  if (acc == 0 && L != 0) return 0;
+  return bwd_bitmap_offset(acc) + bwd_bitmap_bytes(L);
+}
+
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
                        float* delta, void* workspace, size_t workspace_bytes, int B, int H, int L,
                        int d, float scale, int causal, void* stream) {
-  attn_status_t s = check_common(B, H, L, L, d, scale);
-  if (s != ATTN_OK) return s;
-  const void* ptrs16[] = {q, k, v, o, dout, dq, dk, dv, workspace};
-  for (const void* ptr : ptrs16)
-    if (!ptr || !aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
-  if (!lse || !delta || !aligned4(lse) || !aligned4(delta)) return ATTN_ERR_INVALID_ARG;
   if (workspace_bytes < attn_bwd_workspace_bytes(B, H, L, d)) return ATTN_ERR_WORKSPACE;
-  if (L == 0) return ATTN_OK;
-  if ((s = get_encoder()) != ATTN_OK) return s;
-  BwdParams p{};
-  if ((s = status_word(&p.err)) != ATTN_OK) return s;
-  CUtensorMap tq, tk, tv, tdo, tdq;
-  if ((s = make_map(&tq, q, B, H, L, d)) != ATTN_OK) return s;
-  if ((s = make_map(&tk, k, B, H, L, d)) != ATTN_OK) return s;
-  if ((s = make_map(&tv, v, B, H, L, d)) != ATTN_OK) return s;
-  if ((s = make_map(&tdo, dout, B, H, L, d)) != ATTN_OK) return s;
-  if ((s = make_map_f32(&tdq, workspace, B, H, L, d)) != ATTN_OK) return s;
-  p.B = B;
-  p.H = H;
-  p.L = L;
-  p.scale = scale;
-  p.scale_log2 = scale * kLog2e;
-  p.causal = causal ? 1 : 0;
-  p.o = static_cast<const __nv_bfloat16*>(o);
-  p.dout = static_cast<const __nv_bfloat16*>(dout);
-  p.lse = lse;
-  p.delta = delta;
-  p.dq_acc = static_cast<float*>(workspace);
-  p.dq = static_cast<__nv_bfloat16*>(dq);
-  p.dk = static_cast<__nv_bfloat16*>(dk);
-  p.dv = static_cast<__nv_bfloat16*>(dv);
-  // Heads launched together: about 2 groups run at once, each head holding
-  // Q, dO (bf16) and the dQ accumulator (fp32), 8 L d bytes; keep the pair of
-  // groups near 64 MiB, well inside L2.
-  {
-    const long long per_head = 8ll * L * d;
-    long long g = (64ll << 20) / (2 * per_head);
-    if (g < 1) g = 1;
-    if (g > static_cast<long long>(B) * H) g = static_cast<long long>(B) * H;
-    p.head_group = static_cast<int>(g);
-  }
-#ifdef BSS_TRACE
-  p.trace = g_trace_buf;
-  p.trace_cta = g_trace_cta;
-#endif
-  return cuda_status("attn_bwd launch",
-                     launch_bwd(d, tq, tk, tv, tdo, tdq, p, static_cast<cudaStream_t>(stream)));
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, delta, workspace, B, H, L, d, scale, causal,
+                    nullptr, nullptr, 0, stream);
+}
+
+attn_status_t attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
+                                   const float* lse, const void* dout, void* dq, void* dk,
+                                   void* dv, float* delta, void* workspace, size_t workspace_bytes,
+                                   int B, int H, int L, int d, float scale, int causal, int block,
+                                   const int32_t* row_ptr, const int32_t* col_idx, int n_qblk,
+                                   int nnz, void* stream) {
+  if (block != 128) return ATTN_ERR_UNSUPPORTED;
+  if (L < 0) return ATTN_ERR_INVALID_ARG;
+  const long long nblk = (static_cast<long long>(L) + 127) / 128;
+  if (nblk > kMaxKBlocks) return ATTN_ERR_UNSUPPORTED;
+  if (n_qblk != nblk || nnz < 0) return ATTN_ERR_BAD_BLOCKLIST;
+  if (!row_ptr || (nnz > 0 && !col_idx) || !aligned4(row_ptr) || !aligned4(col_idx))
+    return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_bwd_blocksparse_workspace_bytes(B, H, L, d)) return ATTN_ERR_WORKSPACE;
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, delta, workspace, B, H, L, d, scale, causal,
+                    row_ptr, col_idx, nnz, stream);
 }
 
 attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,

@@ -57,7 +57,9 @@ struct BwdCfg {
   static constexpr int kStageOff = kDSOff + kDSBytes;    // dQ staging: 128 rows x 64 fp32
   static constexpr int kStageBytes = kTileM * 64 * 4;
   static constexpr int kStatOff = kStageOff + kStageBytes;   // 2 x (lse2[128], delta[128])
-  static constexpr int kBarOff = kStatOff + 2 * 2 * 128 * 4;
+  static constexpr int kColBmOff = kStatOff + 2 * 2 * 128 * 4;   // block-sparse: this key tile's column
+  static constexpr int kColBmWords = kMaxKBlocks / 32;
+  static constexpr int kBarOff = kColBmOff + kColBmWords * 4;
   static constexpr int kBarKV = 0;
   static constexpr int kBarQFull = 1;
   static constexpr int kBarQEmpty = kBarQFull + kStagesQ;
@@ -117,7 +119,30 @@ struct BwdRegs {
   static_assert(128 * (kLow + 2 * kMid + kHigh) <= 512 * kLaunchRegs, "register split exceeds the launch");
 };
 
-template <int D, bool CAUSAL>
+// The query tiles a key tile meets, in ascending order: a dense range
+// [first, nq) or the set bits of the key tile's column of the block list
+// (kept in shared memory).  Every role walks it identically.
+struct QTiles {
+  const uint32_t* bm;      // nullptr: dense range
+  int first_dense, nq;
+  __device__ __forceinline__ int first() const {
+    if (bm == nullptr) return first_dense < nq ? first_dense : -1;
+    return next(-1);
+  }
+  __device__ __forceinline__ int next(int i) const {
+    if (bm == nullptr) return i + 1 < nq ? i + 1 : -1;
+    int c = i + 1;
+    while (c < nq) {
+      const int w = c >> 5;
+      const uint32_t bits = bm[w] & (0xFFFFFFFFu << (c & 31));
+      if (bits) return (w << 5) + __ffs(bits) - 1;
+      c = (w + 1) << 5;
+    }
+    return -1;
+  }
+};
+
+template <int D, bool CAUSAL, bool SPARSE>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -161,8 +186,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const int bh = grp * p.head_group + (within - j * gsz);
   const int b = bh / p.H;
   const int h = bh - b * p.H;
-  const int i0 = CAUSAL ? j : 0;                  // first query tile that sees these keys
-  const int n_it = nq - i0;
+  // Query tiles met by this key tile: under a causal mask none before j.  A
+  // block-sparse launch takes them from the key tile's column of the block
+  // list (built with the causal cut already applied).
+  uint32_t* col_bm = reinterpret_cast<uint32_t*>(smem + C::kColBmOff);
+  QTiles qs;
+  qs.bm = SPARSE ? col_bm : nullptr;
+  qs.first_dense = CAUSAL ? j : 0;
+  qs.nq = nq;
+  int n_it = SPARSE ? 0 : nq - qs.first_dense;
+  if (SPARSE) {
+    const int words = (nq + 31) / 32;
+    for (int w = tid; w < words; w += C::kThreads)
+      col_bm[w] = __ldg(p.col_bitmap + static_cast<size_t>(j) * p.col_bitmap_words + w);
+    __syncthreads();
+    for (int w = 0; w < words; ++w) n_it += __popc(col_bm[w]);
+  }
 
   if (tid == 0) {
     mbar_init(bar(C::kBarKV), 1);
@@ -211,8 +250,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tma_load_4d(sbase + C::kVOff + c * C::kChunkBytes, &tmV, bar(C::kBarKV), c * 64, j * kTileN, h, b);
       }
       int nq_ld = 0, ndo_ld = 0;
-      for (int it = 0; it < n_it; ++it) {
-        const int row = (i0 + it) * kTileM;
+      for (int i = qs.first(), it = 0; i >= 0; i = qs.next(i), ++it) {
+        const int row = i * kTileM;
         const int sq = it % C::kStagesQ;
         if (it >= C::kStagesQ &&
             !wait_bar(bar(C::kBarQEmpty + sq), ((it / C::kStagesQ) & 1) ^ 1, abort_flag, p.err))
@@ -288,7 +327,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       };
       bool ok = wait_bar(bar(C::kBarKV), 0, abort_flag, p.err);
       if (ok && n_it > 0) ok = issue_s(0) && issue_dp(0);
-      for (int it = 0; it < n_it && ok; ++it) {
+      for (int i = qs.first(), it = 0; i >= 0 && ok; i = qs.next(i), ++it) {
+        const bool more = it + 1 < n_it;               // another query tile follows
         // dV += P^T dO_i  (K dimension = the 128 queries)
         if (!wait_bar(bar(C::kBarPReady), it & 1, abort_flag, p.err)) break;
         BSS_TRACE_EV(p, tr, 1, 4 * it);
@@ -301,7 +341,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                  (it > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(C::kBarDOEmpty + it % C::kStagesDO));   // dP^T(it) and dV(it) read dO_i
-        if (it + 1 < n_it && !issue_s(it + 1)) break;
+        if (more && !issue_s(it + 1)) break;
         // the P/dS warps run for a while: poll gently so that the issue slots
         // they share with this warp stay theirs
         if (!wait_bar_relaxed<64>(bar(C::kBarDSReady), it & 1, abort_flag, p.err)) break;
@@ -328,7 +368,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
         mma_commit(bar(C::kBarQEmpty + it % C::kStagesQ));
         BSS_TRACE_EV(p, tr, 1, 4 * it + 2);
-        if (it + 1 < n_it) {
+        if (more) {
           // dP^T(i+1) over dQ(i): only once dQ(i) has been read out
           if (C::kDQOverDP && !wait_bar(bar(C::kBarDQFree), it & 1, abort_flag, p.err)) break;
           BSS_TRACE_EV(p, tr, 1, 4 * it + 3);
@@ -362,7 +402,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     uint8_t* ds_row = smem + C::kDSOff + X * C::kChunkBytes + kr * 128;   // this key's dS row
     auto load_stats = [&](int i, float& l2, float& dl) {
       const int q = i * kTileM + kr;
-      if (i < nq && q < L) {
+      if (i >= 0 && i < nq && q < L) {
         const float lse = __ldg(p.lse + stat_base + q);
         l2 = (lse == -INF) ? INF : lse * kLog2e;      // an empty row contributes nothing
         dl = __ldg(p.delta + stat_base + q) * scale;
@@ -373,22 +413,21 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     };
     if (X == 0) {
       float l2, dl;
-      load_stats(i0, l2, dl);
+      load_stats(qs.first(), l2, dl);
       stats[kr] = l2;
       stats[128 + kr] = dl;
       mbar_arrive(bar(C::kBarStat + 0));
     }
-    // Buffer (it & 1) holds the statistics of query tile i0 + it (LSE in log2
-    // units, scale * D).  It is rewritten (for tile it + 2) at the end of tile
+    // Buffer (it & 1) holds the statistics of the it-th query tile met (LSE in
+    // log2 units, scale * D).  It is rewritten (for tile it + 2) at the end of tile
     // it + 1 by half 0; by then dP^T(it + 1) has been issued, which waited for
     // dS(it) of both halves, so nobody reads it for tile it any more.
     bool ok = true;
-    for (int it = 0; it < n_it; ++it) {
-      const int i = i0 + it;
+    for (int i = qs.first(), it = 0; i >= 0; i = qs.next(i), ++it) {
       const float* lse2 = stats + (it & 1) * 256 + 64 * X;
       const float* dlt = lse2 + 128;
       float l2n = 0.f, dln = 0.f;
-      if (X == 0) load_stats(i + 1, l2n, dln);
+      if (X == 0) load_stats(qs.next(i), l2n, dln);
       if (!wait_bar(bar(C::kBarSFull), it & 1, abort_flag, p.err) ||
           !wait_bar(bar(C::kBarStat + (it & 1)), (it >> 1) & 1, abort_flag, p.err)) {
         ok = false;
@@ -535,7 +574,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     static_assert(2 * kBoxBytes == C::kStageBytes, "two boxes fill the staging buffer");
     bool ok = true;
     int g = 0;                                    // global round counter
-    for (int it = 0; it < n_it && ok; ++it) {
+    for (int i = qs.first(), it = 0; i >= 0 && ok; i = qs.next(i), ++it) {
       if (!wait_bar_relaxed(bar(C::kBarDQFull), it & 1, abort_flag, p.err)) break;
       BSS_TRACE_EV(p, tr && qr == 0, 3, 3 * it);
       tc_fence_after();
@@ -579,7 +618,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             ok = false;
             break;
           }
-          const int row = (i0 + it) * kTileM;
+          const int row = i * kTileM;
           tma_reduce_add_4d(&tmDQ, stage, 64 * r, row, h, b);
           tma_reduce_add_4d(&tmDQ, stage + kBoxBytes, 64 * r + 32, row, h, b);
           bulk_commit_group();
@@ -649,12 +688,12 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_convert_kernel(const float* a
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPARSE>
 cudaError_t launch_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                         const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
                         cudaStream_t st) {
   using C = BwdCfg<D>;
-  auto kern = attn_bwd_main_kernel<D, CAUSAL>;
+  auto kern = attn_bwd_main_kernel<D, CAUSAL, SPARSE>;
   constexpr int kMaxDev = 64;
   static bool configured[kMaxDev] = {};  // the attribute is per device and function
   int dev = 0;
@@ -682,11 +721,48 @@ unsigned grid_for(long long work, int per_block) {
   return static_cast<unsigned>(blocks);
 }
 
+// Key-major bitmap of a block list: bit i of column c is set when query block
+// i lists key block c.  Duplicates collapse, the order of a row is irrelevant,
+// and under a causal mask a key block after the query block is left out (it
+// holds no allowed pair).  One thread per query block; malformed rows and
+// entries are skipped and reported.
+__global__ void __launch_bounds__(256) attn_blocklist_columns_kernel(
+    const int* row_ptr, const int* col_idx, int n_qblk, int nnz, int causal, uint32_t* bm,
+    int words, int* err) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_qblk; i += gridDim.x * blockDim.x) {
+    const int beg = __ldg(row_ptr + i);
+    const int end = __ldg(row_ptr + i + 1);
+    if (beg < 0 || end < beg || end > nnz) {
+      record_error(err, ATTN_ERR_BAD_BLOCKLIST);
+      continue;
+    }
+    for (int e = beg; e < end; ++e) {
+      const int c = __ldg(col_idx + e);
+      if (c < 0 || c >= n_qblk) {
+        record_error(err, ATTN_ERR_BAD_BLOCKLIST);
+        continue;
+      }
+      if (causal && c > i) continue;
+      atomicOr(bm + static_cast<size_t>(c) * words + (i >> 5), 1u << (i & 31));
+    }
+  }
+}
+
 }  // namespace
 
-cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
-                       cudaStream_t st) {
+cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int n_qblk, int nnz,
+                                     int causal, uint32_t* bitmap, int words, int* err,
+                                     cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(bitmap, 0, static_cast<size_t>(n_qblk) * words * 4, st);
+  if (e != cudaSuccess) return e;
+  attn_blocklist_columns_kernel<<<grid_for(n_qblk, 256), 256, 0, st>>>(row_ptr, col_idx, n_qblk, nnz,
+                                                                      causal, bitmap, words, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(int d, bool sparse, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                       const BwdParams& p, cudaStream_t st) {
   const long long rows = static_cast<long long>(p.B) * p.H * p.L;
   cudaError_t e;
   if (d == 64) {
@@ -697,12 +773,19 @@ cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, cons
     return cudaErrorInvalidValue;
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (d == 64)
-    e = p.causal ? launch_main<64, true>(tq, tk, tv, tdo, tdq, p, st)
-                 : launch_main<64, false>(tq, tk, tv, tdo, tdq, p, st);
-  else
-    e = p.causal ? launch_main<128, true>(tq, tk, tv, tdo, tdq, p, st)
-                 : launch_main<128, false>(tq, tk, tv, tdo, tdq, p, st);
+#define BSS_BWD_CASE(DD, CA, SP)                                  \
+  if (d == DD && (p.causal != 0) == CA && sparse == SP)           \
+    e = launch_main<DD, CA, SP>(tq, tk, tv, tdo, tdq, p, st);
+  e = cudaErrorInvalidValue;
+  BSS_BWD_CASE(64, false, false)
+  BSS_BWD_CASE(64, true, false)
+  BSS_BWD_CASE(128, false, false)
+  BSS_BWD_CASE(128, true, false)
+  BSS_BWD_CASE(64, false, true)
+  BSS_BWD_CASE(64, true, true)
+  BSS_BWD_CASE(128, false, true)
+  BSS_BWD_CASE(128, true, true)
+#undef BSS_BWD_CASE
   if (e != cudaSuccess) return e;
   const long long n8 = rows * d / 8;
   attn_bwd_dq_convert_kernel<<<grid_for(n8, 256), 256, 0, st>>>(p.dq_acc, p.dq, n8);

@@ -185,6 +185,10 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int head_group;          // heads whose key tiles are launched together (see attn_bwd_main_kernel)
+  // block-sparse: key-major bitmap of the block list (bit i of column c: query
+  // block i lists key block c), col_bitmap_words words per column
+  const uint32_t* col_bitmap;
+  int col_bitmap_words;
   int* err;
   long long* trace;        // trace builds only (nullptr otherwise)
   int trace_cta;
@@ -198,8 +202,11 @@ cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUte
                        const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                        cudaStream_t st);
 cudaError_t launch_merge(int d, const MergeParams& p, int* err, cudaStream_t st);
-cudaError_t launch_bwd(int d, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
-                       cudaStream_t st);
+cudaError_t launch_bwd(int d, bool sparse, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                       const BwdParams& p, cudaStream_t st);
+cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int n_qblk, int nnz,
+                                     int causal, uint32_t* bitmap, int words, int* err,
+                                     cudaStream_t st);
 cudaError_t launch_watchdog_selftest(unsigned long long cycles, int* err, cudaStream_t st);
 }  // namespace bss

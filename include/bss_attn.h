@@ -158,6 +158,37 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        int B, int H, int L, int d, float scale, int causal, void* stream);
 
 /*
+ * attn_bwd_blocksparse_workspace_bytes - size of the caller-provided workspace
+ * of attn_bwd_blocksparse: the fp32 dQ accumulator (B*H*L*d elements, rounded
+ * up to 256 bytes) followed by a key-major bitmap of the block list
+ * (ceil(L/128) columns of ceil(ceil(L/128)/32) 32-bit words).
+ */
+size_t attn_bwd_blocksparse_workspace_bytes(int B, int H, int L, int d);
+
+/*
+ * attn_bwd_blocksparse - gradients of attn_fwd_blocksparse by recomputation.
+ * "Exact Blocks, Rings, and Sparsity", section 3 (the backward of section 2
+ * over the same allowed set) and section 6 (gradients flow only through the
+ * kept blocks: the dropped ones have P = 0, and renormalising over the sparse
+ * domain is what the saved LSE already encodes); block-sparse attention
+ * patterns page (compare gradients too, duplicates counted once, empty rows).
+ *   Arguments as attn_bwd plus the block list of attn_fwd_blocksparse (block
+ *   128, DEVICE int32 CSR, raw form accepted) and the same causal flag; lse
+ *   must come from attn_fwd_blocksparse with that list.  Each key tile walks
+ *   the query blocks that list it (the list's transpose, built in the
+ *   workspace on the stream).  A key block no query block lists gets
+ *   dK = dV = 0; a query block with an empty list gets dQ = 0.  Malformed
+ *   entries are handled and reported as in attn_fwd_blocksparse.
+ *   workspace: device, >= attn_bwd_blocksparse_workspace_bytes(B,H,L,d).
+ */
+attn_status_t attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
+                                   const float* lse, const void* dout, void* dq, void* dk,
+                                   void* dv, float* delta, void* workspace, size_t workspace_bytes,
+                                   int B, int H, int L, int d, float scale, int causal, int block,
+                                   const int32_t* row_ptr, const int32_t* col_idx, int n_qblk,
+                                   int nnz, void* stream);
+
+/*
  * attn_bwd_noalloc - attn_bwd for callers that cannot allocate device memory.
  * The source pages have no counterpart: this entry exists for callers that
  * may not call cudaMalloc or own a workspace (an allocator that forbids new

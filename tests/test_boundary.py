@@ -126,6 +126,17 @@ def test_argument_errors_return_codes_before_any_device_work(lib):
     ws = lib.attn_bwd_workspace_bytes(2, 3, 100, 64)
     assert ws == 2 * 3 * 100 * 64 * 4
     assert lib.attn_bwd(P, P, P, P, P, P, P, P, P, P, P, ws - 4, 2, 3, 100, 64, 0.125, 1, None) == 6
+    # block-sparse backward: workspace = accumulator (256-byte aligned) + bitmap
+    # of ceil(L/128) columns of ceil(ceil(L/128)/32) words
+    wss = lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64)
+    acc = 2 * 3 * 1000 * 64 * 4
+    assert wss == ((acc + 255) // 256) * 256 + 8 * 1 * 4
+    sp = lambda block=128, nq=8, ws_=wss, rp=P: (P, P, P, P, P, P, P, P, P, P, P, ws_, 2, 3, 1000,
+                                                 64, 0.125, 1, block, rp, P, nq, 4, None)
+    assert lib.attn_bwd_blocksparse(*sp(block=64)) == 2          # block size other than 128
+    assert lib.attn_bwd_blocksparse(*sp(nq=7)) == 3              # CSR row count mismatch
+    assert lib.attn_bwd_blocksparse(*sp(rp=None)) == 1           # missing row_ptr
+    assert lib.attn_bwd_blocksparse(*sp(ws_=wss - 4)) == 6       # workspace too small
 
 
 def test_binding_fails_loudly_on_cpu_tensors():

@@ -87,6 +87,45 @@ def load_peaks():
     return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+# The kernel behind each row of the step, and the sources that define it (the
+# DRAM traffic recorded for a kernel is used only while they are unchanged).
+KERNEL_OF_ROW = {
+    "fwd": "attn_fwd_kernel (causal, persistent)",
+    "splitkv": "attn_fwd_kernel (partial) x8 + merge_states_kernel",
+    "sparse": "attn_fwd_kernel (block-sparse)",
+    "bwd": "attn_bwd_main_kernel (+ preprocess and dq_convert in the same call)",
+}
+TRAFFIC_KERNEL = {"fwd": "attn_fwd_kernel", "bwd": "attn_bwd_main_kernel"}
+KERNEL_SOURCES = {"attn_fwd_kernel": ["fwd.cu", "common.cuh", "ptx.cuh"],
+                  "attn_bwd_main_kernel": ["bwd.cu", "common.cuh", "ptx.cuh"]}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "block_sparse_softmax_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def dram_traffic(row: str):
+    """DRAM bytes (read + write) per launch of the row's dominant kernel, from
+    the ncu capture summarised in profiles/traffic.json, or None when there is
+    none or the kernel's sources changed after it was taken."""
+    kernel = TRAFFIC_KERNEL.get(row)
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if kernel is None or not os.path.exists(path):
+        return None, "no ncu capture of this kernel"
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if rec is None:
+        return None, "no ncu capture of this kernel"
+    if rec.get("source_sha256") != kernel_source_hash(kernel):
+        return None, "kernel changed since the ncu capture"
+    return rec["dram_bytes_per_launch"], rec.get("capture", "")
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during a timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -103,10 +142,19 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # nvidia-smi takes a while to start: wait (up to 3 s) for its first
+        # sample so that the timed region is covered from its beginning
+        t0 = time.time()
+        while time.time() - t0 < 3.0 and self.proc.poll() is None:
+            self.fh.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -295,11 +343,22 @@ def measure_configs(bss, dev, peaks):
     pairs, tiles = sparse_counts(w.L, rp, ci, True)
     pairs *= w.B * w.H
     tiles *= w.B * w.H
+    # its backward (attn_bwd_blocksparse), from the forward's O and LSE
+    do = make_inputs(Workload(w.name, w.B, w.H, w.L, w.d, True, w.seed, backward=True))["do"].to(dev)
+    ws = torch.empty(bss.attn_bwd_blocksparse_workspace_bytes(w.B, w.H, w.L, w.d), device=dev,
+                     dtype=torch.uint8)
+    g = [torch.empty_like(x["q"]) for _ in range(3)]
+    dl = torch.empty_like(lse)
+    ms_b = bench_kernel(lambda: bss.attn_bwd_blocksparse(
+        x["q"], x["k"], x["v"], o, lse, do, rpd, cid, causal=True, scale=w.scale, workspace=ws,
+        dq=g[0], dk=g[1], dv=g[2], delta=dl))
     out[w.name] = {"ms": round(ms, 4), "logical_pairs": pairs, "executed_tiles": tiles,
                    "pairs_per_s": pairs / ms * 1e3,
                    "tflops_logical": round(4 * w.d * pairs / ms / 1e9, 1),
-                   "tflops_executed": round(4 * w.d * tiles * 128 * 128 / ms / 1e9, 1)}
-    del x, o, lse
+                   "tflops_executed": round(4 * w.d * tiles * 128 * 128 / ms / 1e9, 1),
+                   "bwd_ms": round(ms_b, 4),
+                   "bwd_tflops_logical": round(10 * w.d * pairs / ms_b / 1e9, 1)}
+    del x, o, lse, do, ws, g, dl
     # split-KV L=131072, 8 chunks + merge
     w = SPLITKV_128K
     x = {k: t.to(dev) for k, t in make_inputs(w).items()}
@@ -432,11 +491,7 @@ def run_gpu(args):
     # dominant kernel: the largest share of the step's time
     dom = max(row_avg, key=row_avg.get)
     dom_tf = step.flops[dom] / row_avg[dom] / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
-            traffic = json.load(f).get(dom)
+    traffic, traffic_note = dram_traffic(dom)
     extra = {} if args.quick else measure_configs(bss, dev, peaks)
     out = {
         "metric": METRIC,
@@ -462,14 +517,13 @@ def run_gpu(args):
         "sparse_pairs_per_s": step.pairs_sparse / row_avg["sparse"] * 1e3,
         "sparse_executed_tiles": step.tiles_sparse,
         "row_ms": {k: round(v, 4) for k, v in row_avg.items()},
-        "roofline": {"kernel": {"fwd": "attn_fwd_kernel", "bwd": "attn_bwd (3 kernels)",
-                                "splitkv": "attn_fwd_kernel<partial> x8 + merge",
-                                "sparse": "attn_fwd_kernel<sparse>"}[dom],
+        "roofline": {"kernel": KERNEL_OF_ROW[dom],
+                     "share_of_step": round(row_avg[dom] / sum(row_avg.values()), 4),
                      "bound": "tensor", "achieved": round(dom_tf, 1),
                      "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
                      "frac": round(dom_tf / peaks["bf16_sustained"], 4),
                      "peak_kind": f"bf16 sustained ({peaks['source']})",
-                     "traffic": traffic},
+                     "traffic": traffic, "traffic_note": traffic_note},
         "clocks": clock_info,
         "e2e": {"value": round(world * step.total_flops / ms_e2e / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -629,7 +683,7 @@ def main():
                     default=None,
                     help="run one small case of one kernel (for ncu) and exit")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--quick", action="store_true", help="skip the per-workload measurements")

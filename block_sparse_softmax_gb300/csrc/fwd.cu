@@ -472,8 +472,8 @@ __global__ void __launch_bounds__(384, 1)
           ok = wait_bar(bar(C::kBarKFull + sk), (i / C::kStagesK) & 1, abort_flag, p.err);
           if (ok) {
             tc_fence_after();
-            for (int t = 0; t < 2 && ok; ++t)
-              if ((mask >> t) & 1) ok = issue_qk(t, sk, kb);
+            if (ok && (mask & 1)) ok = issue_qk(0, sk, kb);
+            if (ok && (mask & 2)) ok = issue_qk(1, sk, kb);
             if (ok) mma_commit(bar(C::kBarKEmpty + sk));
           }
         }
@@ -489,32 +489,28 @@ __global__ void __launch_bounds__(384, 1)
           BSS_TRACE_EV(p, tr, 1, 4 * i);
           tc_fence_after();
           bool kready = false;
-          for (int t = 0; t < 2 && ok; ++t) {
+          // tile t's P V of this block, then its S of the next block; called
+          // with constant t so that the per-tile counters stay in registers
+          auto tile_step = [&](const int t) -> bool {
             if ((mask >> t) & 1) {
-              if (!wait_bar(bar(C::kBarPFull + t), pcount[t] & 1, abort_flag, p.err)) {
-                ok = false;
-                break;
-              }
+              if (!wait_bar(bar(C::kBarPFull + t), pcount[t] & 1, abort_flag, p.err)) return false;
               ++pcount[t];
               BSS_TRACE_EV(p, tr, 1, 4 * i + 1 + t);
               tc_fence_after();
-              if (!issue_pv(t, sv)) {
-                ok = false;
-                break;
-              }
+              if (!issue_pv(t, sv)) return false;
             }
             if ((nmask >> t) & 1) {
               if (!kready) {
-                if (!wait_bar(bar(C::kBarKFull + skn), ((i + 1) / C::kStagesK) & 1, abort_flag, p.err)) {
-                  ok = false;
-                  break;
-                }
+                if (!wait_bar(bar(C::kBarKFull + skn), ((i + 1) / C::kStagesK) & 1, abort_flag, p.err))
+                  return false;
                 tc_fence_after();
                 kready = true;
               }
-              ok = issue_qk(t, skn, nkb);
+              return issue_qk(t, skn, nkb);
             }
-          }
+            return true;
+          };
+          ok = tile_step(0) && tile_step(1);
           if (!ok) break;
           BSS_TRACE_EV(p, tr, 1, 4 * i + 3);
           mma_commit(bar(C::kBarVEmpty + sv));
@@ -524,6 +520,7 @@ __global__ void __launch_bounds__(384, 1)
           ++i;
         }
         if (!ok) break;
+#pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (ostarted[t]) {
             mma_commit(bar(C::kBarOFull + t));
@@ -567,7 +564,7 @@ __global__ void __launch_bounds__(384, 1)
     while (ok) {
       const FwdItem it = fwd_item<CAUSAL>(item, p);
       const Schedule sch(it, sched_bm, C::kBitmapWords);
-      const int r0 = it.r0[t];
+      const int r0 = t ? it.r0[1] : it.r0[0];
       const int row = r0 + row_in_tile;
 
       float m2 = NEG_INF;     // reference max (log2 units), moved only by > 8

@@ -35,7 +35,8 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import (BWD_8K, CAUSAL_4K, CAUSAL_16K, DENSE_SMALL, SPARSE_16K,  # noqa: E402
+from workloads import (BWD_8K, CAUSAL_4K, CAUSAL_16K, DECODE_16K, DENSE_SMALL,  # noqa: E402
+                       SPARSE_16K,
                        SPLITKV_128K, Workload, chunk_bounds, local_global_random_blocklist,
                        make_inputs)
 
@@ -91,7 +92,7 @@ def load_peaks():
 # DRAM traffic recorded for a kernel is used only while they are unchanged).
 KERNEL_OF_ROW = {
     "fwd": "attn_fwd_kernel (causal, persistent)",
-    "splitkv": "attn_fwd_kernel (partial) x8 + merge_states_kernel",
+    "splitkv": "attn_fwd_kernel (partial, 8 key chunks in one launch) + merge_states_kernel",
     "sparse": "attn_fwd_kernel (block-sparse)",
     "bwd": "attn_bwd_main_kernel (+ preprocess and dq_convert in the same call)",
 }
@@ -211,13 +212,9 @@ class Step:
         self.dev = {k: v.to(dev) for k, v in cpu.items()}
         self.o = torch.empty_like(self.dev["q"])
         self.lse = torch.empty((B, H, L), device=dev)
-        self.chunks = chunk_bounds(L, 8)
-        C = len(self.chunks)
-        self.kc = [self.dev["k"][:, :, s:e].contiguous() for s, e in self.chunks]
-        self.vc = [self.dev["v"][:, :, s:e].contiguous() for s, e in self.chunks]
-        self.m = torch.empty((C, B, H, L), device=dev)
-        self.l = torch.empty_like(self.m)
-        self.acc = torch.empty((C, B, H, L, d), device=dev)
+        self.n_chunks = 8
+        self.ws_split = torch.empty(bss.attn_fwd_splitkv_workspace_bytes(B, H, L, L, d, self.n_chunks),
+                                    device=dev, dtype=torch.uint8)
         self.o_split = torch.empty_like(self.o)
         self.lse_split = torch.empty_like(self.lse)
         nblk = (L + 127) // 128
@@ -243,7 +240,7 @@ class Step:
             "bwd": 10 * d * self.pairs_causal,
         }
         self.total_flops = sum(self.flops.values())
-        self.launches_per_step = 1 + (C + 1) + 1 + 3
+        self.launches_per_step = 1 + 2 + 1 + 3
         self.events = None
 
     def run(self, timed_rows=False):
@@ -255,10 +252,8 @@ class Step:
         if ev is not None:
             ev["fwd"][1].record()
             ev["splitkv"][0].record()
-        for c, (s, _) in enumerate(self.chunks):
-            bss.attn_fwd_partial(d["q"], self.kc[c], self.vc[c], causal=True, scale=w.scale,
-                                 k_offset=s, m=self.m[c], l=self.l[c], acc=self.acc[c])
-        bss.attn_merge_states(self.m, self.l, self.acc, out=self.o_split, lse=self.lse_split)
+        bss.attn_fwd_splitkv(d["q"], d["k"], d["v"], self.n_chunks, causal=True, scale=w.scale,
+                             workspace=self.ws_split, out=self.o_split, lse=self.lse_split)
         if ev is not None:
             ev["splitkv"][1].record()
             ev["sparse"][0].record()
@@ -377,17 +372,45 @@ def measure_configs(bss, dev, peaks):
             bss.attn_fwd_partial(x["q"], kc[c], vc[c], causal=True, scale=w.scale, k_offset=s,
                                  m=m[c], l=l_[c], acc=acc[c])
 
-    ms_p = bench_kernel(partials, reps=3, warmup=1)
+    ms_p = bench_kernel(partials, reps=2, warmup=1)
     ms_m = bench_kernel(lambda: bss.attn_merge_states(m, l_, acc, out=o, lse=lse), reps=10)
+    del m, l_, acc, kc, vc
+    # the same in one split-KV launch (chunks read in place) + merge
+    ws = torch.empty(bss.attn_fwd_splitkv_workspace_bytes(w.B, w.H, w.L, w.L, w.d, w.chunks),
+                     device=dev, dtype=torch.uint8)
+    ms_s = bench_kernel(lambda: bss.attn_fwd_splitkv(x["q"], x["k"], x["v"], w.chunks, causal=True,
+                                                     scale=w.scale, workspace=ws, out=o, lse=lse),
+                        reps=3, warmup=1)
     fl = 4 * w.d * w.B * w.H * causal_pairs(w.L, w.L)
     rows = w.B * w.H * w.L
     nonempty = sum(w.B * w.H * max(0, w.L - s) for s, _ in bounds)
     merge_bytes = C * rows * 8 + nonempty * w.d * 4 + rows * (w.d * 2 + 4)
-    out[w.name] = {"partials_ms": round(ms_p, 3), "merge_ms": round(ms_m, 4),
-                   "tflops": round(fl / (ms_p + ms_m) / 1e9, 1),
+    out[w.name] = {"splitkv_ms": round(ms_s, 3), "tflops": round(fl / ms_s / 1e9, 1),
+                   "per_chunk_launches_ms": round(ms_p + ms_m, 3),
+                   "merge_ms": round(ms_m, 4),
                    "merge_gbs": round(merge_bytes / ms_m / 1e6, 1),
                    "merge_frac_hbm": round(merge_bytes / ms_m / 1e6 / peaks["hbm_gbs"], 4)}
-    del x, kc, vc, m, l_, acc, o, lse
+    del x, o, lse, ws
+    # decode-shaped: 16 queries at the end of a 16384-key causal cache, 16 chunks
+    w = DECODE_16K
+    x = {k: t.to(dev) for k, t in make_inputs(w).items()}
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(w.B, w.H, w.Lq, device=dev)
+    ws = torch.empty(bss.attn_fwd_splitkv_workspace_bytes(w.B, w.H, w.Lq, w.L, w.d, w.chunks),
+                     device=dev, dtype=torch.uint8)
+    qo = w.L - w.Lq
+    ms_d = bench_kernel(lambda: bss.attn_fwd_splitkv(x["q"], x["k"], x["v"], w.chunks, causal=True,
+                                                     scale=w.scale, q_offset=qo, workspace=ws,
+                                                     out=o, lse=lse), reps=20)
+    ms_1 = bench_kernel(lambda: bss.attn_fwd(x["q"], x["k"], x["v"], causal=True, scale=w.scale,
+                                             q_offset=qo, out=o, lse=lse), reps=10)
+    pairs = w.B * w.H * causal_pairs(w.Lq, w.L, q0=qo)
+    kv_bytes = 2 * w.B * w.H * w.L * w.d * 2
+    out[w.name] = {"ms": round(ms_d, 4), "unsplit_ms": round(ms_1, 4),
+                   "tflops": round(4 * w.d * pairs / ms_d / 1e9, 2),
+                   "kv_gbs": round(kv_bytes / ms_d / 1e6, 1),
+                   "kv_frac_hbm": round(kv_bytes / ms_d / 1e6 / peaks["hbm_gbs"], 4)}
+    del x, o, lse, ws
     # fwd + bwd L=8192 d=64
     w = BWD_8K
     x = {k: t.to(dev) for k, t in make_inputs(w).items()}

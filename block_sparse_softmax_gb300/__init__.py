@@ -25,7 +25,7 @@ __all__ = [
     "attn_fwd_blocksparse", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_blocksparse",
     "attn_bwd_blocksparse_workspace_bytes", "attn_bwd_noalloc",
     "attn_poll_status",
-    "attn_watchdog_selftest", "attn_fwd_splitkv", "library",
+    "attn_watchdog_selftest", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes", "library",
 ]
 
 OK = 0
@@ -137,23 +137,34 @@ def attn_merge_states(m: torch.Tensor, l: torch.Tensor, acc: torch.Tensor, *, ou
     return out, lse
 
 
-def attn_fwd_splitkv(q, k, v, chunks: int, *, causal: bool = False, scale: Optional[float] = None):
-    """Exact attention computed as ``chunks`` separate KV chunks (attn_fwd_partial on each)
-    followed by attn_merge_states: the Ring-Attention combine on one GPU."""
-    B, H, L, d = q.shape
+def attn_fwd_splitkv_workspace_bytes(B: int, H: int, Lq: int, Lk: int, d: int, chunks: int) -> int:
+    return int(_lib.load().attn_fwd_splitkv_workspace_bytes(B, H, Lq, Lk, d, chunks))
+
+
+def attn_fwd_splitkv(q, k, v, chunks: int, *, causal: bool = False, scale: Optional[float] = None,
+                     q_offset: int = 0, k_offset: int = 0, workspace: Optional[torch.Tensor] = None,
+                     out=None, lse=None):
+    """Exact attention with the keys cut into ``chunks`` chunks (each a multiple of
+    128 keys) whose partial states are computed in one launch and merged: the
+    split-KV / decode-shaped forward (the Ring-Attention combine on one GPU)."""
+    B, H, Lq, d = q.shape
     Lk = k.shape[2]
-    step = (Lk + chunks - 1) // chunks
-    bounds = [(s, min(Lk, s + step)) for s in range(0, Lk, step)]
-    C = len(bounds)
-    m = torch.empty((C, B, H, L), device=q.device, dtype=torch.float32)
-    l = torch.empty_like(m)
-    acc = torch.empty((C, B, H, L, d), device=q.device, dtype=torch.float32)
-    for c, (s, e) in enumerate(bounds):
-        kc = k[:, :, s:e].contiguous() if chunks > 1 else k
-        vc = v[:, :, s:e].contiguous() if chunks > 1 else v
-        attn_fwd_partial(q, kc, vc, causal=causal, scale=scale, k_offset=s, m=m[c], l=l[c],
-                         acc=acc[c])
-    return attn_merge_states(m, l, acc)
+    _need(q, "q", torch.bfloat16, (B, H, Lq, d))
+    _need(k, "k", torch.bfloat16, (B, H, Lk, d))
+    _need(v, "v", torch.bfloat16, (B, H, Lk, d))
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32) if lse is None else lse
+    _need(out, "out", torch.bfloat16, (B, H, Lq, d))
+    _need(lse, "lse", torch.float32, (B, H, Lq))
+    nbytes = attn_fwd_splitkv_workspace_bytes(B, H, Lq, Lk, d, chunks)
+    if workspace is None:
+        workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
+    st = _lib.load().attn_fwd_splitkv(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), B, H, Lq, Lk, d,
+        _scale(scale, d), int(causal), int(q_offset), int(k_offset), int(chunks), _stream_of(q))
+    _check(st, "attn_fwd_splitkv")
+    return out, lse
 
 
 def attn_blocklist_normalize(row_ptr, col_idx, n_kblk: int) -> Tuple[np.ndarray, np.ndarray]:

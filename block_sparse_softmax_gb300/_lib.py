@@ -27,6 +27,12 @@ _SIGNATURES = {
     "attn_merge_states": (_C.c_int, [_C.c_int, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                      _C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int, _C.c_int,
                                      _C.c_int, _C.c_void_p]),
+    "attn_fwd_splitkv_workspace_bytes": (_C.c_size_t, [_C.c_int, _C.c_int, _C.c_int, _C.c_int,
+                                                       _C.c_int, _C.c_int]),
+    "attn_fwd_splitkv": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
+                                    _C.c_void_p, _C.c_void_p, _C.c_size_t, _C.c_int, _C.c_int,
+                                    _C.c_int, _C.c_int, _C.c_int, _C.c_float, _C.c_int,
+                                    _C.c_int64, _C.c_int64, _C.c_int, _C.c_void_p]),
     "attn_blocklist_normalize": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int,
                                             _C.c_void_p, _C.c_void_p, _C.c_void_p]),
     "attn_fwd_blocksparse": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,

@@ -163,7 +163,12 @@ attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int
   p.k_offset = k_offset;
   p.causal = causal ? 1 : 0;
   p.n_pairs = (Lq + 255) / 256;
-  p.n_items = B * H * p.n_pairs;
+  if (p.n_chunks <= 0) {            // no key split: one chunk holding every key
+    p.n_chunks = 1;
+    p.chunk_len = Lk;
+  }
+  if (static_cast<long long>(p.n_chunks) * B * H * p.n_pairs > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
+  p.n_items = p.n_chunks * B * H * p.n_pairs;
 #ifdef BSS_TRACE
   p.trace = g_trace_buf;
   p.trace_cta = g_trace_cta;
@@ -288,6 +293,27 @@ attn_status_t bwd_common(const void* q, const void* k, const void* v, const void
                                                    static_cast<cudaStream_t>(stream)));
 }
 
+// Split-KV forward: keys in chunks of a multiple of 128, each chunk's partial
+// states in the workspace as acc [C, B*H*Lq, d] | m [C, B*H*Lq] | l [C, B*H*Lq]
+// (each part at a 256-byte boundary).
+struct SplitLayout {
+  int chunk_len, chunks;
+  size_t rows, acc_off, m_off, l_off, bytes;
+};
+SplitLayout split_layout(int B, int H, int Lq, int Lk, int d, int n_chunks) {
+  SplitLayout s{};
+  const long long per = (static_cast<long long>(Lk) + n_chunks - 1) / n_chunks;
+  s.chunk_len = static_cast<int>(per <= 0 ? 128 : ((per + 127) / 128) * 128);
+  s.chunks = Lk <= 0 ? 1 : static_cast<int>((static_cast<long long>(Lk) + s.chunk_len - 1) / s.chunk_len);
+  s.rows = static_cast<size_t>(B) * H * (Lq < 0 ? 0 : Lq);
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  s.acc_off = 0;
+  s.m_off = up(s.chunks * s.rows * static_cast<size_t>(d) * 4);
+  s.l_off = s.m_off + up(s.chunks * s.rows * 4);
+  s.bytes = s.l_off + up(s.chunks * s.rows * 4);
+  return s;
+}
+
 }  // namespace
 }  // namespace bss
 
@@ -334,6 +360,35 @@ attn_status_t attn_fwd_partial(const void* q, const void* k, const void* v, floa
   p.acc_out = acc;
   return fwd_common(q, k, v, B, H, Lq, Lk, d, scale, causal, q_offset, k_offset, false, true, p,
                     stream);
+}
+
+size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Lq, int Lk, int d, int n_chunks) {
+  if (B < 1 || H < 1 || Lq < 0 || Lk < 0 || d < 1 || n_chunks < 1 || n_chunks > 64) return 0;
+  return split_layout(B, H, Lq, Lk, d, n_chunks).bytes;
+}
+
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               void* workspace, size_t workspace_bytes, int B, int H, int Lq,
+                               int Lk, int d, float scale, int causal, int64_t q_offset,
+                               int64_t k_offset, int n_chunks, void* stream) {
+  if (n_chunks < 1 || n_chunks > 64) return ATTN_ERR_INVALID_ARG;
+  if (!o || !lse || !aligned16(o) || !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
+  attn_status_t s = check_common(B, H, Lq, Lk, d, scale);
+  if (s != ATTN_OK) return s;
+  const SplitLayout lay = split_layout(B, H, Lq, Lk, d, n_chunks);
+  if (!workspace || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < lay.bytes) return ATTN_ERR_WORKSPACE;
+  if (Lq == 0) return ATTN_OK;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  FwdParams p{};
+  p.acc_out = reinterpret_cast<float*>(ws + lay.acc_off);
+  p.m_out = reinterpret_cast<float*>(ws + lay.m_off);
+  p.l_out = reinterpret_cast<float*>(ws + lay.l_off);
+  p.n_chunks = lay.chunks;
+  p.chunk_len = lay.chunk_len;
+  s = fwd_common(q, k, v, B, H, Lq, Lk, d, scale, causal, q_offset, k_offset, false, true, p, stream);
+  if (s != ATTN_OK) return s;
+  return attn_merge_states(lay.chunks, p.m_out, p.l_out, p.acc_out, o, lse, B, H, Lq, d, stream);
 }
 
 attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o,

@@ -156,7 +156,9 @@ struct FwdParams {
   const int* col_idx;
   int n_qblk, nnz;
   int n_pairs;             // query-row pairs per head: ceil(Lq / 256)
-  int n_items;             // work items (= CTAs launched): B * H * n_pairs
+  int n_chunks;            // key chunks, each with its own partial state (1: none)
+  int chunk_len;           // keys per chunk (a multiple of 128 when n_chunks > 1)
+  int n_items;             // work items (= CTAs launched): n_chunks * B * H * n_pairs
   int* err;
   long long* trace;        // trace builds only (nullptr otherwise)
   int trace_cta;

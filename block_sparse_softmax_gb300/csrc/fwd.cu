@@ -111,29 +111,42 @@ struct FwdRegs {
 // see the most keys) comes first, so that the longest items start first.
 struct FwdItem {
   int b, h, bh;
+  int c;           // key chunk (0 without a split)
+  int kbase;       // row of the chunk's first key in K and V
+  int Lkc;         // keys in the chunk
+  long long koff;  // absolute position of the chunk's first key (causal mask)
   int r0[2];       // first query row of each tile
-  int kbmax[2];    // last key block each tile can see (-1: none)
+  int kbmax[2];    // last key block (of the chunk) each tile can see (-1: none)
 };
 
+// Items are numbered row-pair-major, then key chunk, then head: under a
+// causal mask the last pair (whose rows see the most keys) comes first, and
+// the heads of one pair and chunk sit side by side.
 template <bool CAUSAL>
 __device__ __forceinline__ FwdItem fwd_item(int item, const FwdParams& p) {
   FwdItem it;
   const int BH = p.B * p.H;
-  const int rank = item / BH;
-  it.bh = item - rank * BH;
+  const int per_rank = BH * p.n_chunks;
+  const int rank = item / per_rank;
+  const int rem = item - rank * per_rank;
+  it.c = rem / BH;
+  it.bh = rem - it.c * BH;
   it.b = it.bh / p.H;
   it.h = it.bh - it.b * p.H;
+  it.kbase = it.c * p.chunk_len;
+  it.Lkc = min(p.chunk_len, p.Lk - it.kbase);
+  it.koff = p.k_offset + it.kbase;
   const int pair = CAUSAL ? (p.n_pairs - 1 - rank) : rank;
   it.r0[0] = pair * 2 * kTileM;
   it.r0[1] = it.r0[0] + kTileM;
-  const int nk = (p.Lk + kTileN - 1) / kTileN;
+  const int nk = it.Lkc > 0 ? (it.Lkc + kTileN - 1) / kTileN : 0;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    if (it.r0[t] >= p.Lq) {
+    if (it.r0[t] >= p.Lq || nk == 0) {
       it.kbmax[t] = -1;
     } else if (CAUSAL) {
       const long long r_last = min(it.r0[t] + kTileM - 1, p.Lq - 1);
-      const long long lim = r_last + p.q_offset - p.k_offset;
+      const long long lim = r_last + p.q_offset - it.koff;
       it.kbmax[t] = lim < 0 ? -1 : static_cast<int>(lim / kTileN < nk - 1 ? lim / kTileN : nk - 1);
     } else {
       it.kbmax[t] = nk - 1;
@@ -348,7 +361,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(bar(C::kBarKFull + sk), C::kTileBytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_4d(ks + c * C::kChunkBytes, &tmK, bar(C::kBarKFull + sk), c * 64, kb * kTileN,
+            tma_load_4d(ks + c * C::kChunkBytes, &tmK, bar(C::kBarKFull + sk), c * 64, it.kbase + kb * kTileN,
                         it.h, it.b);
           ++ik;
           const int sv = iv % C::kStagesV;
@@ -362,7 +375,7 @@ __global__ void __launch_bounds__(384, 1)
           mbar_arrive_expect_tx(bar(C::kBarVFull + sv), C::kTileBytes);
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_4d(vs + c * C::kChunkBytes, &tmV, bar(C::kBarVFull + sv), c * 64, kb * kTileN,
+            tma_load_4d(vs + c * C::kChunkBytes, &tmV, bar(C::kBarVFull + sv), c * 64, it.kbase + kb * kTileN,
                         it.h, it.b);
           ++iv;
           kb = nkb;
@@ -588,12 +601,12 @@ __global__ void __launch_bounds__(384, 1)
 
         // element mask: only where the block crosses the diagonal or the end
         const int kstart = kb * kTileN;
-        const bool edge = (kstart + kTileN > p.Lk) ||
-                          (CAUSAL && (static_cast<long long>(kstart) + kTileN - 1 + p.k_offset >
+        const bool edge = (kstart + kTileN > it.Lkc) ||
+                          (CAUSAL && (static_cast<long long>(kstart) + kTileN - 1 + it.koff >
                                       static_cast<long long>(r0) + p.q_offset));
         if (edge) {
-          long long lim = static_cast<long long>(p.Lk) - 1 - kstart;
-          if (CAUSAL) lim = min(lim, static_cast<long long>(row) + p.q_offset - p.k_offset - kstart);
+          long long lim = static_cast<long long>(it.Lkc) - 1 - kstart;
+          if (CAUSAL) lim = min(lim, static_cast<long long>(row) + p.q_offset - it.koff - kstart);
           const int jl = static_cast<int>(max(-1ll, min(127ll, lim)));
 #pragma unroll
           for (int c = 0; c < 4; ++c)
@@ -688,9 +701,11 @@ __global__ void __launch_bounds__(384, 1)
       }
       BSS_TRACE_EV(p, trw, 4 + t, 2 * n);
       const bool inb = row < p.Lq;
-      const size_t row_g = static_cast<size_t>(it.bh) * p.Lq + (inb ? row : 0);
+      // partial states of chunk c follow those of chunks 0 .. c-1
+      const size_t rows0 = static_cast<size_t>(it.c) * p.B * p.H * p.Lq + static_cast<size_t>(it.bh) * p.Lq;
+      const size_t row_g = rows0 + (inb ? row : 0);
       // first row of this warp (rows past Lq are masked out of `valid`)
-      const size_t wrow0 = static_cast<size_t>(it.bh) * p.Lq + (r0 + wq * 32);
+      const size_t wrow0 = rows0 + (r0 + wq * 32);
       if (PARTIAL) {
         // An empty state (m = -inf) is fully described by m and l; its acc
         // row is not written (a merge never reads it).

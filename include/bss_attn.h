@@ -101,6 +101,36 @@ attn_status_t attn_merge_states(int C, const float* m, const float* l, const flo
                                 void* o, float* lse, int B, int H, int L, int d, void* stream);
 
 /*
+ * attn_fwd_splitkv_workspace_bytes - workspace of attn_fwd_splitkv: the fp32
+ * partial states (m, l, acc) of every key chunk, 0 for invalid arguments.
+ */
+size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Lq, int Lk, int d, int n_chunks);
+
+/*
+ * attn_fwd_splitkv - exact attention with the keys split into chunks whose
+ * partial states are computed in one launch and then merged: the split-KV
+ * (decode-shaped) forward.
+ * "Exact Blocks, Rings, and Sparsity", section 4 (each Ring step folds one KV
+ * block into the state (m, l, A); the merge is associative and order-free)
+ * and section 2 (the merge invariant).
+ *   Arguments and results as attn_fwd; n_chunks in [1, 64].  The keys are cut
+ *   into chunks of ceil(Lk / n_chunks) keys rounded up to a multiple of 128
+ *   (so there may be fewer chunks than asked), each read in place from k and
+ *   v.  A chunk wholly in the causal future of a query tile is skipped for
+ *   that tile (its state is empty and the merge ignores it).  Meant for
+ *   shapes with few query tiles against many keys, e.g. decoding: Lq of one
+ *   to a few hundred queries against a long cache, q_offset = Lk - Lq under a
+ *   causal mask.
+ *   workspace: device, 16-byte aligned, >= attn_fwd_splitkv_workspace_bytes
+ *   bytes; contents on entry irrelevant.  Two launches on the stream: the
+ *   partial states, then attn_merge_states.
+ */
+attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                               void* workspace, size_t workspace_bytes, int B, int H, int Lq,
+                               int Lk, int d, float scale, int causal, int64_t q_offset,
+                               int64_t k_offset, int n_chunks, void* stream);
+
+/*
  * attn_blocklist_normalize - HOST function: canonical form of a CSR block list.
  * Block-sparse attention patterns page, 'Count active blocks and acknowledge the
  * changed operator' (duplicate entries never count twice; order carries no meaning).

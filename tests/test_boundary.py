@@ -126,6 +126,15 @@ def test_argument_errors_return_codes_before_any_device_work(lib):
     ws = lib.attn_bwd_workspace_bytes(2, 3, 100, 64)
     assert ws == 2 * 3 * 100 * 64 * 4
     assert lib.attn_bwd(P, P, P, P, P, P, P, P, P, P, P, ws - 4, 2, 3, 100, 64, 0.125, 1, None) == 6
+    # split-KV forward: chunks of ceil(Lk / n) keys rounded up to 128; workspace =
+    # acc | m | l of every chunk, each part at a 256-byte boundary
+    wsk = lib.attn_fwd_splitkv_workspace_bytes(2, 3, 100, 1000, 64, 4)
+    assert wsk == 4 * 600 * 64 * 4 + 2 * 9728
+    assert lib.attn_fwd_splitkv_workspace_bytes(2, 3, 100, 1000, 64, 65) == 0
+    kv = lambda n=4, ws_=wsk: (P, P, P, P, P, P, ws_, 2, 3, 100, 1000, 64, 0.125, 1, 900, 0, n, None)
+    assert lib.attn_fwd_splitkv(*kv(n=0)) == 1                   # chunk count out of range
+    assert lib.attn_fwd_splitkv(*kv(n=65)) == 1
+    assert lib.attn_fwd_splitkv(*kv(ws_=wsk - 4)) == 6           # workspace too small
     # block-sparse backward: workspace = accumulator (256-byte aligned) + bitmap
     # of ceil(L/128) columns of ceil(ceil(L/128)/32) words
     wss = lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64)

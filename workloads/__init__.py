@@ -45,6 +45,7 @@ class Workload:
     chunks: int = 1          # split-KV chunks merged afterwards
     backward: bool = False
     description: str = ""
+    Lq: Optional[int] = None  # decode-shaped: only the last Lq rows of the draw are queries
 
     @property
     def scale(self) -> float:
@@ -73,7 +74,15 @@ BWD_8K = Workload("fwdbwd_B8_H16_L8192_d64", 8, 16, 8192, 64, True, 4, backward=
 CAUSAL_16K = Workload("causal_B2_H16_L16384_d128", 2, 16, 16384, 128, True, 1,
                       description="dense causal forward at L=16384, d=128 (B=2 H=16)")
 
-ALL = [DENSE_SMALL, CAUSAL_4K, SPARSE_16K, SPLITKV_128K, BWD_8K, CAUSAL_16K]
+# Decode-shaped split-KV forward (the Ring combine's other use): the queries
+# are the last 16 positions of the draw (q_offset = L - 16, causal) against a
+# 16384-key cache cut into 16 chunks.
+DECODE_16K = Workload("decode_B4_H16_Lq16_Lk16384_d128", 4, 16, 16384, 128, True, 5, chunks=16,
+                      Lq=16,
+                      description="decode-shaped forward: 16 queries at the end of a 16384-key "
+                                  "causal cache, 16 KV chunks merged")
+
+ALL = [DENSE_SMALL, CAUSAL_4K, SPARSE_16K, SPLITKV_128K, BWD_8K, CAUSAL_16K, DECODE_16K]
 BY_NAME = {w.name: w for w in ALL}
 
 
@@ -102,7 +111,10 @@ def make_inputs(w: Workload, L: Optional[int] = None, B: Optional[int] = None,
     n = 4 if w.backward else 3
     ts = randn_bf16((B, H, L, w.d), w.seed, n, w.value_scale)
     names = ["q", "k", "v", "do"][:n]
-    return dict(zip(names, ts))
+    out = dict(zip(names, ts))
+    if w.Lq is not None:                 # decode-shaped: queries are the last Lq positions
+        out["q"] = out["q"][:, :, L - w.Lq:].contiguous()
+    return out
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:

@@ -25,7 +25,8 @@ __all__ = [
     "attn_fwd_blocksparse", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_blocksparse",
     "attn_bwd_blocksparse_workspace_bytes", "attn_bwd_noalloc",
     "attn_poll_status",
-    "attn_watchdog_selftest", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes", "library",
+    "attn_watchdog_selftest", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
+    "attn_select_blocks", "library",
 ]
 
 OK = 0
@@ -167,6 +168,33 @@ def attn_fwd_splitkv(q, k, v, chunks: int, *, causal: bool = False, scale: Optio
     return out, lse
 
 
+def attn_select_blocks(q, k, top_r: int, *, local_blocks: int = 1, causal: bool = True,
+                       n_lists: int = 1, scale: Optional[float] = None, block: int = 128,
+                       workspace: Optional[torch.Tensor] = None):
+    """Block lists from mean-pooled scores: (row_ptr [n_lists, n+1], col_idx) int32 on
+    q's device, the input of attn_fwd_blocksparse / attn_bwd_blocksparse."""
+    B, H, L, d = q.shape
+    _need(q, "q", torch.bfloat16, (B, H, L, d))
+    _need(k, "k", torch.bfloat16, (B, H, L, d))
+    lib = _lib.load()
+    n = (L + block - 1) // block
+    nnz = int(lib.attn_select_blocks_nnz(L, top_r, local_blocks, int(causal), n_lists))
+    if nnz < 0:
+        raise AttnError(ERR_INVALID_ARG, "attn_select_blocks: invalid arguments")
+    row_ptr = torch.empty((n_lists, n + 1), device=q.device, dtype=torch.int32)
+    col_idx = torch.empty(max(1, nnz), device=q.device, dtype=torch.int32)
+    nbytes = int(lib.attn_select_blocks_workspace_bytes(B, H, L, d))
+    if workspace is None:
+        workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
+    st = lib.attn_select_blocks(q.data_ptr(), k.data_ptr(), B, H, L, d, _scale(scale, d),
+                                int(causal), int(block), int(top_r), int(local_blocks),
+                                int(n_lists), row_ptr.data_ptr(), col_idx.data_ptr(),
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream_of(q))
+    _check(st, "attn_select_blocks")
+    return row_ptr, col_idx[:nnz]
+
+
 def attn_blocklist_normalize(row_ptr, col_idx, n_kblk: int) -> Tuple[np.ndarray, np.ndarray]:
     """Canonical CSR (ascending, duplicates removed), computed by the library on the host."""
     rp = np.ascontiguousarray(np.asarray(row_ptr, dtype=np.int32))
@@ -183,15 +211,20 @@ def attn_blocklist_normalize(row_ptr, col_idx, n_kblk: int) -> Tuple[np.ndarray,
 
 
 def _csr_on_device(row_ptr, col_idx, device):
-    """int32 CSR on the tensors' device; an empty col_idx gets a one-element
+    """int32 CSR on the tensors' device as (row_ptr, col_idx, nnz, n_lists,
+    n_qblk).  A 1-D row_ptr is one list shared by every head; a 2-D
+    [n_lists, n_qblk + 1] row_ptr holds one list per group of heads, each
+    with offsets into the one col_idx.  An empty col_idx gets a one-element
     placeholder (never read) so that its pointer is valid."""
     rp = torch.as_tensor(np.asarray(row_ptr, dtype=np.int32) if not torch.is_tensor(row_ptr)
                          else row_ptr).to(device=device, dtype=torch.int32).contiguous()
     ci = torch.as_tensor(np.asarray(col_idx, dtype=np.int32) if not torch.is_tensor(col_idx)
                          else col_idx).to(device=device, dtype=torch.int32).contiguous()
+    n_lists = 1 if rp.dim() == 1 else rp.shape[0]
+    n_qblk = rp.shape[-1] - 1
     if ci.numel() == 0:
-        return rp, torch.zeros(1, device=device, dtype=torch.int32), 0
-    return rp, ci, ci.numel()
+        return rp, torch.zeros(1, device=device, dtype=torch.int32), 0, n_lists, n_qblk
+    return rp, ci, ci.numel(), n_lists, n_qblk
 
 
 def attn_fwd_blocksparse(q, k, v, row_ptr, col_idx, *, causal: bool = False,
@@ -201,14 +234,14 @@ def attn_fwd_blocksparse(q, k, v, row_ptr, col_idx, *, causal: bool = False,
     _need(q, "q", torch.bfloat16, (B, H, L, d))
     _need(k, "k", torch.bfloat16, (B, H, L, d))
     _need(v, "v", torch.bfloat16, (B, H, L, d))
-    rp, ci, nnz = _csr_on_device(row_ptr, col_idx, q.device)
+    rp, ci, nnz, n_lists, n_qblk = _csr_on_device(row_ptr, col_idx, q.device)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, L), device=q.device, dtype=torch.float32) if lse is None else lse
     _need(out, "out", torch.bfloat16, (B, H, L, d))
     _need(lse, "lse", torch.float32, (B, H, L))
     st = _lib.load().attn_fwd_blocksparse(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, L, d,
-        _scale(scale, d), int(causal), int(block), rp.data_ptr(), ci.data_ptr(), rp.numel() - 1,
+        _scale(scale, d), int(causal), int(block), rp.data_ptr(), ci.data_ptr(), n_lists, n_qblk,
         nnz, _stream_of(q))
     _check(st, "attn_fwd_blocksparse")
     return out, lse
@@ -241,8 +274,8 @@ def attn_bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: Optional[flo
     return dq, dk, dv, delta
 
 
-def attn_bwd_blocksparse_workspace_bytes(B: int, H: int, L: int, d: int) -> int:
-    return int(_lib.load().attn_bwd_blocksparse_workspace_bytes(B, H, L, d))
+def attn_bwd_blocksparse_workspace_bytes(B: int, H: int, L: int, d: int, n_lists: int = 1) -> int:
+    return int(_lib.load().attn_bwd_blocksparse_workspace_bytes(B, H, L, d, n_lists))
 
 
 def attn_bwd_blocksparse(q, k, v, o, lse, dout, row_ptr, col_idx, *, causal: bool = False,
@@ -254,19 +287,19 @@ def attn_bwd_blocksparse(q, k, v, o, lse, dout, row_ptr, col_idx, *, causal: boo
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
         _need(t, name, torch.bfloat16, (B, H, L, d))
     _need(lse, "lse", torch.float32, (B, H, L))
-    rp, ci, nnz = _csr_on_device(row_ptr, col_idx, q.device)
+    rp, ci, nnz, n_lists, n_qblk = _csr_on_device(row_ptr, col_idx, q.device)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     delta = torch.empty((B, H, L), device=q.device, dtype=torch.float32) if delta is None else delta
-    nbytes = attn_bwd_blocksparse_workspace_bytes(B, H, L, d)
+    nbytes = attn_bwd_blocksparse_workspace_bytes(B, H, L, d, n_lists)
     if workspace is None:
         workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
     st = _lib.load().attn_bwd_blocksparse(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), B, H, L, d, _scale(scale, d), int(causal),
-        int(block), rp.data_ptr(), ci.data_ptr(), rp.numel() - 1, nnz, _stream_of(q))
+        int(block), rp.data_ptr(), ci.data_ptr(), n_lists, n_qblk, nnz, _stream_of(q))
     _check(st, "attn_bwd_blocksparse")
     return dq, dk, dv, delta
 

@@ -33,25 +33,31 @@ _SIGNATURES = {
                                     _C.c_void_p, _C.c_void_p, _C.c_size_t, _C.c_int, _C.c_int,
                                     _C.c_int, _C.c_int, _C.c_int, _C.c_float, _C.c_int,
                                     _C.c_int64, _C.c_int64, _C.c_int, _C.c_void_p]),
+    "attn_select_blocks_workspace_bytes": (_C.c_size_t, [_C.c_int, _C.c_int, _C.c_int, _C.c_int]),
+    "attn_select_blocks_nnz": (_C.c_int64, [_C.c_int, _C.c_int, _C.c_int, _C.c_int, _C.c_int]),
+    "attn_select_blocks": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int, _C.c_int,
+                                      _C.c_int, _C.c_float, _C.c_int, _C.c_int, _C.c_int,
+                                      _C.c_int, _C.c_int, _C.c_void_p, _C.c_void_p, _C.c_void_p,
+                                      _C.c_size_t, _C.c_void_p]),
     "attn_blocklist_normalize": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int,
                                             _C.c_void_p, _C.c_void_p, _C.c_void_p]),
     "attn_fwd_blocksparse": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                         _C.c_void_p, _C.c_int, _C.c_int, _C.c_int, _C.c_int,
                                         _C.c_float, _C.c_int, _C.c_int, _C.c_void_p, _C.c_void_p,
-                                        _C.c_int, _C.c_int, _C.c_void_p]),
+                                        _C.c_int, _C.c_int, _C.c_int, _C.c_void_p]),
     "attn_bwd_workspace_bytes": (_C.c_size_t, [_C.c_int, _C.c_int, _C.c_int, _C.c_int]),
     "attn_bwd": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                             _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                             _C.c_void_p, _C.c_size_t, _C.c_int, _C.c_int, _C.c_int, _C.c_int,
                             _C.c_float, _C.c_int, _C.c_void_p]),
     "attn_bwd_blocksparse_workspace_bytes": (_C.c_size_t, [_C.c_int, _C.c_int, _C.c_int,
-                                                           _C.c_int]),
+                                                           _C.c_int, _C.c_int]),
     "attn_bwd_blocksparse": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                         _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                         _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_size_t,
                                         _C.c_int, _C.c_int, _C.c_int, _C.c_int, _C.c_float,
                                         _C.c_int, _C.c_int, _C.c_void_p, _C.c_void_p, _C.c_int,
-                                        _C.c_int, _C.c_void_p]),
+                                        _C.c_int, _C.c_int, _C.c_void_p]),
     "attn_bwd_noalloc": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                     _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                     _C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int, _C.c_int,

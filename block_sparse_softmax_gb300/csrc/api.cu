@@ -220,6 +220,14 @@ attn_status_t noalloc_scratch(float** out) {
 // Workspace of the block-sparse backward: the fp32 dQ accumulator, then (at a
 // 256-byte boundary) the key-major bitmap of the block list.
 size_t bwd_bitmap_offset(size_t acc_bytes) { return (acc_bytes + 255) & ~static_cast<size_t>(255); }
+// Heads per block list: n_lists lists share the B*H heads in consecutive
+// groups (1 list: every head uses it); 0 when n_lists does not divide B*H.
+long long heads_per_list(int B, int H, int n_lists) {
+  const long long bh = static_cast<long long>(B) * H;
+  if (n_lists < 1 || bh % n_lists != 0) return 0;
+  return bh / n_lists;
+}
+
 size_t bwd_bitmap_bytes(int L) {
   const size_t nblk = (static_cast<size_t>(L < 0 ? 0 : L) + 127) / 128;
   return nblk * ((nblk + 31) / 32) * 4;
@@ -230,8 +238,8 @@ size_t bwd_bitmap_bytes(int L) {
 attn_status_t bwd_common(const void* q, const void* k, const void* v, const void* o,
                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
                          float* delta, void* workspace, int B, int H, int L, int d, float scale,
-                         int causal, const int32_t* row_ptr, const int32_t* col_idx, int nnz,
-                         void* stream) {
+                         int causal, const int32_t* row_ptr, const int32_t* col_idx, int n_lists,
+                         int nnz, void* stream) {
   attn_status_t s = check_common(B, H, L, L, d, scale);
   if (s != ATTN_OK) return s;
   const void* ptrs16[] = {q, k, v, o, dout, dq, dk, dv, workspace};
@@ -283,8 +291,9 @@ attn_status_t bwd_common(const void* q, const void* k, const void* v, const void
                                                bwd_bitmap_offset(attn_bwd_workspace_bytes(B, H, L, d)));
     p.col_bitmap = bm;
     p.col_bitmap_words = (nblk + 31) / 32;
+    p.heads_per_list = static_cast<int>(heads_per_list(B, H, n_lists));
     s = cuda_status("attn_bwd_blocksparse block-list transpose",
-                    launch_blocklist_columns(row_ptr, col_idx, nblk, nnz, causal, bm,
+                    launch_blocklist_columns(row_ptr, col_idx, n_lists, nblk, nnz, causal, bm,
                                              p.col_bitmap_words, p.err,
                                              static_cast<cudaStream_t>(stream)));
     if (s != ATTN_OK) return s;
@@ -394,13 +403,15 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
 attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o,
                                    float* lse, int B, int H, int L, int d, float scale, int causal,
                                    int block, const int32_t* row_ptr, const int32_t* col_idx,
-                                   int n_qblk, int nnz, void* stream) {
+                                   int n_lists, int n_qblk, int nnz, void* stream) {
   if (!o || !lse || !aligned16(o) || !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
   if (block != 128) return ATTN_ERR_UNSUPPORTED;
   if (L < 0) return ATTN_ERR_INVALID_ARG;
   const long long nblk = (static_cast<long long>(L) + 127) / 128;
   if (nblk > kMaxKBlocks) return ATTN_ERR_UNSUPPORTED;
   if (n_qblk != nblk || nnz < 0) return ATTN_ERR_BAD_BLOCKLIST;
+  const long long hpl = heads_per_list(B, H, n_lists);
+  if (hpl == 0) return ATTN_ERR_BAD_BLOCKLIST;
   if (!row_ptr || (nnz > 0 && !col_idx) || !aligned4(row_ptr) || !aligned4(col_idx))
     return ATTN_ERR_INVALID_ARG;
   FwdParams p{};
@@ -410,6 +421,7 @@ attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, 
   p.col_idx = col_idx;
   p.n_qblk = n_qblk;
   p.nnz = nnz;
+  p.heads_per_list = static_cast<int>(hpl);
   return fwd_common(q, k, v, B, H, L, L, d, scale, causal, 0, 0, true, false, p, stream);
 }
 
@@ -433,6 +445,46 @@ attn_status_t attn_merge_states(int C, const float* m, const float* l, const flo
   p.lse = lse;
   return cuda_status("attn_merge_states launch",
                      launch_merge(d, p, err, static_cast<cudaStream_t>(stream)));
+}
+
+size_t attn_select_blocks_workspace_bytes(int B, int H, int L, int d) {
+  if (B < 1 || H < 1 || L < 0 || d < 1) return 0;
+  const size_t n = (static_cast<size_t>(L) + 127) / 128;
+  const size_t pooled = static_cast<size_t>(B) * H * n * d * 4;
+  return 2 * ((pooled + 255) & ~static_cast<size_t>(255)) + (n + 1) * 4;
+}
+
+int64_t attn_select_blocks_nnz(int L, int top_r, int local_blocks, int causal, int n_lists) {
+  if (L < 0 || top_r < 0 || local_blocks < 0 || n_lists < 1) return -1;
+  return static_cast<int64_t>(n_lists) * select_row_entries(L, top_r, local_blocks, causal ? 1 : 0);
+}
+
+attn_status_t attn_select_blocks(const void* q, const void* k, int B, int H, int L, int d,
+                                 float scale, int causal, int block, int top_r, int local_blocks,
+                                 int n_lists, int32_t* row_ptr, int32_t* col_idx, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  attn_status_t s = check_common(B, H, L, L, d, scale);
+  if (s != ATTN_OK) return s;
+  if (block != 128) return ATTN_ERR_UNSUPPORTED;
+  if (top_r < 0 || local_blocks < 0 || top_r + local_blocks > 256) return ATTN_ERR_INVALID_ARG;
+  const long long n = (static_cast<long long>(L) + 127) / 128;
+  if (n > kMaxKBlocks) return ATTN_ERR_UNSUPPORTED;
+  const long long hpl = heads_per_list(B, H, n_lists);
+  if (hpl == 0) return ATTN_ERR_BAD_BLOCKLIST;
+  if ((hpl * d + n) * 4 > 200 * 1024) return ATTN_ERR_UNSUPPORTED;   // the selection CTA's smem
+  if (!q || !k || !aligned16(q) || !aligned16(k) || !row_ptr || !aligned4(row_ptr)) return ATTN_ERR_INVALID_ARG;
+  if (!col_idx || !aligned4(col_idx) || !workspace || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_select_blocks_workspace_bytes(B, H, L, d)) return ATTN_ERR_WORKSPACE;
+  if (L == 0) return ATTN_OK;
+  const size_t pooled = static_cast<size_t>(B) * H * n * d * 4;
+  const size_t pooled_up = (pooled + 255) & ~static_cast<size_t>(255);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  return cuda_status("attn_select_blocks launch",
+                     launch_select(d, q, k, B, H, L, n_lists, top_r, local_blocks, causal ? 1 : 0,
+                                   scale, row_ptr, col_idx, reinterpret_cast<float*>(ws),
+                                   reinterpret_cast<float*>(ws + pooled_up),
+                                   reinterpret_cast<int*>(ws + 2 * pooled_up),
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 attn_status_t attn_blocklist_normalize(const int32_t* row_ptr, const int32_t* col_idx, int n_qblk,
@@ -466,10 +518,10 @@ size_t attn_bwd_workspace_bytes(int B, int H, int L, int d) {
   return static_cast<size_t>(B) * H * static_cast<size_t>(L) * d * sizeof(float);
 }
 
-size_t attn_bwd_blocksparse_workspace_bytes(int B, int H, int L, int d) {
+size_t attn_bwd_blocksparse_workspace_bytes(int B, int H, int L, int d, int n_lists) {
   const size_t acc = attn_bwd_workspace_bytes(B, H, L, d);
-  if (acc == 0 && L != 0) return 0;
-  return bwd_bitmap_offset(acc) + bwd_bitmap_bytes(L);
+  if ((acc == 0 && L != 0) || heads_per_list(B, H, n_lists) == 0) return 0;
+  return bwd_bitmap_offset(acc) + static_cast<size_t>(n_lists) * bwd_bitmap_bytes(L);
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -478,25 +530,26 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        int d, float scale, int causal, void* stream) {
   if (workspace_bytes < attn_bwd_workspace_bytes(B, H, L, d)) return ATTN_ERR_WORKSPACE;
   return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, delta, workspace, B, H, L, d, scale, causal,
-                    nullptr, nullptr, 0, stream);
+                    nullptr, nullptr, 1, 0, stream);
 }
 
 attn_status_t attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
                                    const float* lse, const void* dout, void* dq, void* dk,
                                    void* dv, float* delta, void* workspace, size_t workspace_bytes,
                                    int B, int H, int L, int d, float scale, int causal, int block,
-                                   const int32_t* row_ptr, const int32_t* col_idx, int n_qblk,
-                                   int nnz, void* stream) {
+                                   const int32_t* row_ptr, const int32_t* col_idx, int n_lists,
+                                   int n_qblk, int nnz, void* stream) {
   if (block != 128) return ATTN_ERR_UNSUPPORTED;
   if (L < 0) return ATTN_ERR_INVALID_ARG;
   const long long nblk = (static_cast<long long>(L) + 127) / 128;
   if (nblk > kMaxKBlocks) return ATTN_ERR_UNSUPPORTED;
-  if (n_qblk != nblk || nnz < 0) return ATTN_ERR_BAD_BLOCKLIST;
+  if (n_qblk != nblk || nnz < 0 || heads_per_list(B, H, n_lists) == 0) return ATTN_ERR_BAD_BLOCKLIST;
   if (!row_ptr || (nnz > 0 && !col_idx) || !aligned4(row_ptr) || !aligned4(col_idx))
     return ATTN_ERR_INVALID_ARG;
-  if (workspace_bytes < attn_bwd_blocksparse_workspace_bytes(B, H, L, d)) return ATTN_ERR_WORKSPACE;
+  if (workspace_bytes < attn_bwd_blocksparse_workspace_bytes(B, H, L, d, n_lists))
+    return ATTN_ERR_WORKSPACE;
   return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, delta, workspace, B, H, L, d, scale, causal,
-                    row_ptr, col_idx, nnz, stream);
+                    row_ptr, col_idx, n_lists, nnz, stream);
 }
 
 attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,

@@ -198,7 +198,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   if (SPARSE) {
     const int words = (nq + 31) / 32;
     for (int w = tid; w < words; w += C::kThreads)
-      col_bm[w] = __ldg(p.col_bitmap + static_cast<size_t>(j) * p.col_bitmap_words + w);
+      col_bm[w] = __ldg(p.col_bitmap +
+                        (static_cast<size_t>(bh / p.heads_per_list) * nq + j) * p.col_bitmap_words + w);
     __syncthreads();
     for (int w = 0; w < words; ++w) n_it += __popc(col_bm[w]);
   }
@@ -721,21 +722,27 @@ unsigned grid_for(long long work, int per_block) {
   return static_cast<unsigned>(blocks);
 }
 
-// Key-major bitmap of a block list: bit i of column c is set when query block
-// i lists key block c.  Duplicates collapse, the order of a row is irrelevant,
-// and under a causal mask a key block after the query block is left out (it
-// holds no allowed pair).  One thread per query block; malformed rows and
-// entries are skipped and reported.
+// Key-major bitmaps of the block lists: bit i of column c of list l is set
+// when query block i of list l lists key block c.  Duplicates collapse, the
+// order of a row is irrelevant, and under a causal mask a key block after the
+// query block is left out (it holds no allowed pair).  One thread per (list,
+// query block); malformed rows and entries are skipped and reported.
 __global__ void __launch_bounds__(256) attn_blocklist_columns_kernel(
-    const int* row_ptr, const int* col_idx, int n_qblk, int nnz, int causal, uint32_t* bm,
-    int words, int* err) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_qblk; i += gridDim.x * blockDim.x) {
-    const int beg = __ldg(row_ptr + i);
-    const int end = __ldg(row_ptr + i + 1);
+    const int* row_ptr, const int* col_idx, int n_lists, int n_qblk, int nnz, int causal,
+    uint32_t* bm, int words, int* err) {
+  const long long total = static_cast<long long>(n_lists) * n_qblk;
+  for (long long x = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; x < total;
+       x += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int list = static_cast<int>(x / n_qblk);
+    const int i = static_cast<int>(x - static_cast<long long>(list) * n_qblk);
+    const int* rp = row_ptr + static_cast<size_t>(list) * (n_qblk + 1);
+    const int beg = __ldg(rp + i);
+    const int end = __ldg(rp + i + 1);
     if (beg < 0 || end < beg || end > nnz) {
       record_error(err, ATTN_ERR_BAD_BLOCKLIST);
       continue;
     }
+    uint32_t* lbm = bm + static_cast<size_t>(list) * n_qblk * words;
     for (int e = beg; e < end; ++e) {
       const int c = __ldg(col_idx + e);
       if (c < 0 || c >= n_qblk) {
@@ -743,20 +750,21 @@ __global__ void __launch_bounds__(256) attn_blocklist_columns_kernel(
         continue;
       }
       if (causal && c > i) continue;
-      atomicOr(bm + static_cast<size_t>(c) * words + (i >> 5), 1u << (i & 31));
+      atomicOr(lbm + static_cast<size_t>(c) * words + (i >> 5), 1u << (i & 31));
     }
   }
 }
 
 }  // namespace
 
-cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int n_qblk, int nnz,
-                                     int causal, uint32_t* bitmap, int words, int* err,
+cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int n_lists, int n_qblk,
+                                     int nnz, int causal, uint32_t* bitmap, int words, int* err,
                                      cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(bitmap, 0, static_cast<size_t>(n_qblk) * words * 4, st);
+  const size_t bytes = static_cast<size_t>(n_lists) * n_qblk * words * 4;
+  cudaError_t e = cudaMemsetAsync(bitmap, 0, bytes, st);
   if (e != cudaSuccess) return e;
-  attn_blocklist_columns_kernel<<<grid_for(n_qblk, 256), 256, 0, st>>>(row_ptr, col_idx, n_qblk, nnz,
-                                                                      causal, bitmap, words, err);
+  attn_blocklist_columns_kernel<<<grid_for(static_cast<long long>(n_lists) * n_qblk, 256), 256, 0, st>>>(
+      row_ptr, col_idx, n_lists, n_qblk, nnz, causal, bitmap, words, err);
   return cudaGetLastError();
 }
 

@@ -152,9 +152,10 @@ struct FwdParams {
   float* l_out;            // [B,H,Lq]
   float* acc_out;          // [B,H,Lq,d]
   // block-sparse list (device CSR over 128-blocks)
-  const int* row_ptr;
+  const int* row_ptr;      // [n_lists][n_qblk + 1], offsets into col_idx
   const int* col_idx;
   int n_qblk, nnz;
+  int heads_per_list;      // head (b*H + h) uses list (b*H + h) / heads_per_list
   int n_pairs;             // query-row pairs per head: ceil(Lq / 256)
   int n_chunks;            // key chunks, each with its own partial state (1: none)
   int chunk_len;           // keys per chunk (a multiple of 128 when n_chunks > 1)
@@ -189,8 +190,9 @@ struct BwdParams {
   int head_group;          // heads whose key tiles are launched together (see attn_bwd_main_kernel)
   // block-sparse: key-major bitmap of the block list (bit i of column c: query
   // block i lists key block c), col_bitmap_words words per column
-  const uint32_t* col_bitmap;
+  const uint32_t* col_bitmap;   // [n_lists][n_kblk][col_bitmap_words]
   int col_bitmap_words;
+  int heads_per_list;           // head (b*H + h) uses list (b*H + h) / heads_per_list
   int* err;
   long long* trace;        // trace builds only (nullptr otherwise)
   int trace_cta;
@@ -207,8 +209,12 @@ cudaError_t launch_merge(int d, const MergeParams& p, int* err, cudaStream_t st)
 cudaError_t launch_bwd(int d, bool sparse, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                        const BwdParams& p, cudaStream_t st);
-cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int n_qblk, int nnz,
-                                     int causal, uint32_t* bitmap, int words, int* err,
+cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int n_lists, int n_qblk,
+                                     int nnz, int causal, uint32_t* bitmap, int words, int* err,
                                      cudaStream_t st);
 cudaError_t launch_watchdog_selftest(unsigned long long cycles, int* err, cudaStream_t st);
+int select_row_entries(int L, int top_r, int local, int causal);
+cudaError_t launch_select(int d, const void* q, const void* k, int B, int H, int L, int n_lists,
+                          int top_r, int local, int causal, float scale, int* row_ptr, int* col_idx,
+                          float* qbar, float* kbar, int* prefix, cudaStream_t st);
 }  // namespace bss

@@ -279,8 +279,9 @@ __global__ void __launch_bounds__(384, 1)
     for (int t = 0; t < 2; ++t) {
       const int qb = it0.r0[t] / kTileM;
       if (it0.r0[t] >= p.Lq || qb >= p.n_qblk) continue;
-      const int beg = __ldg(p.row_ptr + qb);
-      const int end = __ldg(p.row_ptr + qb + 1);
+      const int* rp = p.row_ptr + static_cast<size_t>(it0.bh / p.heads_per_list) * (p.n_qblk + 1);
+      const int beg = __ldg(rp + qb);
+      const int end = __ldg(rp + qb + 1);
       if (beg < 0 || end < beg || end > p.nnz) {
         if (tid == 0) record_error(p.err, ATTN_ERR_BAD_BLOCKLIST);
         continue;

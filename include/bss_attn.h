@@ -152,8 +152,13 @@ attn_status_t attn_blocklist_normalize(const int32_t* row_ptr, const int32_t* co
  * (drop-and-renormalise); block-sparse attention patterns page (triangular
  * element mask inside diagonal blocks, partial blocks, duplicates, empty rows).
  *   q/k/v/o/lse as attn_fwd with Lq = Lk = L.  block must be 128.
- *   row_ptr [n_qblk+1], col_idx [nnz]: DEVICE int32 CSR, n_qblk = ceil(L/128),
- *   raw form accepted (any order, duplicates counted once).  A listed block
+ *   row_ptr [n_lists][n_qblk+1], col_idx [nnz]: DEVICE int32 CSR, n_qblk =
+ *   ceil(L/128), raw form accepted (any order, duplicates counted once).
+ *   n_lists >= 1 lists share the B*H heads in consecutive groups: head
+ *   (b*H + h) uses list (b*H + h) / (B*H / n_lists), so n_lists must divide
+ *   B*H (1: one list for every head; B*H: one per head; B*H_kv with grouped
+ *   query heads: one per KV head).  Each list's row_ptr holds offsets into
+ *   the one col_idx array (else ATTN_ERR_BAD_BLOCKLIST).  A listed block
  *   wholly in the causal future contributes nothing.  An entry outside
  *   [0, ceil(L/128)) is ignored and reported as ATTN_ERR_BAD_BLOCKLIST by
  *   attn_poll_status; so is a row whose row_ptr range is not inside [0, nnz]
@@ -163,7 +168,37 @@ attn_status_t attn_blocklist_normalize(const int32_t* row_ptr, const int32_t* co
 attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o,
                                    float* lse, int B, int H, int L, int d, float scale,
                                    int causal, int block, const int32_t* row_ptr,
-                                   const int32_t* col_idx, int n_qblk, int nnz, void* stream);
+                                   const int32_t* col_idx, int n_lists, int n_qblk, int nnz,
+                                   void* stream);
+
+/*
+ * attn_select_blocks - block lists for attn_fwd_blocksparse from mean-pooled
+ * scores (a selector that needs no trained weights).
+ * "Exact Blocks, Rings, and Sparsity", section 5 ('Why the sparse unit is
+ * usually a block': the selector must score something cheaper than Q K^T, and
+ * it chooses an exact set: selected blocks united with a mandatory local
+ * window; 'Fixed pooling: a cheap proxy, not the true block mass') and
+ * section 6 (query heads that share a KV head share the block choice).
+ *   q, k [B,H,L,d] bf16 (device).  Per 128-row block the query and key rows
+ *   are averaged (fp32); query block a scores key block c by the sum, over
+ *   the heads that share a list, of scale * qbar_a . kbar_c (the block pair's
+ *   mean logit).  Row a keeps the local window a, a-1, .., a-local_blocks+1
+ *   (those >= 0) and the top_r other candidates (under a causal mask only
+ *   blocks <= a), larger score first, the lower index on equal scores, listed
+ *   in ascending order.  n_lists as in attn_fwd_blocksparse.
+ *   Out (device): row_ptr [n_lists][n+1] (offsets into col_idx),
+ *   col_idx [attn_select_blocks_nnz(...)] int32 - the input format of
+ *   attn_fwd_blocksparse and attn_bwd_blocksparse.
+ *   block must be 128; top_r + local_blocks <= 256; the heads of one list
+ *   times d, plus n, must fit 200 KB of fp32 (else ATTN_ERR_UNSUPPORTED).
+ *   workspace: device, 16-byte aligned, >= attn_select_blocks_workspace_bytes.
+ */
+size_t attn_select_blocks_workspace_bytes(int B, int H, int L, int d);
+int64_t attn_select_blocks_nnz(int L, int top_r, int local_blocks, int causal, int n_lists);
+attn_status_t attn_select_blocks(const void* q, const void* k, int B, int H, int L, int d,
+                                 float scale, int causal, int block, int top_r, int local_blocks,
+                                 int n_lists, int32_t* row_ptr, int32_t* col_idx, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 /*
  * attn_bwd_workspace_bytes - size of the caller-provided workspace of attn_bwd
@@ -190,10 +225,11 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 /*
  * attn_bwd_blocksparse_workspace_bytes - size of the caller-provided workspace
  * of attn_bwd_blocksparse: the fp32 dQ accumulator (B*H*L*d elements, rounded
- * up to 256 bytes) followed by a key-major bitmap of the block list
- * (ceil(L/128) columns of ceil(ceil(L/128)/32) 32-bit words).
+ * up to 256 bytes) followed by a key-major bitmap of each of the n_lists
+ * block lists (ceil(L/128) columns of ceil(ceil(L/128)/32) 32-bit words);
+ * 0 when n_lists does not divide B*H.
  */
-size_t attn_bwd_blocksparse_workspace_bytes(int B, int H, int L, int d);
+size_t attn_bwd_blocksparse_workspace_bytes(int B, int H, int L, int d, int n_lists);
 
 /*
  * attn_bwd_blocksparse - gradients of attn_fwd_blocksparse by recomputation.
@@ -215,8 +251,8 @@ attn_status_t attn_bwd_blocksparse(const void* q, const void* k, const void* v, 
                                    const float* lse, const void* dout, void* dq, void* dk,
                                    void* dv, float* delta, void* workspace, size_t workspace_bytes,
                                    int B, int H, int L, int d, float scale, int causal, int block,
-                                   const int32_t* row_ptr, const int32_t* col_idx, int n_qblk,
-                                   int nnz, void* stream);
+                                   const int32_t* row_ptr, const int32_t* col_idx, int n_lists,
+                                   int n_qblk, int nnz, void* stream);
 
 /*
  * attn_bwd_noalloc - attn_bwd for callers that cannot allocate device memory.

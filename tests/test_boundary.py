@@ -115,10 +115,15 @@ def test_argument_errors_return_codes_before_any_device_work(lib):
     assert lib.attn_fwd(*args(scale=-1.0)) == 1           # non-positive scale
     assert lib.attn_fwd(*args(B=0)) == 1                  # empty batch
     # block size other than 128, CSR row count mismatch, too many key blocks
-    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 256, 64, 0.125, 1, 64, P, P, 2, 4, None) == 2
-    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 256, 64, 0.125, 1, 128, P, P, 3, 4, None) == 3
-    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 4097 * 128, 64, 0.125, 1, 128, P, P,
+    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 256, 64, 0.125, 1, 64, P, P, 1, 2, 4,
+                                    None) == 2
+    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 256, 64, 0.125, 1, 128, P, P, 1, 3, 4,
+                                    None) == 3
+    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 4097 * 128, 64, 0.125, 1, 128, P, P, 1,
                                     4097, 4, None) == 2
+    # lists must divide the B*H heads into equal groups
+    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 2, 3, 256, 64, 0.125, 1, 128, P, P, 4, 2, 4,
+                                    None) == 3
     # merge: chunk count out of range
     assert lib.attn_merge_states(0, P, P, P, P, P, 1, 1, 16, 64, None) == 1
     assert lib.attn_merge_states(65, P, P, P, P, P, 1, 1, 16, 64, None) == 1
@@ -137,11 +142,13 @@ def test_argument_errors_return_codes_before_any_device_work(lib):
     assert lib.attn_fwd_splitkv(*kv(ws_=wsk - 4)) == 6           # workspace too small
     # block-sparse backward: workspace = accumulator (256-byte aligned) + bitmap
     # of ceil(L/128) columns of ceil(ceil(L/128)/32) words
-    wss = lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64)
+    wss = lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64, 1)
     acc = 2 * 3 * 1000 * 64 * 4
     assert wss == ((acc + 255) // 256) * 256 + 8 * 1 * 4
+    assert lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64, 6) == wss + 5 * 8 * 1 * 4
+    assert lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64, 4) == 0   # 4 does not divide 6
     sp = lambda block=128, nq=8, ws_=wss, rp=P: (P, P, P, P, P, P, P, P, P, P, P, ws_, 2, 3, 1000,
-                                                 64, 0.125, 1, block, rp, P, nq, 4, None)
+                                                 64, 0.125, 1, block, rp, P, 1, nq, 4, None)
     assert lib.attn_bwd_blocksparse(*sp(block=64)) == 2          # block size other than 128
     assert lib.attn_bwd_blocksparse(*sp(nq=7)) == 3              # CSR row count mismatch
     assert lib.attn_bwd_blocksparse(*sp(rp=None)) == 1           # missing row_ptr

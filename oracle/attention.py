@@ -30,7 +30,12 @@ Readings where the pages are silent (each also listed in the design notes):
     number);
   * a row with no allowed key has O = 0 and LSE = -inf and gets zero gradient;
   * causal visibility with offsets is ``j + k_offset <= i + q_offset``;
-  * LSE is the natural log of the normaliser of the *scaled* logits.
+  * LSE is the natural log of the normaliser of the *scaled* logits;
+  * grouped key/value heads ([EBRS] §6: under grouped-query attention several
+    query heads share one physical KV head): with H query heads and H_kv key/
+    value heads, H_kv dividing H, query head h reads key/value head
+    h // (H / H_kv) (consecutive groups), and the gradient of a shared key/
+    value head is the sum of the gradients its query heads send it.
 
 Parity status: every function here is pinned by tests against closed forms,
 the pages' worked examples, invariants, a library routine and brute force.
@@ -146,22 +151,32 @@ def forward_head(q, k, v, scale, mask_fn, rows=None, group=256):
     return O, lse
 
 
+def kv_group(H: int, H_kv: int) -> int:
+    """Query heads per key/value head; H_kv must divide H ([EBRS] §6)."""
+    if H_kv < 1 or H % H_kv:
+        raise ValueError(f"{H_kv} key/value heads do not divide {H} query heads")
+    return H // H_kv
+
+
 def attention_forward(q, k, v, scale, *, causal=False, q_offset=0, k_offset=0,
                       block=None, row_ptr=None, col_idx=None, rows=None,
                       heads=None):
-    """O [B,H,R,d] and LSE [B,H,R] for arrays q [B,H,Lq,d], k/v [B,H,Lk,d].
+    """O [B,H,R,d] and LSE [B,H,R] for arrays q [B,H,Lq,d], k/v [B,H_kv,Lk,d].
 
-    ``rows`` restricts the evaluation to a subset of query rows (all heads);
-    ``heads`` to a list of (b, h) pairs (the result then has shape [n, R, ...]).
+    Query head h reads key/value head h // (H / H_kv).  ``rows`` restricts the
+    evaluation to a subset of query rows (all heads); ``heads`` to a list of
+    (b, h) query heads (the result then has shape [n, R, ...]).
     """
     Lk = k.shape[-2]
+    G = kv_group(q.shape[1], k.shape[1])
 
     def mask_fn(r):
         return allowed_rows(r, Lk, causal=causal, q_offset=q_offset, k_offset=k_offset,
                             block=block, row_ptr=row_ptr, col_idx=col_idx)
 
     if heads is not None:
-        outs = [forward_head(q[b, h], k[b, h], v[b, h], scale, mask_fn, rows) for b, h in heads]
+        outs = [forward_head(q[b, h], k[b, h // G], v[b, h // G], scale, mask_fn, rows)
+                for b, h in heads]
         return np.stack([o for o, _ in outs]), np.stack([l for _, l in outs])
     B, H = q.shape[:2]
     R = q.shape[2] if rows is None else len(rows)
@@ -169,7 +184,8 @@ def attention_forward(q, k, v, scale, *, causal=False, q_offset=0, k_offset=0,
     lse = np.zeros((B, H, R))
     for b in range(B):
         for h in range(H):
-            O[b, h], lse[b, h] = forward_head(q[b, h], k[b, h], v[b, h], scale, mask_fn, rows)
+            O[b, h], lse[b, h] = forward_head(q[b, h], k[b, h // G], v[b, h // G], scale,
+                                              mask_fn, rows)
     return O, lse
 
 
@@ -264,11 +280,18 @@ def backward_head(q, k, v, do, scale, M):
 
 def attention_backward(q, k, v, do, scale, *, causal=False, block=None, row_ptr=None,
                        col_idx=None, heads=None):
-    """(dq, dk, dv, D) for [B,H,L,d] arrays (square, offsets 0)."""
+    """(dq, dk, dv, D) for q/do [B,H,L,d] and k/v [B,H_kv,L,d] (square, offsets 0).
+
+    dk and dv of key/value head g add the gradients of its query heads
+    g*G .. g*G+G-1 (G = H / H_kv).  With ``heads`` (a list of (b, h) query
+    heads) the per-query-head terms are returned unsummed, shape [n, L, d].
+    """
     Lq, Lk = q.shape[-2], k.shape[-2]
+    G = kv_group(q.shape[1], k.shape[1])
     M = allowed_mask(Lq, Lk, causal=causal, block=block, row_ptr=row_ptr, col_idx=col_idx)
     if heads is not None:
-        outs = [backward_head(q[b, h], k[b, h], v[b, h], do[b, h], scale, M) for b, h in heads]
+        outs = [backward_head(q[b, h], k[b, h // G], v[b, h // G], do[b, h], scale, M)
+                for b, h in heads]
         return tuple(np.stack([o[i] for o in outs]) for i in range(4))
     B, H = q.shape[:2]
     dq = np.zeros_like(q)
@@ -277,8 +300,10 @@ def attention_backward(q, k, v, do, scale, *, causal=False, block=None, row_ptr=
     D = np.zeros(q.shape[:3])
     for b in range(B):
         for h in range(H):
-            dq[b, h], dk[b, h], dv[b, h], D[b, h] = backward_head(
-                q[b, h], k[b, h], v[b, h], do[b, h], scale, M)
+            dq[b, h], dk_h, dv_h, D[b, h] = backward_head(
+                q[b, h], k[b, h // G], v[b, h // G], do[b, h], scale, M)
+            dk[b, h // G] += dk_h
+            dv[b, h // G] += dv_h
     return dq, dk, dv, D
 
 

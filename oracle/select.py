@@ -68,11 +68,14 @@ def select_row(scores_row, a: int, n_kblk: int, top_r: int, local: int, causal: 
 
 def select_blocks(q, k, scale, *, top_r: int, local: int, causal: bool, n_lists: int,
                   block: int = 128, dtype=np.float32):
-    """Block lists for q, k [B,H,L,d]: ``n_lists`` lists over the B*H heads in
-    consecutive groups (head b*H + h uses list (b*H + h) // (B*H // n_lists)).
+    """Block lists for q [B,H,L,d] and k [B,H_kv,L,d]: ``n_lists`` lists over the
+    B*H query heads in consecutive groups (head b*H + h uses list
+    (b*H + h) // (B*H // n_lists)); query head h pools the keys of key head
+    h // (H / H_kv).
     Returns (row_ptr [n_lists, n+1], col_idx, lists) where row_ptr holds
     offsets into the one col_idx array and ``lists`` the per-list rows."""
     B, H, L, _ = q.shape
+    G = H // k.shape[1]
     n = (L + block - 1) // block
     hpl = B * H // n_lists
     lists = []
@@ -80,7 +83,7 @@ def select_blocks(q, k, scale, *, top_r: int, local: int, causal: bool, n_lists:
         S = np.zeros((n, n), dtype=dtype)
         for x in range(lst * hpl, (lst + 1) * hpl):
             b, h = divmod(x, H)
-            S = (S + pooled_scores(q[b, h], k[b, h], scale, block, dtype)).astype(dtype)
+            S = (S + pooled_scores(q[b, h], k[b, h // G], scale, block, dtype)).astype(dtype)
         lists.append([select_row(S[a], a, n, top_r, local, causal) for a in range(n)])
     rps, cols, off = [], [], 0
     for rows in lists:

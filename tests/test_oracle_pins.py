@@ -466,3 +466,69 @@ def test_local_global_random_pattern_counts():
     raw, uniq = len(ci), sum(len(s) for s in sets)
     assert raw > uniq     # duplicates present in the raw list
     assert 800 < uniq < 900 and 850 < raw < 900
+
+
+# ---------------------------------------------------------------------------
+# Grouped key/value heads ([EBRS] §6: query heads sharing one KV head)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (6, 1), (3, 3)])
+def test_grouped_heads_match_torch_sdpa_with_gqa(H, Hkv):
+    """Library routine: torch SDPA with enable_gqa (query head h reads KV head
+    h // (H / H_kv)), forward and autograd gradients; the shared head's dK/dV
+    is the sum over its query heads."""
+    B, L, d = 2, 33, 5
+    q, do = _rand((B, H, L, d), 100), _rand((B, H, L, d), 101)
+    k, v = _rand((B, Hkv, L, d), 102), _rand((B, Hkv, L, d), 103)
+    scale = 0.45
+    M = oracle.allowed_mask(L, L, causal=True)
+    O, lse = oracle.attention_forward(q, k, v, scale, causal=True)
+    dq, dk, dv, D = oracle.attention_backward(q, k, v, do, scale, causal=True)
+    tq, tk, tv = (torch.from_numpy(a.copy()).requires_grad_() for a in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk, tv, attn_mask=torch.from_numpy(M), scale=scale, enable_gqa=True)
+    out.backward(torch.from_numpy(do))
+    assert np.allclose(O, out.detach().numpy(), atol=1e-12)
+    assert np.allclose(dq, tq.grad.numpy(), atol=1e-11)
+    assert np.allclose(dk, tk.grad.numpy(), atol=1e-11)
+    assert np.allclose(dv, tv.grad.numpy(), atol=1e-11)
+    G = H // Hkv
+    for b, h in itertools.product(range(B), range(H)):
+        assert np.allclose(lse[b, h], _lse_lib(q[b, h], k[b, h // G], scale, M), atol=1e-12)
+
+
+def test_grouped_heads_gradient_by_finite_differences():
+    """Brute force: a shared key/value head perturbed once moves the outputs of
+    every query head of its group, so its gradient is the group's sum."""
+    B, H, Hkv, L, d, h = 1, 2, 1, 5, 2, 1e-6
+    q, do = _rand((B, H, L, d), 110), _rand((B, H, L, d), 111)
+    k, v = _rand((B, Hkv, L, d), 112), _rand((B, Hkv, L, d), 113)
+    M = oracle.allowed_mask(L, L, causal=True).tolist()
+    scale = 0.9
+
+    def loss(k_, v_):
+        tot = 0.0
+        for hq in range(H):
+            O, _ = _scalar_attention(q[0, hq].tolist(), k_[0, 0].tolist(), v_[0, 0].tolist(),
+                                     scale, M)
+            tot += float((O * do[0, hq]).sum())
+        return tot
+
+    _, dk, dv, _ = oracle.attention_backward(q, k, v, do, scale, causal=True)
+    for arr, grad, which in ((k, dk, 0), (v, dv, 1)):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            args = [k.copy(), v.copy()]
+            args[which][idx] += h
+            fp = loss(*args)
+            args[which][idx] -= 2 * h
+            fm = loss(*args)
+            num[idx] = (fp - fm) / (2 * h)
+        assert np.allclose(grad, num, atol=1e-7), which
+
+
+def test_kv_heads_must_divide_query_heads():
+    with pytest.raises(ValueError):
+        oracle.kv_group(6, 4)
+    with pytest.raises(ValueError):
+        oracle.kv_group(2, 0)

@@ -98,3 +98,18 @@ def test_shared_lists_add_the_heads_scores():
     _, _, per_head = sel.select_blocks(q, k, scale, top_r=1, local=1, causal=True, n_lists=2)
     S1 = sel.pooled_scores(q[0, 1], k[0, 1], scale)
     assert per_head[1] == [sel.select_row(S1[a], a, n, 1, 1, True) for a in range(n)]
+
+
+def test_grouped_heads_pool_their_shared_key_head():
+    """Query heads 0, 1 share key head 0 and heads 2, 3 key head 1: a list over
+    each pair adds the two query heads' scores against that pair's key head."""
+    rng = np.random.default_rng(4)
+    B, H, Hkv, L, d, scale = 1, 4, 2, 640, 8, 0.3
+    q = rng.standard_normal((B, H, L, d)).astype(np.float32)
+    k = rng.standard_normal((B, Hkv, L, d)).astype(np.float32)
+    _, _, lists = sel.select_blocks(q, k, scale, top_r=2, local=1, causal=False, n_lists=2)
+    n = (L + 127) // 128
+    for lst, kh in ((0, 0), (1, 1)):
+        S = (sel.pooled_scores(q[0, 2 * lst], k[0, kh], scale)
+             + sel.pooled_scores(q[0, 2 * lst + 1], k[0, kh], scale))
+        assert lists[lst] == [sel.select_row(S[a], a, n, 2, 1, False) for a in range(n)]

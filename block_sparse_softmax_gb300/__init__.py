@@ -81,18 +81,19 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
              scale: Optional[float] = None, q_offset: int = 0, k_offset: int = 0,
              out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None
              ) -> Tuple[torch.Tensor, torch.Tensor]:
-    """O [B,H,Lq,d] bf16 and LSE [B,H,Lq] fp32 of exact (optionally causal) attention."""
+    """O [B,H,Lq,d] bf16 and LSE [B,H,Lq] fp32 of exact (optionally causal) attention.
+    k and v may have fewer heads than q (grouped query heads)."""
     B, H, Lq, d = q.shape
-    Lk = k.shape[2]
+    Hkv, Lk = k.shape[1], k.shape[2]
     _need(q, "q", torch.bfloat16, (B, H, Lq, d))
-    _need(k, "k", torch.bfloat16, (B, H, Lk, d))
-    _need(v, "v", torch.bfloat16, (B, H, Lk, d))
+    _need(k, "k", torch.bfloat16, (B, Hkv, Lk, d))
+    _need(v, "v", torch.bfloat16, (B, Hkv, Lk, d))
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32) if lse is None else lse
     _need(out, "out", torch.bfloat16, (B, H, Lq, d))
     _need(lse, "lse", torch.float32, (B, H, Lq))
     st = _lib.load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                              lse.data_ptr(), B, H, Lq, Lk, d, _scale(scale, d), int(causal),
+                              lse.data_ptr(), B, H, Hkv, Lq, Lk, d, _scale(scale, d), int(causal),
                               int(q_offset), int(k_offset), _stream_of(q))
     _check(st, "attn_fwd")
     return out, lse
@@ -102,10 +103,10 @@ def attn_fwd_partial(q, k, v, *, causal: bool = False, scale: Optional[float] = 
                      q_offset: int = 0, k_offset: int = 0, m=None, l=None, acc=None):
     """Unnormalised state (m, l, acc) of the query rows over one KV chunk."""
     B, H, Lq, d = q.shape
-    Lk = k.shape[2]
+    Hkv, Lk = k.shape[1], k.shape[2]
     _need(q, "q", torch.bfloat16, (B, H, Lq, d))
-    _need(k, "k", torch.bfloat16, (B, H, Lk, d))
-    _need(v, "v", torch.bfloat16, (B, H, Lk, d))
+    _need(k, "k", torch.bfloat16, (B, Hkv, Lk, d))
+    _need(v, "v", torch.bfloat16, (B, Hkv, Lk, d))
     dev = q.device
     m = torch.empty((B, H, Lq), device=dev, dtype=torch.float32) if m is None else m
     l = torch.empty((B, H, Lq), device=dev, dtype=torch.float32) if l is None else l
@@ -114,7 +115,7 @@ def attn_fwd_partial(q, k, v, *, causal: bool = False, scale: Optional[float] = 
     _need(l, "l", torch.float32, (B, H, Lq))
     _need(acc, "acc", torch.float32, (B, H, Lq, d))
     st = _lib.load().attn_fwd_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), m.data_ptr(),
-                                      l.data_ptr(), acc.data_ptr(), B, H, Lq, Lk, d,
+                                      l.data_ptr(), acc.data_ptr(), B, H, Hkv, Lq, Lk, d,
                                       _scale(scale, d), int(causal), int(q_offset), int(k_offset),
                                       _stream_of(q))
     _check(st, "attn_fwd_partial")
@@ -149,10 +150,10 @@ def attn_fwd_splitkv(q, k, v, chunks: int, *, causal: bool = False, scale: Optio
     128 keys) whose partial states are computed in one launch and merged: the
     split-KV / decode-shaped forward (the Ring-Attention combine on one GPU)."""
     B, H, Lq, d = q.shape
-    Lk = k.shape[2]
+    Hkv, Lk = k.shape[1], k.shape[2]
     _need(q, "q", torch.bfloat16, (B, H, Lq, d))
-    _need(k, "k", torch.bfloat16, (B, H, Lk, d))
-    _need(v, "v", torch.bfloat16, (B, H, Lk, d))
+    _need(k, "k", torch.bfloat16, (B, Hkv, Lk, d))
+    _need(v, "v", torch.bfloat16, (B, Hkv, Lk, d))
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32) if lse is None else lse
     _need(out, "out", torch.bfloat16, (B, H, Lq, d))
@@ -162,8 +163,8 @@ def attn_fwd_splitkv(q, k, v, chunks: int, *, causal: bool = False, scale: Optio
         workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
     st = _lib.load().attn_fwd_splitkv(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-        workspace.data_ptr(), workspace.numel() * workspace.element_size(), B, H, Lq, Lk, d,
-        _scale(scale, d), int(causal), int(q_offset), int(k_offset), int(chunks), _stream_of(q))
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), B, H, Hkv, Lq, Lk,
+        d, _scale(scale, d), int(causal), int(q_offset), int(k_offset), int(chunks), _stream_of(q))
     _check(st, "attn_fwd_splitkv")
     return out, lse
 
@@ -174,8 +175,9 @@ def attn_select_blocks(q, k, top_r: int, *, local_blocks: int = 1, causal: bool 
     """Block lists from mean-pooled scores: (row_ptr [n_lists, n+1], col_idx) int32 on
     q's device, the input of attn_fwd_blocksparse / attn_bwd_blocksparse."""
     B, H, L, d = q.shape
+    Hkv = k.shape[1]
     _need(q, "q", torch.bfloat16, (B, H, L, d))
-    _need(k, "k", torch.bfloat16, (B, H, L, d))
+    _need(k, "k", torch.bfloat16, (B, Hkv, L, d))
     lib = _lib.load()
     n = (L + block - 1) // block
     nnz = int(lib.attn_select_blocks_nnz(L, top_r, local_blocks, int(causal), n_lists))
@@ -186,7 +188,7 @@ def attn_select_blocks(q, k, top_r: int, *, local_blocks: int = 1, causal: bool 
     nbytes = int(lib.attn_select_blocks_workspace_bytes(B, H, L, d))
     if workspace is None:
         workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
-    st = lib.attn_select_blocks(q.data_ptr(), k.data_ptr(), B, H, L, d, _scale(scale, d),
+    st = lib.attn_select_blocks(q.data_ptr(), k.data_ptr(), B, H, Hkv, L, d, _scale(scale, d),
                                 int(causal), int(block), int(top_r), int(local_blocks),
                                 int(n_lists), row_ptr.data_ptr(), col_idx.data_ptr(),
                                 workspace.data_ptr(), workspace.numel() * workspace.element_size(),
@@ -231,17 +233,18 @@ def attn_fwd_blocksparse(q, k, v, row_ptr, col_idx, *, causal: bool = False,
                          scale: Optional[float] = None, block: int = 128, out=None, lse=None):
     """Attention over per-query-block CSR lists of key blocks (raw form accepted)."""
     B, H, L, d = q.shape
+    Hkv = k.shape[1]
     _need(q, "q", torch.bfloat16, (B, H, L, d))
-    _need(k, "k", torch.bfloat16, (B, H, L, d))
-    _need(v, "v", torch.bfloat16, (B, H, L, d))
+    _need(k, "k", torch.bfloat16, (B, Hkv, L, d))
+    _need(v, "v", torch.bfloat16, (B, Hkv, L, d))
     rp, ci, nnz, n_lists, n_qblk = _csr_on_device(row_ptr, col_idx, q.device)
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, L), device=q.device, dtype=torch.float32) if lse is None else lse
     _need(out, "out", torch.bfloat16, (B, H, L, d))
     _need(lse, "lse", torch.float32, (B, H, L))
     st = _lib.load().attn_fwd_blocksparse(
-        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, L, d,
-        _scale(scale, d), int(causal), int(block), rp.data_ptr(), ci.data_ptr(), n_lists, n_qblk,
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Hkv, L,
+        d, _scale(scale, d), int(causal), int(block), rp.data_ptr(), ci.data_ptr(), n_lists, n_qblk,
         nnz, _stream_of(q))
     _check(st, "attn_fwd_blocksparse")
     return out, lse
@@ -255,8 +258,11 @@ def attn_bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: Optional[flo
              workspace: Optional[torch.Tensor] = None, dq=None, dk=None, dv=None, delta=None):
     """Gradients (dq, dk, dv) bf16 and delta = rowsum(dO * O) fp32, by recomputation."""
     B, H, L, d = q.shape
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+    Hkv = k.shape[1]
+    for name, t in (("q", q), ("o", o), ("dout", dout)):
         _need(t, name, torch.bfloat16, (B, H, L, d))
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, (B, Hkv, L, d))
     _need(lse, "lse", torch.float32, (B, H, L))
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -268,8 +274,8 @@ def attn_bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: Optional[flo
     st = _lib.load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                               lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
                               dv.data_ptr(), delta.data_ptr(), workspace.data_ptr(),
-                              workspace.numel() * workspace.element_size(), B, H, L, d,
-                              _scale(scale, d), int(causal), _stream_of(q))
+                              workspace.numel() * workspace.element_size(), B, H, Hkv, L,
+                              d, _scale(scale, d), int(causal), _stream_of(q))
     _check(st, "attn_bwd")
     return dq, dk, dv, delta
 
@@ -284,8 +290,11 @@ def attn_bwd_blocksparse(q, k, v, o, lse, dout, row_ptr, col_idx, *, causal: boo
                          delta=None):
     """Gradients of attn_fwd_blocksparse with the same block list (raw CSR accepted)."""
     B, H, L, d = q.shape
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+    Hkv = k.shape[1]
+    for name, t in (("q", q), ("o", o), ("dout", dout)):
         _need(t, name, torch.bfloat16, (B, H, L, d))
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, (B, Hkv, L, d))
     _need(lse, "lse", torch.float32, (B, H, L))
     rp, ci, nnz, n_lists, n_qblk = _csr_on_device(row_ptr, col_idx, q.device)
     dq = torch.empty_like(q) if dq is None else dq
@@ -298,8 +307,8 @@ def attn_bwd_blocksparse(q, k, v, o, lse, dout, row_ptr, col_idx, *, causal: boo
     st = _lib.load().attn_bwd_blocksparse(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), B, H, L, d, _scale(scale, d), int(causal),
-        int(block), rp.data_ptr(), ci.data_ptr(), n_lists, n_qblk, nnz, _stream_of(q))
+        workspace.numel() * workspace.element_size(), B, H, Hkv, L, d, _scale(scale, d),
+        int(causal), int(block), rp.data_ptr(), ci.data_ptr(), n_lists, n_qblk, nnz, _stream_of(q))
     _check(st, "attn_bwd_blocksparse")
     return dq, dk, dv, delta
 
@@ -315,8 +324,11 @@ def attn_bwd_noalloc(q, k, v, o, lse, dout, *, causal: bool = False,
     race; the first call on a device should come before any stream capture.
     Outputs not given are allocated here by PyTorch, as for every other binding."""
     B, H, L, d = q.shape
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+    Hkv = k.shape[1]
+    for name, t in (("q", q), ("o", o), ("dout", dout)):
         _need(t, name, torch.bfloat16, (B, H, L, d))
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, (B, Hkv, L, d))
     _need(lse, "lse", torch.float32, (B, H, L))
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
@@ -324,8 +336,8 @@ def attn_bwd_noalloc(q, k, v, o, lse, dout, *, causal: bool = False,
     delta = torch.empty((B, H, L), device=q.device, dtype=torch.float32) if delta is None else delta
     st = _lib.load().attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                       lse.data_ptr(), dout.data_ptr(), dq.data_ptr(),
-                                      dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), B, H, L, d,
-                                      _scale(scale, d), int(causal), _stream_of(q))
+                                      dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), B, H, Hkv,
+                                      L, d, _scale(scale, d), int(causal), _stream_of(q))
     _check(st, "attn_bwd_noalloc")
     return dq, dk, dv, delta
 

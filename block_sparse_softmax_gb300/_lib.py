@@ -18,12 +18,12 @@ _SIGNATURES = {
     "attn_last_error_message": (_C.c_char_p, []),
     "attn_version": (_C.c_int, []),
     "attn_fwd": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
-                            _C.c_int, _C.c_int, _C.c_int, _C.c_int, _C.c_int, _C.c_float,
-                            _C.c_int, _C.c_int64, _C.c_int64, _C.c_void_p]),
+                            _C.c_int, _C.c_int, _C.c_int, _C.c_int, _C.c_int, _C.c_int,
+                            _C.c_float, _C.c_int, _C.c_int64, _C.c_int64, _C.c_void_p]),
     "attn_fwd_partial": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                     _C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int, _C.c_int,
-                                    _C.c_int, _C.c_int, _C.c_float, _C.c_int, _C.c_int64,
-                                    _C.c_int64, _C.c_void_p]),
+                                    _C.c_int, _C.c_int, _C.c_int, _C.c_float, _C.c_int,
+                                    _C.c_int64, _C.c_int64, _C.c_void_p]),
     "attn_merge_states": (_C.c_int, [_C.c_int, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                      _C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int, _C.c_int,
                                      _C.c_int, _C.c_void_p]),
@@ -31,37 +31,37 @@ _SIGNATURES = {
                                                        _C.c_int, _C.c_int]),
     "attn_fwd_splitkv": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                     _C.c_void_p, _C.c_void_p, _C.c_size_t, _C.c_int, _C.c_int,
-                                    _C.c_int, _C.c_int, _C.c_int, _C.c_float, _C.c_int,
+                                    _C.c_int, _C.c_int, _C.c_int, _C.c_int, _C.c_float, _C.c_int,
                                     _C.c_int64, _C.c_int64, _C.c_int, _C.c_void_p]),
     "attn_select_blocks_workspace_bytes": (_C.c_size_t, [_C.c_int, _C.c_int, _C.c_int, _C.c_int]),
     "attn_select_blocks_nnz": (_C.c_int64, [_C.c_int, _C.c_int, _C.c_int, _C.c_int, _C.c_int]),
     "attn_select_blocks": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int, _C.c_int,
-                                      _C.c_int, _C.c_float, _C.c_int, _C.c_int, _C.c_int,
-                                      _C.c_int, _C.c_int, _C.c_void_p, _C.c_void_p, _C.c_void_p,
-                                      _C.c_size_t, _C.c_void_p]),
+                                      _C.c_int, _C.c_int, _C.c_float, _C.c_int, _C.c_int,
+                                      _C.c_int, _C.c_int, _C.c_int, _C.c_void_p, _C.c_void_p,
+                                      _C.c_void_p, _C.c_size_t, _C.c_void_p]),
     "attn_blocklist_normalize": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int,
                                             _C.c_void_p, _C.c_void_p, _C.c_void_p]),
     "attn_fwd_blocksparse": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                         _C.c_void_p, _C.c_int, _C.c_int, _C.c_int, _C.c_int,
-                                        _C.c_float, _C.c_int, _C.c_int, _C.c_void_p, _C.c_void_p,
-                                        _C.c_int, _C.c_int, _C.c_int, _C.c_void_p]),
+                                        _C.c_int, _C.c_float, _C.c_int, _C.c_int, _C.c_void_p,
+                                        _C.c_void_p, _C.c_int, _C.c_int, _C.c_int, _C.c_void_p]),
     "attn_bwd_workspace_bytes": (_C.c_size_t, [_C.c_int, _C.c_int, _C.c_int, _C.c_int]),
     "attn_bwd": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                             _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                             _C.c_void_p, _C.c_size_t, _C.c_int, _C.c_int, _C.c_int, _C.c_int,
-                            _C.c_float, _C.c_int, _C.c_void_p]),
+                            _C.c_int, _C.c_float, _C.c_int, _C.c_void_p]),
     "attn_bwd_blocksparse_workspace_bytes": (_C.c_size_t, [_C.c_int, _C.c_int, _C.c_int,
                                                            _C.c_int, _C.c_int]),
     "attn_bwd_blocksparse": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                         _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                         _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_size_t,
-                                        _C.c_int, _C.c_int, _C.c_int, _C.c_int, _C.c_float,
-                                        _C.c_int, _C.c_int, _C.c_void_p, _C.c_void_p, _C.c_int,
-                                        _C.c_int, _C.c_int, _C.c_void_p]),
+                                        _C.c_int, _C.c_int, _C.c_int, _C.c_int, _C.c_int,
+                                        _C.c_float, _C.c_int, _C.c_int, _C.c_void_p, _C.c_void_p,
+                                        _C.c_int, _C.c_int, _C.c_int, _C.c_void_p]),
     "attn_bwd_noalloc": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                     _C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                     _C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int, _C.c_int,
-                                    _C.c_int, _C.c_float, _C.c_int, _C.c_void_p]),
+                                    _C.c_int, _C.c_int, _C.c_float, _C.c_int, _C.c_void_p]),
     "attn_poll_status": (_C.c_int, [_C.c_void_p]),
     "attn_watchdog_selftest": (_C.c_int, [_C.c_ulonglong, _C.c_void_p]),
 }

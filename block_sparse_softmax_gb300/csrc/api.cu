@@ -124,6 +124,10 @@ attn_status_t make_map_f32(CUtensorMap* map, void* ptr, int B, int H, long long 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
+// K/V heads: 1 <= Hkv <= H and Hkv divides H (query head h reads K/V head
+// h / (H / Hkv)).
+bool valid_kv_heads(int H, int Hkv) { return Hkv >= 1 && Hkv <= H && H % Hkv == 0; }
+
 attn_status_t check_common(int B, int H, long long Lq, long long Lk, int d, float scale) {
   if (B < 1 || H < 1 || Lq < 0 || Lk < 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
@@ -139,12 +143,13 @@ attn_status_t cuda_status(const char* where, cudaError_t e) {
   return ATTN_ERR_CUDA;
 }
 
-attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int H, int Lq,
-                         int Lk, int d, float scale, int causal, long long q_offset,
+attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int H, int Hkv,
+                         int Lq, int Lk, int d, float scale, int causal, long long q_offset,
                          long long k_offset, bool sparse, bool partial, FwdParams& p,
                          void* stream) {
   attn_status_t s = check_common(B, H, Lq, Lk, d, scale);
   if (s != ATTN_OK) return s;
+  if (!valid_kv_heads(H, Hkv)) return ATTN_ERR_INVALID_ARG;
   if (q_offset < 0 || k_offset < 0) return ATTN_ERR_INVALID_ARG;
   if (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v)) return ATTN_ERR_INVALID_ARG;
   if (Lq == 0) return ATTN_OK;
@@ -152,10 +157,11 @@ attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int
   if ((s = status_word(&p.err)) != ATTN_OK) return s;
   CUtensorMap tq, tk, tv;
   if ((s = make_map(&tq, q, B, H, Lq, d)) != ATTN_OK) return s;
-  if ((s = make_map(&tk, k, B, H, Lk, d)) != ATTN_OK) return s;
-  if ((s = make_map(&tv, v, B, H, Lk, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tk, k, B, Hkv, Lk, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tv, v, B, Hkv, Lk, d)) != ATTN_OK) return s;
   p.B = B;
   p.H = H;
+  p.Hkv = Hkv;
   p.Lq = Lq;
   p.Lk = Lk;
   p.scale_log2 = scale * kLog2e;
@@ -237,11 +243,12 @@ size_t bwd_bitmap_bytes(int L) {
 // or causal); the workspace size has been checked by the caller.
 attn_status_t bwd_common(const void* q, const void* k, const void* v, const void* o,
                          const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                         float* delta, void* workspace, int B, int H, int L, int d, float scale,
+                         float* delta, void* workspace, int B, int H, int Hkv, int L, int d, float scale,
                          int causal, const int32_t* row_ptr, const int32_t* col_idx, int n_lists,
                          int nnz, void* stream) {
   attn_status_t s = check_common(B, H, L, L, d, scale);
   if (s != ATTN_OK) return s;
+  if (!valid_kv_heads(H, Hkv)) return ATTN_ERR_INVALID_ARG;
   const void* ptrs16[] = {q, k, v, o, dout, dq, dk, dv, workspace};
   for (const void* ptr : ptrs16)
     if (!ptr || !aligned16(ptr)) return ATTN_ERR_INVALID_ARG;
@@ -252,12 +259,13 @@ attn_status_t bwd_common(const void* q, const void* k, const void* v, const void
   if ((s = status_word(&p.err)) != ATTN_OK) return s;
   CUtensorMap tq, tk, tv, tdo, tdq;
   if ((s = make_map(&tq, q, B, H, L, d)) != ATTN_OK) return s;
-  if ((s = make_map(&tk, k, B, H, L, d)) != ATTN_OK) return s;
-  if ((s = make_map(&tv, v, B, H, L, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tk, k, B, Hkv, L, d)) != ATTN_OK) return s;
+  if ((s = make_map(&tv, v, B, Hkv, L, d)) != ATTN_OK) return s;
   if ((s = make_map(&tdo, dout, B, H, L, d)) != ATTN_OK) return s;
   if ((s = make_map_f32(&tdq, workspace, B, H, L, d)) != ATTN_OK) return s;
   p.B = B;
   p.H = H;
+  p.Hkv = Hkv;
   p.L = L;
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
@@ -270,14 +278,14 @@ attn_status_t bwd_common(const void* q, const void* k, const void* v, const void
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
-  // Heads launched together: about 2 groups run at once, each head holding
-  // Q, dO (bf16) and the dQ accumulator (fp32), 8 L d bytes; keep the pair of
-  // groups near 64 MiB, well inside L2.
+  // K/V heads launched together: about 2 groups run at once, each K/V head
+  // holding Q, dO (bf16) and the dQ accumulator (fp32) of its H/Hkv query
+  // heads, 8 L d bytes each; keep the pair of groups near 64 MiB, well inside L2.
   {
-    const long long per_head = 8ll * L * d;
+    const long long per_head = 8ll * L * d * (H / Hkv);
     long long g = (64ll << 20) / (2 * per_head);
     if (g < 1) g = 1;
-    if (g > static_cast<long long>(B) * H) g = static_cast<long long>(B) * H;
+    if (g > static_cast<long long>(B) * Hkv) g = static_cast<long long>(B) * Hkv;
     p.head_group = static_cast<int>(g);
   }
 #ifdef BSS_TRACE
@@ -292,6 +300,9 @@ attn_status_t bwd_common(const void* q, const void* k, const void* v, const void
     p.col_bitmap = bm;
     p.col_bitmap_words = (nblk + 31) / 32;
     p.heads_per_list = static_cast<int>(heads_per_list(B, H, n_lists));
+    // a K/V key tile walks the lists of all its query heads at once: they must
+    // be one list (lists shared by whole groups of query heads)
+    if (p.heads_per_list % (H / Hkv) != 0) return ATTN_ERR_BAD_BLOCKLIST;
     s = cuda_status("attn_bwd_blocksparse block-list transpose",
                     launch_blocklist_columns(row_ptr, col_idx, n_lists, nblk, nnz, causal, bm,
                                              p.col_bitmap_words, p.err,
@@ -348,27 +359,28 @@ const char* attn_last_error_message(void) { return g_last_error; }
 int attn_version(void) { return 100; }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                       int H, int Lq, int Lk, int d, float scale, int causal, int64_t q_offset,
-                       int64_t k_offset, void* stream) {
+                       int H, int H_kv, int Lq, int Lk, int d, float scale, int causal,
+                       int64_t q_offset, int64_t k_offset, void* stream) {
   if (!o || !lse || !aligned16(o) || !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
   FwdParams p{};
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
-  return fwd_common(q, k, v, B, H, Lq, Lk, d, scale, causal, q_offset, k_offset, false, false, p,
-                    stream);
+  return fwd_common(q, k, v, B, H, H_kv, Lq, Lk, d, scale, causal, q_offset, k_offset, false,
+                    false, p, stream);
 }
 
 attn_status_t attn_fwd_partial(const void* q, const void* k, const void* v, float* m, float* l,
-                               float* acc, int B, int H, int Lq, int Lk, int d, float scale,
-                               int causal, int64_t q_offset, int64_t k_offset, void* stream) {
+                               float* acc, int B, int H, int H_kv, int Lq, int Lk, int d,
+                               float scale, int causal, int64_t q_offset, int64_t k_offset,
+                               void* stream) {
   if (!m || !l || !acc || !aligned4(m) || !aligned4(l) || !aligned16(acc))
     return ATTN_ERR_INVALID_ARG;
   FwdParams p{};
   p.m_out = m;
   p.l_out = l;
   p.acc_out = acc;
-  return fwd_common(q, k, v, B, H, Lq, Lk, d, scale, causal, q_offset, k_offset, false, true, p,
-                    stream);
+  return fwd_common(q, k, v, B, H, H_kv, Lq, Lk, d, scale, causal, q_offset, k_offset, false,
+                    true, p, stream);
 }
 
 size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Lq, int Lk, int d, int n_chunks) {
@@ -377,8 +389,8 @@ size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Lq, int Lk, int d, int
 }
 
 attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
-                               void* workspace, size_t workspace_bytes, int B, int H, int Lq,
-                               int Lk, int d, float scale, int causal, int64_t q_offset,
+                               void* workspace, size_t workspace_bytes, int B, int H, int H_kv,
+                               int Lq, int Lk, int d, float scale, int causal, int64_t q_offset,
                                int64_t k_offset, int n_chunks, void* stream) {
   if (n_chunks < 1 || n_chunks > 64) return ATTN_ERR_INVALID_ARG;
   if (!o || !lse || !aligned16(o) || !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
@@ -395,13 +407,15 @@ attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void
   p.l_out = reinterpret_cast<float*>(ws + lay.l_off);
   p.n_chunks = lay.chunks;
   p.chunk_len = lay.chunk_len;
-  s = fwd_common(q, k, v, B, H, Lq, Lk, d, scale, causal, q_offset, k_offset, false, true, p, stream);
+  s = fwd_common(q, k, v, B, H, H_kv, Lq, Lk, d, scale, causal, q_offset, k_offset, false, true, p,
+                 stream);
   if (s != ATTN_OK) return s;
   return attn_merge_states(lay.chunks, p.m_out, p.l_out, p.acc_out, o, lse, B, H, Lq, d, stream);
 }
 
 attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o,
-                                   float* lse, int B, int H, int L, int d, float scale, int causal,
+                                   float* lse, int B, int H, int H_kv, int L, int d, float scale,
+                                   int causal,
                                    int block, const int32_t* row_ptr, const int32_t* col_idx,
                                    int n_lists, int n_qblk, int nnz, void* stream) {
   if (!o || !lse || !aligned16(o) || !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
@@ -422,7 +436,7 @@ attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, 
   p.n_qblk = n_qblk;
   p.nnz = nnz;
   p.heads_per_list = static_cast<int>(hpl);
-  return fwd_common(q, k, v, B, H, L, L, d, scale, causal, 0, 0, true, false, p, stream);
+  return fwd_common(q, k, v, B, H, H_kv, L, L, d, scale, causal, 0, 0, true, false, p, stream);
 }
 
 attn_status_t attn_merge_states(int C, const float* m, const float* l, const float* acc, void* o,
@@ -459,12 +473,13 @@ int64_t attn_select_blocks_nnz(int L, int top_r, int local_blocks, int causal, i
   return static_cast<int64_t>(n_lists) * select_row_entries(L, top_r, local_blocks, causal ? 1 : 0);
 }
 
-attn_status_t attn_select_blocks(const void* q, const void* k, int B, int H, int L, int d,
+attn_status_t attn_select_blocks(const void* q, const void* k, int B, int H, int H_kv, int L, int d,
                                  float scale, int causal, int block, int top_r, int local_blocks,
                                  int n_lists, int32_t* row_ptr, int32_t* col_idx, void* workspace,
                                  size_t workspace_bytes, void* stream) {
   attn_status_t s = check_common(B, H, L, L, d, scale);
   if (s != ATTN_OK) return s;
+  if (!valid_kv_heads(H, H_kv)) return ATTN_ERR_INVALID_ARG;
   if (block != 128) return ATTN_ERR_UNSUPPORTED;
   if (top_r < 0 || local_blocks < 0 || top_r + local_blocks > 256) return ATTN_ERR_INVALID_ARG;
   const long long n = (static_cast<long long>(L) + 127) / 128;
@@ -480,7 +495,7 @@ attn_status_t attn_select_blocks(const void* q, const void* k, int B, int H, int
   const size_t pooled_up = (pooled + 255) & ~static_cast<size_t>(255);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   return cuda_status("attn_select_blocks launch",
-                     launch_select(d, q, k, B, H, L, n_lists, top_r, local_blocks, causal ? 1 : 0,
+                     launch_select(d, q, k, B, H, H_kv, L, n_lists, top_r, local_blocks, causal ? 1 : 0,
                                    scale, row_ptr, col_idx, reinterpret_cast<float*>(ws),
                                    reinterpret_cast<float*>(ws + pooled_up),
                                    reinterpret_cast<int*>(ws + 2 * pooled_up),
@@ -526,17 +541,18 @@ size_t attn_bwd_blocksparse_workspace_bytes(int B, int H, int L, int d, int n_li
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                       float* delta, void* workspace, size_t workspace_bytes, int B, int H, int L,
-                       int d, float scale, int causal, void* stream) {
+                       float* delta, void* workspace, size_t workspace_bytes, int B, int H,
+                       int H_kv, int L, int d, float scale, int causal, void* stream) {
   if (workspace_bytes < attn_bwd_workspace_bytes(B, H, L, d)) return ATTN_ERR_WORKSPACE;
-  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, delta, workspace, B, H, L, d, scale, causal,
-                    nullptr, nullptr, 1, 0, stream);
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, delta, workspace, B, H, H_kv, L, d, scale,
+                    causal, nullptr, nullptr, 1, 0, stream);
 }
 
 attn_status_t attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
                                    const float* lse, const void* dout, void* dq, void* dk,
                                    void* dv, float* delta, void* workspace, size_t workspace_bytes,
-                                   int B, int H, int L, int d, float scale, int causal, int block,
+                                   int B, int H, int H_kv, int L, int d, float scale, int causal,
+                                   int block,
                                    const int32_t* row_ptr, const int32_t* col_idx, int n_lists,
                                    int n_qblk, int nnz, void* stream) {
   if (block != 128) return ATTN_ERR_UNSUPPORTED;
@@ -548,14 +564,14 @@ attn_status_t attn_bwd_blocksparse(const void* q, const void* k, const void* v, 
     return ATTN_ERR_INVALID_ARG;
   if (workspace_bytes < attn_bwd_blocksparse_workspace_bytes(B, H, L, d, n_lists))
     return ATTN_ERR_WORKSPACE;
-  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, delta, workspace, B, H, L, d, scale, causal,
-                    row_ptr, col_idx, n_lists, nnz, stream);
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, delta, workspace, B, H, H_kv, L, d, scale,
+                    causal, row_ptr, col_idx, n_lists, nnz, stream);
 }
 
 attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                               float* delta, int B, int H, int L, int d, float scale, int causal,
-                               void* stream) {
+                               float* delta, int B, int H, int H_kv, int L, int d, float scale,
+                               int causal, void* stream) {
   if (B < 1 || H < 1 || L < 0) return ATTN_ERR_INVALID_ARG;
   const size_t need = static_cast<size_t>(B) * H * static_cast<size_t>(L) * (d > 0 ? d : 0);
   if (need > kNoAllocScratchFloats) {
@@ -569,7 +585,7 @@ attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, cons
   attn_status_t s = noalloc_scratch(&scratch);
   if (s != ATTN_OK) return s;
   return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, scratch,
-                  kNoAllocScratchFloats * sizeof(float), B, H, L, d, scale, causal, stream);
+                  kNoAllocScratchFloats * sizeof(float), B, H, H_kv, L, d, scale, causal, stream);
 }
 
 attn_status_t attn_poll_status(void* stream) {

@@ -142,6 +142,22 @@ struct QTiles {
   }
 };
 
+// The (query head of the group, query tile) pairs a KV-head key tile meets:
+// the query tiles of every query head that reads this KV head, head by head.
+struct QWalk {
+  QTiles qs;
+  int G;                   // query heads per KV head
+  __device__ __forceinline__ void start(int& g, int& i) const {
+    g = 0;
+    i = qs.first();
+  }
+  // the pair after (g, i); i < 0 at the end
+  __device__ __forceinline__ void advance(int& g, int& i) const {
+    i = qs.next(i);
+    if (i < 0 && ++g < G) i = qs.first();
+  }
+};
+
 template <int D, bool CAUSAL, bool SPARSE>
 __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -178,14 +194,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   // reduce-adds are read-modify-writes in L2 rather than in DRAM.
   const int L = p.L;
   const int nq = (L + kTileM - 1) / kTileM;
-  const int BH = p.B * p.H;
+  // heads here are K/V heads: the CTA owns a key tile of one (b, K/V head)
+  // and meets the query tiles of the G query heads that read it
+  const int BH = p.B * p.Hkv;
+  const int G = p.H / p.Hkv;
   const int grp = static_cast<int>(blockIdx.x) / (p.head_group * nq);
   const int gsz = min(p.head_group, BH - grp * p.head_group);
   const int within = static_cast<int>(blockIdx.x) - grp * p.head_group * nq;
   const int j = within / gsz;                     // key tile owned by this CTA
-  const int bh = grp * p.head_group + (within - j * gsz);
-  const int b = bh / p.H;
-  const int h = bh - b * p.H;
+  const int bh = grp * p.head_group + (within - j * gsz);   // (b, K/V head)
+  const int b = bh / p.Hkv;
+  const int h = bh - b * p.Hkv;                   // K/V head
+  const int hq0 = h * G;                          // first query head of the group
+  const int bhq0 = b * p.H + hq0;
   // Query tiles met by this key tile: under a causal mask none before j.  A
   // block-sparse launch takes them from the key tile's column of the block
   // list (built with the causal cut already applied).
@@ -194,15 +215,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   qs.bm = SPARSE ? col_bm : nullptr;
   qs.first_dense = CAUSAL ? j : 0;
   qs.nq = nq;
-  int n_it = SPARSE ? 0 : nq - qs.first_dense;
+  int n_it = SPARSE ? 0 : nq - qs.first_dense;   // query tiles per query head
   if (SPARSE) {
     const int words = (nq + 31) / 32;
     for (int w = tid; w < words; w += C::kThreads)
       col_bm[w] = __ldg(p.col_bitmap +
-                        (static_cast<size_t>(bh / p.heads_per_list) * nq + j) * p.col_bitmap_words + w);
+                        (static_cast<size_t>(bhq0 / p.heads_per_list) * nq + j) * p.col_bitmap_words + w);
     __syncthreads();
     for (int w = 0; w < words; ++w) n_it += __popc(col_bm[w]);
   }
+  n_it *= G;                                      // over all query heads of the group
+  QWalk walk;
+  walk.qs = qs;
+  walk.G = G;
 
   if (tid == 0) {
     mbar_init(bar(C::kBarKV), 1);
@@ -251,8 +276,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tma_load_4d(sbase + C::kVOff + c * C::kChunkBytes, &tmV, bar(C::kBarKV), c * 64, j * kTileN, h, b);
       }
       int nq_ld = 0, ndo_ld = 0;
-      for (int i = qs.first(), it = 0; i >= 0; i = qs.next(i), ++it) {
+      int g, i;
+      walk.start(g, i);
+      for (int it = 0; i >= 0; walk.advance(g, i), ++it) {
         const int row = i * kTileM;
+        const int hq = hq0 + g;
         const int sq = it % C::kStagesQ;
         if (it >= C::kStagesQ &&
             !wait_bar(bar(C::kBarQEmpty + sq), ((it / C::kStagesQ) & 1) ^ 1, abort_flag, p.err))
@@ -260,7 +288,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_arrive_expect_tx(bar(C::kBarQFull + sq), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_4d(sbase + C::kQOff + sq * C::kTileBytes + c * C::kChunkBytes, &tmQ,
-                      bar(C::kBarQFull + sq), c * 64, row, h, b);
+                      bar(C::kBarQFull + sq), c * 64, row, hq, b);
         ++nq_ld;
         const int sd = it % C::kStagesDO;
         if (it >= C::kStagesDO &&
@@ -269,7 +297,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mbar_arrive_expect_tx(bar(C::kBarDOFull + sd), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           tma_load_4d(sbase + C::kDOOff + sd * C::kTileBytes + c * C::kChunkBytes, &tmDO,
-                      bar(C::kBarDOFull + sd), c * 64, row, h, b);
+                      bar(C::kBarDOFull + sd), c * 64, row, hq, b);
         ++ndo_ld;
       }
       // Drain: every load issued has landed before the CTA may exit.
@@ -328,7 +356,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       };
       bool ok = wait_bar(bar(C::kBarKV), 0, abort_flag, p.err);
       if (ok && n_it > 0) ok = issue_s(0) && issue_dp(0);
-      for (int i = qs.first(), it = 0; i >= 0 && ok; i = qs.next(i), ++it) {
+      int g, i;
+      walk.start(g, i);
+      for (int it = 0; i >= 0 && ok; walk.advance(g, i), ++it) {
         const bool more = it + 1 < n_it;               // another query tile follows
         // dV += P^T dO_i  (K dimension = the 128 queries)
         if (!wait_bar(bar(C::kBarPReady), it & 1, abort_flag, p.err)) break;
@@ -399,11 +429,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const float sl2 = p.scale_log2;
     const float scale = p.scale;
     const float INF = __int_as_float(0x7f800000);
-    const size_t stat_base = static_cast<size_t>(bh) * L;
     uint8_t* ds_row = smem + C::kDSOff + X * C::kChunkBytes + kr * 128;   // this key's dS row
-    auto load_stats = [&](int i, float& l2, float& dl) {
+    // statistics of query tile i of query head hq0 + g
+    auto load_stats = [&](int g, int i, float& l2, float& dl) {
       const int q = i * kTileM + kr;
       if (i >= 0 && i < nq && q < L) {
+        const size_t stat_base = static_cast<size_t>(bhq0 + g) * L;
         const float lse = __ldg(p.lse + stat_base + q);
         l2 = (lse == -INF) ? INF : lse * kLog2e;      // an empty row contributes nothing
         dl = __ldg(p.delta + stat_base + q) * scale;
@@ -414,7 +445,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     };
     if (X == 0) {
       float l2, dl;
-      load_stats(qs.first(), l2, dl);
+      load_stats(0, qs.first(), l2, dl);
       stats[kr] = l2;
       stats[128 + kr] = dl;
       mbar_arrive(bar(C::kBarStat + 0));
@@ -424,11 +455,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     // it + 1 by half 0; by then dP^T(it + 1) has been issued, which waited for
     // dS(it) of both halves, so nobody reads it for tile it any more.
     bool ok = true;
-    for (int i = qs.first(), it = 0; i >= 0; i = qs.next(i), ++it) {
+    int g, i;
+    walk.start(g, i);
+    for (int it = 0; i >= 0; walk.advance(g, i), ++it) {
       const float* lse2 = stats + (it & 1) * 256 + 64 * X;
       const float* dlt = lse2 + 128;
       float l2n = 0.f, dln = 0.f;
-      if (X == 0) load_stats(qs.next(i), l2n, dln);
+      if (X == 0) {
+        int gn = g, in = i;
+        walk.advance(gn, in);
+        load_stats(gn, in, l2n, dln);
+      }
       if (!wait_bar(bar(C::kBarSFull), it & 1, abort_flag, p.err) ||
           !wait_bar(bar(C::kBarStat + (it & 1)), (it >> 1) & 1, abort_flag, p.err)) {
         ok = false;
@@ -575,7 +612,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     static_assert(2 * kBoxBytes == C::kStageBytes, "two boxes fill the staging buffer");
     bool ok = true;
     int g = 0;                                    // global round counter
-    for (int i = qs.first(), it = 0; i >= 0 && ok; i = qs.next(i), ++it) {
+    int gq, i;                                    // query head of the group, query tile
+    walk.start(gq, i);
+    for (int it = 0; i >= 0 && ok; walk.advance(gq, i), ++it) {
       if (!wait_bar_relaxed(bar(C::kBarDQFull), it & 1, abort_flag, p.err)) break;
       BSS_TRACE_EV(p, tr && qr == 0, 3, 3 * it);
       tc_fence_after();
@@ -620,8 +659,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
             break;
           }
           const int row = i * kTileM;
-          tma_reduce_add_4d(&tmDQ, stage, 64 * r, row, h, b);
-          tma_reduce_add_4d(&tmDQ, stage + kBoxBytes, 64 * r + 32, row, h, b);
+          tma_reduce_add_4d(&tmDQ, stage, 64 * r, row, hq0 + gq, b);
+          tma_reduce_add_4d(&tmDQ, stage + kBoxBytes, 64 * r + 32, row, hq0 + gq, b);
           bulk_commit_group();
         }
         __syncwarp();                               // reconverge before the next TMEM load
@@ -709,7 +748,7 @@ cudaError_t launch_main(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  const int n_cta = p.B * p.H * ((p.L + kTileN - 1) / kTileN);
+  const int n_cta = p.B * p.Hkv * ((p.L + kTileN - 1) / kTileN);
   kern<<<n_cta, C::kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError();
 }

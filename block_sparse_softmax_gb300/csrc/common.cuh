@@ -141,6 +141,7 @@ __device__ __forceinline__ bool wait_bar_relaxed(uint32_t bar, uint32_t parity,
 
 struct FwdParams {
   int B, H, Lq, Lk;
+  int Hkv;                 // K/V heads; query head h reads K/V head h / (H / Hkv)
   float scale_log2;        // scale * log2(e): scores are exponentiated in base 2
   long long q_offset, k_offset;
   int causal;
@@ -177,6 +178,7 @@ struct MergeParams {
 
 struct BwdParams {
   int B, H, L;
+  int Hkv;                 // K/V heads; query head h reads K/V head h / (H / Hkv)
   float scale, scale_log2;
   int causal;
   const __nv_bfloat16* o;
@@ -214,7 +216,7 @@ cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int
                                      cudaStream_t st);
 cudaError_t launch_watchdog_selftest(unsigned long long cycles, int* err, cudaStream_t st);
 int select_row_entries(int L, int top_r, int local, int causal);
-cudaError_t launch_select(int d, const void* q, const void* k, int B, int H, int L, int n_lists,
-                          int top_r, int local, int causal, float scale, int* row_ptr, int* col_idx,
-                          float* qbar, float* kbar, int* prefix, cudaStream_t st);
+cudaError_t launch_select(int d, const void* q, const void* k, int B, int H, int Hkv, int L,
+                          int n_lists, int top_r, int local, int causal, float scale, int* row_ptr,
+                          int* col_idx, float* qbar, float* kbar, int* prefix, cudaStream_t st);
 }  // namespace bss

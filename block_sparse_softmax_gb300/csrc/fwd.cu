@@ -111,6 +111,7 @@ struct FwdRegs {
 // see the most keys) comes first, so that the longest items start first.
 struct FwdItem {
   int b, h, bh;
+  int hkv;         // K/V head read by query head h
   int c;           // key chunk (0 without a split)
   int kbase;       // row of the chunk's first key in K and V
   int Lkc;         // keys in the chunk
@@ -133,6 +134,7 @@ __device__ __forceinline__ FwdItem fwd_item(int item, const FwdParams& p) {
   it.bh = rem - it.c * BH;
   it.b = it.bh / p.H;
   it.h = it.bh - it.b * p.H;
+  it.hkv = it.h / (p.H / p.Hkv);
   it.kbase = it.c * p.chunk_len;
   it.Lkc = min(p.chunk_len, p.Lk - it.kbase);
   it.koff = p.k_offset + it.kbase;
@@ -363,7 +365,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_4d(ks + c * C::kChunkBytes, &tmK, bar(C::kBarKFull + sk), c * 64, it.kbase + kb * kTileN,
-                        it.h, it.b);
+                        it.hkv, it.b);
           ++ik;
           const int sv = iv % C::kStagesV;
           if (iv >= C::kStagesV &&
@@ -377,7 +379,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_4d(vs + c * C::kChunkBytes, &tmV, bar(C::kBarVFull + sv), c * 64, it.kbase + kb * kTileN,
-                        it.h, it.b);
+                        it.hkv, it.b);
           ++iv;
           kb = nkb;
         }

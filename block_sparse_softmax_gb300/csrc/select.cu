@@ -73,7 +73,8 @@ template <int D>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* qbar, const float* kbar,
                                                             const int* prefix, int* col_idx, int n,
                                                             int hpl, int top_r, int local,
-                                                            int causal, float scale) {
+                                                            int causal, float scale, int H,
+                                                            int group) {
   extern __shared__ float sel_smem[];
   float* qs = sel_smem;               // [hpl][D] query block means of the list's heads
   float* sc = sel_smem + hpl * D;     // [n] candidate scores (-inf: not a candidate)
@@ -96,7 +97,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* qbar, 
     if (c <= last && !(c >= wlo && c <= a)) {
       v = 0.f;
       for (int x = 0; x < hpl; ++x) {
-        const float* kr = kbar + ((static_cast<size_t>(l) * hpl + x) * n + c) * D;
+        // query head (b, hq) = l*hpl + x reads the block means of K/V head hq / group
+        const int bhq = l * hpl + x;
+        const int bq = bhq / H;
+        const size_t bkv = static_cast<size_t>(bq) * (H / group) + (bhq - bq * H) / group;
+        const float* kr = kbar + (bkv * n + c) * D;
         const float* qr = qs + x * D;
         float dot = 0.f;
 #pragma unroll 8
@@ -165,13 +170,15 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* qbar, 
 }
 
 template <int D>
-cudaError_t launch_select_d(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H, int L,
-                            int n_lists, int top_r, int local, int causal, float scale, int* row_ptr,
-                            int* col_idx, float* qbar, float* kbar, int* prefix, cudaStream_t st) {
+cudaError_t launch_select_d(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H, int Hkv,
+                            int L, int n_lists, int top_r, int local, int causal, float scale,
+                            int* row_ptr, int* col_idx, float* qbar, float* kbar, int* prefix,
+                            cudaStream_t st) {
   const int n = (L + kTileN - 1) / kTileN;
   const long long bhn = static_cast<long long>(B) * H * n;
+  const long long bkvn = static_cast<long long>(B) * Hkv * n;
   pool_blocks_kernel<D><<<static_cast<unsigned>(bhn), D, 0, st>>>(q, qbar, L, n);
-  pool_blocks_kernel<D><<<static_cast<unsigned>(bhn), D, 0, st>>>(k, kbar, L, n);
+  pool_blocks_kernel<D><<<static_cast<unsigned>(bkvn), D, 0, st>>>(k, kbar, L, n);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   select_rowptr_kernel<<<1, kSelThreads, 0, st>>>(prefix, row_ptr, n_lists, n, top_r, local, causal);
@@ -183,7 +190,7 @@ cudaError_t launch_select_d(const __nv_bfloat16* q, const __nv_bfloat16* k, int 
                                 static_cast<int>(smem))) != cudaSuccess)
     return e;
   kern<<<static_cast<unsigned>(static_cast<long long>(n_lists) * n), kSelThreads, smem, st>>>(
-      qbar, kbar, prefix, col_idx, n, hpl, top_r, local, causal, scale);
+      qbar, kbar, prefix, col_idx, n, hpl, top_r, local, causal, scale, H, H / Hkv);
   return cudaGetLastError();
 }
 
@@ -196,16 +203,16 @@ int select_row_entries(int L, int top_r, int local, int causal) {
   return acc;
 }
 
-cudaError_t launch_select(int d, const void* q, const void* k, int B, int H, int L, int n_lists,
-                          int top_r, int local, int causal, float scale, int* row_ptr, int* col_idx,
-                          float* qbar, float* kbar, int* prefix, cudaStream_t st) {
+cudaError_t launch_select(int d, const void* q, const void* k, int B, int H, int Hkv, int L,
+                          int n_lists, int top_r, int local, int causal, float scale, int* row_ptr,
+                          int* col_idx, float* qbar, float* kbar, int* prefix, cudaStream_t st) {
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
   const auto* kk = static_cast<const __nv_bfloat16*>(k);
   if (d == 64)
-    return launch_select_d<64>(qq, kk, B, H, L, n_lists, top_r, local, causal, scale, row_ptr,
+    return launch_select_d<64>(qq, kk, B, H, Hkv, L, n_lists, top_r, local, causal, scale, row_ptr,
                                col_idx, qbar, kbar, prefix, st);
   if (d == 128)
-    return launch_select_d<128>(qq, kk, B, H, L, n_lists, top_r, local, causal, scale, row_ptr,
+    return launch_select_d<128>(qq, kk, B, H, Hkv, L, n_lists, top_r, local, causal, scale, row_ptr,
                                 col_idx, qbar, kbar, prefix, st);
   return cudaErrorInvalidValue;
 }

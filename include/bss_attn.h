@@ -13,6 +13,13 @@
  * Conventions shared by every entry point.
  *   - Tensors are contiguous row-major [B, H, L, d] (d fastest), bf16 unless
  *     stated; LSE, partial states and delta are fp32.  d must be 64 or 128.
+ *   - Grouped heads: H query heads read H_kv K/V heads (1 <= H_kv <= H, H_kv
+ *     divides H; H_kv = H is ordinary multi-head attention).  q, o, dout, dq,
+ *     lse and delta have H heads; k, v, dk and dv have H_kv heads, and query
+ *     head h reads K/V head h / (H / H_kv) ("Exact Blocks, Rings, and
+ *     Sparsity", section 6: query heads that share one physical KV head).
+ *     dk and dv are summed over the query heads of their group.  Otherwise
+ *     ATTN_ERR_INVALID_ARG.
  *   - All pointers to tensors are DEVICE pointers, 16-byte aligned, owned by
  *     the caller.  The library never allocates, frees or synchronises device
  *     memory (attn_poll_status excepted) and keeps no pointer after a call
@@ -68,7 +75,7 @@ const char* attn_last_error_message(void);
  *   scale must be finite and > 0 (the pages use d^-1/2).
  */
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                       int B, int H, int Lq, int Lk, int d, float scale, int causal,
+                       int B, int H, int H_kv, int Lq, int Lk, int d, float scale, int causal,
                        int64_t q_offset, int64_t k_offset, void* stream);
 
 /*
@@ -85,7 +92,8 @@ attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, flo
  */
 attn_status_t attn_fwd_partial(const void* q, const void* k, const void* v,
                                float* m, float* l, float* acc,
-                               int B, int H, int Lq, int Lk, int d, float scale, int causal,
+                               int B, int H, int H_kv, int Lq, int Lk, int d, float scale,
+                               int causal,
                                int64_t q_offset, int64_t k_offset, void* stream);
 
 /*
@@ -126,7 +134,8 @@ size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int Lq, int Lk, int d, int
  *   partial states, then attn_merge_states.
  */
 attn_status_t attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
-                               void* workspace, size_t workspace_bytes, int B, int H, int Lq,
+                               void* workspace, size_t workspace_bytes, int B, int H, int H_kv,
+                               int Lq,
                                int Lk, int d, float scale, int causal, int64_t q_offset,
                                int64_t k_offset, int n_chunks, void* stream);
 
@@ -166,7 +175,7 @@ attn_status_t attn_blocklist_normalize(const int32_t* row_ptr, const int32_t* co
  *   gets O = 0, LSE = -inf.  L <= 4096*128 (at most 4096 key blocks).
  */
 attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o,
-                                   float* lse, int B, int H, int L, int d, float scale,
+                                   float* lse, int B, int H, int H_kv, int L, int d, float scale,
                                    int causal, int block, const int32_t* row_ptr,
                                    const int32_t* col_idx, int n_lists, int n_qblk, int nnz,
                                    void* stream);
@@ -195,7 +204,8 @@ attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, 
  */
 size_t attn_select_blocks_workspace_bytes(int B, int H, int L, int d);
 int64_t attn_select_blocks_nnz(int L, int top_r, int local_blocks, int causal, int n_lists);
-attn_status_t attn_select_blocks(const void* q, const void* k, int B, int H, int L, int d,
+attn_status_t attn_select_blocks(const void* q, const void* k, int B, int H, int H_kv, int L,
+                                 int d,
                                  float scale, int causal, int block, int top_r, int local_blocks,
                                  int n_lists, int32_t* row_ptr, int32_t* col_idx, void* workspace,
                                  size_t workspace_bytes, void* stream);
@@ -220,7 +230,8 @@ size_t attn_bwd_workspace_bytes(int B, int H, int L, int d);
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
                        const float* lse, const void* dout, void* dq, void* dk, void* dv,
                        float* delta, void* workspace, size_t workspace_bytes,
-                       int B, int H, int L, int d, float scale, int causal, void* stream);
+                       int B, int H, int H_kv, int L, int d, float scale, int causal,
+                       void* stream);
 
 /*
  * attn_bwd_blocksparse_workspace_bytes - size of the caller-provided workspace
@@ -244,13 +255,16 @@ size_t attn_bwd_blocksparse_workspace_bytes(int B, int H, int L, int d, int n_li
  *   the query blocks that list it (the list's transpose, built in the
  *   workspace on the stream).  A key block no query block lists gets
  *   dK = dV = 0; a query block with an empty list gets dQ = 0.  Malformed
- *   entries are handled and reported as in attn_fwd_blocksparse.
- *   workspace: device, >= attn_bwd_blocksparse_workspace_bytes(B,H,L,d).
+ *   entries are handled and reported as in attn_fwd_blocksparse.  With
+ *   grouped heads the query heads of one K/V head must share one list
+ *   (B*H/n_lists a multiple of H/H_kv), else ATTN_ERR_BAD_BLOCKLIST.
+ *   workspace: device, >= attn_bwd_blocksparse_workspace_bytes(B,H,L,d,n_lists).
  */
 attn_status_t attn_bwd_blocksparse(const void* q, const void* k, const void* v, const void* o,
                                    const float* lse, const void* dout, void* dq, void* dk,
                                    void* dv, float* delta, void* workspace, size_t workspace_bytes,
-                                   int B, int H, int L, int d, float scale, int causal, int block,
+                                   int B, int H, int H_kv, int L, int d, float scale, int causal,
+                                   int block,
                                    const int32_t* row_ptr, const int32_t* col_idx, int n_lists,
                                    int n_qblk, int nnz, void* stream);
 
@@ -274,7 +288,8 @@ attn_status_t attn_bwd_blocksparse(const void* q, const void* k, const void* v, 
  */
 attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                                const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                               float* delta, int B, int H, int L, int d, float scale, int causal,
+                               float* delta, int B, int H, int H_kv, int L, int d, float scale,
+                               int causal,
                                void* stream);
 
 /*

@@ -107,22 +107,26 @@ def test_blocklist_normalize_rejects_malformed(lib, rp, ci):
 def test_argument_errors_return_codes_before_any_device_work(lib):
     P = ctypes.c_void_p(16 * 1000)       # aligned dummy addresses, never dereferenced
     bad = ctypes.c_void_p(16 * 1000 + 2)
-    args = lambda q=P, d=64, scale=0.125, B=1: (q, P, P, P, P, B, 1, 256, 256, d, scale, 0, 0, 0, None)
+    args = lambda q=P, d=64, scale=0.125, B=1, H=1, Hkv=1: (q, P, P, P, P, B, H, Hkv, 256, 256, d, scale,
+                                                            0, 0, 0, None)
     assert lib.attn_fwd(*args(d=96)) == 2                 # unsupported head dim
     assert lib.attn_fwd(*args(q=None)) == 1               # null pointer
     assert lib.attn_fwd(*args(q=bad)) == 1                # misaligned pointer
     assert lib.attn_fwd(*args(scale=float("nan"))) == 1   # non-finite scale
     assert lib.attn_fwd(*args(scale=-1.0)) == 1           # non-positive scale
     assert lib.attn_fwd(*args(B=0)) == 1                  # empty batch
+    assert lib.attn_fwd(*args(H=6, Hkv=4)) == 1           # K/V heads must divide the query heads
+    assert lib.attn_fwd(*args(H=6, Hkv=0)) == 1
+    assert lib.attn_fwd(*args(H=2, Hkv=3)) == 1
     # block size other than 128, CSR row count mismatch, too many key blocks
-    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 256, 64, 0.125, 1, 64, P, P, 1, 2, 4,
+    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 1, 256, 64, 0.125, 1, 64, P, P, 1, 2, 4,
                                     None) == 2
-    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 256, 64, 0.125, 1, 128, P, P, 1, 3, 4,
+    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 1, 256, 64, 0.125, 1, 128, P, P, 1, 3, 4,
                                     None) == 3
-    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 4097 * 128, 64, 0.125, 1, 128, P, P, 1,
+    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 1, 1, 1, 4097 * 128, 64, 0.125, 1, 128, P, P, 1,
                                     4097, 4, None) == 2
     # lists must divide the B*H heads into equal groups
-    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 2, 3, 256, 64, 0.125, 1, 128, P, P, 4, 2, 4,
+    assert lib.attn_fwd_blocksparse(P, P, P, P, P, 2, 3, 3, 256, 64, 0.125, 1, 128, P, P, 4, 2, 4,
                                     None) == 3
     # merge: chunk count out of range
     assert lib.attn_merge_states(0, P, P, P, P, P, 1, 1, 16, 64, None) == 1
@@ -130,13 +134,14 @@ def test_argument_errors_return_codes_before_any_device_work(lib):
     # backward: workspace too small
     ws = lib.attn_bwd_workspace_bytes(2, 3, 100, 64)
     assert ws == 2 * 3 * 100 * 64 * 4
-    assert lib.attn_bwd(P, P, P, P, P, P, P, P, P, P, P, ws - 4, 2, 3, 100, 64, 0.125, 1, None) == 6
+    assert lib.attn_bwd(P, P, P, P, P, P, P, P, P, P, P, ws - 4, 2, 3, 3, 100, 64, 0.125, 1, None) == 6
     # split-KV forward: chunks of ceil(Lk / n) keys rounded up to 128; workspace =
     # acc | m | l of every chunk, each part at a 256-byte boundary
     wsk = lib.attn_fwd_splitkv_workspace_bytes(2, 3, 100, 1000, 64, 4)
     assert wsk == 4 * 600 * 64 * 4 + 2 * 9728
     assert lib.attn_fwd_splitkv_workspace_bytes(2, 3, 100, 1000, 64, 65) == 0
-    kv = lambda n=4, ws_=wsk: (P, P, P, P, P, P, ws_, 2, 3, 100, 1000, 64, 0.125, 1, 900, 0, n, None)
+    kv = lambda n=4, ws_=wsk: (P, P, P, P, P, P, ws_, 2, 3, 1, 100, 1000, 64, 0.125, 1, 900, 0, n,
+                                  None)
     assert lib.attn_fwd_splitkv(*kv(n=0)) == 1                   # chunk count out of range
     assert lib.attn_fwd_splitkv(*kv(n=65)) == 1
     assert lib.attn_fwd_splitkv(*kv(ws_=wsk - 4)) == 6           # workspace too small
@@ -147,8 +152,8 @@ def test_argument_errors_return_codes_before_any_device_work(lib):
     assert wss == ((acc + 255) // 256) * 256 + 8 * 1 * 4
     assert lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64, 6) == wss + 5 * 8 * 1 * 4
     assert lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64, 4) == 0   # 4 does not divide 6
-    sp = lambda block=128, nq=8, ws_=wss, rp=P: (P, P, P, P, P, P, P, P, P, P, P, ws_, 2, 3, 1000,
-                                                 64, 0.125, 1, block, rp, P, 1, nq, 4, None)
+    sp = lambda block=128, nq=8, ws_=wss, rp=P: (P, P, P, P, P, P, P, P, P, P, P, ws_, 2, 3, 3,
+                                                 1000, 64, 0.125, 1, block, rp, P, 1, nq, 4, None)
     assert lib.attn_bwd_blocksparse(*sp(block=64)) == 2          # block size other than 128
     assert lib.attn_bwd_blocksparse(*sp(nq=7)) == 3              # CSR row count mismatch
     assert lib.attn_bwd_blocksparse(*sp(rp=None)) == 1           # missing row_ptr

@@ -35,7 +35,7 @@ def _call_noalloc(lib, x, o, lse, causal, scale):
     stream = torch.cuda.current_stream().cuda_stream
     st = lib.attn_bwd_noalloc(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
                               o.data_ptr(), lse.data_ptr(), x["do"].data_ptr(), dq.data_ptr(),
-                              dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), B, H, L, d, scale,
+                              dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), B, H, H, L, d, scale,
                               int(causal), stream)
     assert st == 0, lib.attn_last_error_message()
     return dq, dk, dv, delta
@@ -66,10 +66,10 @@ def test_noalloc_matches_attn_bwd_on_two_calls_in_a_row(lib, order):
 def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
     # 1 x 16 x 4097 x 128 > 8388608 floats: rejected before any device work
     p = ctypes.c_void_p(16 * 4096)
-    st = lib.attn_bwd_noalloc(p, p, p, p, p, p, p, p, p, p, 1, 16, 4097, 128, 0.125, 1, None)
+    st = lib.attn_bwd_noalloc(p, p, p, p, p, p, p, p, p, p, 1, 16, 16, 4097, 128, 0.125, 1, None)
     assert st == 6
     assert b"exceeds the static scratch" in lib.attn_last_error_message()
     # exactly at the limit is accepted by the size check (fails later only on the
     # null pointer test here, which is ATTN_ERR_INVALID_ARG, not the size error)
-    st = lib.attn_bwd_noalloc(None, p, p, p, p, p, p, p, p, p, 1, 16, 4096, 128, 0.125, 1, None)
+    st = lib.attn_bwd_noalloc(None, p, p, p, p, p, p, p, p, p, 1, 16, 16, 4096, 128, 0.125, 1, None)
     assert st == 1

@@ -36,7 +36,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 from workloads import (BWD_8K, CAUSAL_4K, CAUSAL_16K, DECODE_16K, DENSE_SMALL,  # noqa: E402
-                       SPARSE_16K,
+                       GQA_16K, SPARSE_16K,
                        SPLITKV_128K, Workload, chunk_bounds, local_global_random_blocklist,
                        make_inputs)
 
@@ -290,12 +290,17 @@ def time_loop(fn, steps, warmup, sync_all):
 
 
 def bench_kernel(fn, reps=10, warmup=3):
+    """Median device time of fn() between CUDA events on the current stream.
+    A ~1 ms device sleep queued ahead of each start event keeps the GPU busy
+    while the host enqueues the call, so the events bracket device work only
+    (not the binding's host time)."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     times = []
     for _ in range(reps):
+        torch.cuda._sleep(2_000_000)
         s.record()
         fn()
         e.record()
@@ -353,7 +358,30 @@ def measure_configs(bss, dev, peaks):
                    "tflops_executed": round(4 * w.d * tiles * 128 * 128 / ms / 1e9, 1),
                    "bwd_ms": round(ms_b, 4),
                    "bwd_tflops_logical": round(10 * w.d * pairs / ms_b / 1e9, 1)}
-    del x, o, lse, do, ws, g, dl
+    del do, ws, g, dl
+    # mean-pooled selector on the same inputs: one list per head of the 4 local
+    # and 4 best-scoring blocks; HBM-bound (Q and K read once for the block
+    # means), then the block-sparse forward on the lists it chose
+    n_lists = w.B * w.H
+    sel_ws = torch.empty(bss.attn_select_blocks_workspace_bytes(w.B, w.H, w.L, w.d), device=dev,
+                         dtype=torch.uint8)
+    ms_sel = bench_kernel(lambda: bss.attn_select_blocks(
+        x["q"], x["k"], 4, local_blocks=4, causal=True, n_lists=n_lists, scale=w.scale,
+        workspace=sel_ws), reps=20)
+    srp, sci = bss.attn_select_blocks(x["q"], x["k"], 4, local_blocks=4, causal=True,
+                                      n_lists=n_lists, scale=w.scale, workspace=sel_ws)
+    ms_sf = bench_kernel(lambda: bss.attn_fwd_blocksparse(x["q"], x["k"], x["v"], srp, sci,
+                                                          causal=True, scale=w.scale, out=o,
+                                                          lse=lse))
+    sel_bytes = 2 * w.B * w.H * w.L * w.d * 2
+    sel_tiles = int(sci.numel())
+    out["selector_" + w.name] = {
+        "select_ms": round(ms_sel, 4), "select_gbs": round(sel_bytes / ms_sel / 1e6, 1),
+        "select_frac_hbm": round(sel_bytes / ms_sel / 1e6 / peaks["hbm_gbs"], 4),
+        "lists": n_lists, "entries": sel_tiles, "sparse_fwd_ms": round(ms_sf, 4),
+        "sparse_fwd_tflops_executed": round(4 * w.d * sel_tiles * 128 * 128 / ms_sf / 1e9, 1),
+        "select_share": round(ms_sel / (ms_sel + ms_sf), 4)}
+    del x, o, lse, sel_ws, srp, sci
     # split-KV L=131072, 8 chunks + merge
     w = SPLITKV_128K
     x = {k: t.to(dev) for k, t in make_inputs(w).items()}
@@ -428,6 +456,25 @@ def measure_configs(bss, dev, peaks):
     out[w.name] = {"fwd_ms": round(ms_f, 4), "bwd_ms": round(ms_b, 4),
                    "fwd_tflops": round(4 * w.d * pairs / ms_f / 1e9, 1),
                    "bwd_tflops": round(10 * w.d * pairs / ms_b / 1e9, 1)}
+    del x, o, lse, ws, g, dl
+    # grouped key/value heads: 16 query heads over 4 shared K/V heads, L=16384
+    w = GQA_16K
+    x = {k: t.to(dev) for k, t in make_inputs(w).items()}
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(w.B, w.H, w.L, device=dev)
+    ws = torch.empty(bss.attn_bwd_workspace_bytes(w.B, w.H, w.L, w.d), device=dev, dtype=torch.uint8)
+    g = [torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])]
+    dl = torch.empty_like(lse)
+    ms_f = bench_kernel(lambda: bss.attn_fwd(x["q"], x["k"], x["v"], causal=True, scale=w.scale,
+                                             out=o, lse=lse), reps=10)
+    ms_b = bench_kernel(lambda: bss.attn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], causal=True,
+                                             scale=w.scale, workspace=ws, dq=g[0], dk=g[1],
+                                             dv=g[2], delta=dl), reps=10)
+    pairs = w.B * w.H * causal_pairs(w.L, w.L)
+    out[w.name] = {"fwd_ms": round(ms_f, 4), "bwd_ms": round(ms_b, 4),
+                   "fwd_tflops": round(4 * w.d * pairs / ms_f / 1e9, 1),
+                   "bwd_tflops": round(10 * w.d * pairs / ms_b / 1e9, 1),
+                   "fwd_frac_burst": round(4 * w.d * pairs / ms_f / 1e9 / pk, 4)}
     return out
 
 

@@ -26,7 +26,7 @@ __all__ = [
     "attn_bwd_blocksparse_workspace_bytes", "attn_bwd_noalloc",
     "attn_poll_status",
     "attn_watchdog_selftest", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
-    "attn_select_blocks", "library",
+    "attn_select_blocks", "attn_select_blocks_workspace_bytes", "attn_select_blocks_nnz", "library",
 ]
 
 OK = 0
@@ -169,6 +169,16 @@ def attn_fwd_splitkv(q, k, v, chunks: int, *, causal: bool = False, scale: Optio
     return out, lse
 
 
+def attn_select_blocks_workspace_bytes(B: int, H: int, L: int, d: int) -> int:
+    return int(_lib.load().attn_select_blocks_workspace_bytes(B, H, L, d))
+
+
+def attn_select_blocks_nnz(L: int, top_r: int, local_blocks: int, causal: bool,
+                           n_lists: int = 1) -> int:
+    """Entries of the lists attn_select_blocks writes (all lists together)."""
+    return int(_lib.load().attn_select_blocks_nnz(L, top_r, local_blocks, int(causal), n_lists))
+
+
 def attn_select_blocks(q, k, top_r: int, *, local_blocks: int = 1, causal: bool = True,
                        n_lists: int = 1, scale: Optional[float] = None, block: int = 128,
                        workspace: Optional[torch.Tensor] = None):
@@ -180,12 +190,12 @@ def attn_select_blocks(q, k, top_r: int, *, local_blocks: int = 1, causal: bool 
     _need(k, "k", torch.bfloat16, (B, Hkv, L, d))
     lib = _lib.load()
     n = (L + block - 1) // block
-    nnz = int(lib.attn_select_blocks_nnz(L, top_r, local_blocks, int(causal), n_lists))
+    nnz = attn_select_blocks_nnz(L, top_r, local_blocks, causal, n_lists)
     if nnz < 0:
         raise AttnError(ERR_INVALID_ARG, "attn_select_blocks: invalid arguments")
     row_ptr = torch.empty((n_lists, n + 1), device=q.device, dtype=torch.int32)
     col_idx = torch.empty(max(1, nnz), device=q.device, dtype=torch.int32)
-    nbytes = int(lib.attn_select_blocks_workspace_bytes(B, H, L, d))
+    nbytes = attn_select_blocks_workspace_bytes(B, H, L, d)
     if workspace is None:
         workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
     st = lib.attn_select_blocks(q.data_ptr(), k.data_ptr(), B, H, Hkv, L, d, _scale(scale, d),

@@ -465,7 +465,7 @@ size_t attn_select_blocks_workspace_bytes(int B, int H, int L, int d) {
   if (B < 1 || H < 1 || L < 0 || d < 1) return 0;
   const size_t n = (static_cast<size_t>(L) + 127) / 128;
   const size_t pooled = static_cast<size_t>(B) * H * n * d * 4;
-  return 2 * ((pooled + 255) & ~static_cast<size_t>(255)) + (n + 1) * 4;
+  return 2 * ((pooled + 255) & ~static_cast<size_t>(255));
 }
 
 int64_t attn_select_blocks_nnz(int L, int top_r, int local_blocks, int causal, int n_lists) {
@@ -486,7 +486,9 @@ attn_status_t attn_select_blocks(const void* q, const void* k, int B, int H, int
   if (n > kMaxKBlocks) return ATTN_ERR_UNSUPPORTED;
   const long long hpl = heads_per_list(B, H, n_lists);
   if (hpl == 0) return ATTN_ERR_BAD_BLOCKLIST;
-  if ((hpl * d + n) * 4 > 200 * 1024) return ATTN_ERR_UNSUPPORTED;   // the selection CTA's smem
+  if (static_cast<long long>(n_lists) * select_row_entries(L, top_r, local_blocks, causal ? 1 : 0) >
+      INT_MAX)
+    return ATTN_ERR_UNSUPPORTED;   // int32 row offsets
   if (!q || !k || !aligned16(q) || !aligned16(k) || !row_ptr || !aligned4(row_ptr)) return ATTN_ERR_INVALID_ARG;
   if (!col_idx || !aligned4(col_idx) || !workspace || !aligned16(workspace)) return ATTN_ERR_INVALID_ARG;
   if (workspace_bytes < attn_select_blocks_workspace_bytes(B, H, L, d)) return ATTN_ERR_WORKSPACE;
@@ -498,7 +500,6 @@ attn_status_t attn_select_blocks(const void* q, const void* k, int B, int H, int
                      launch_select(d, q, k, B, H, H_kv, L, n_lists, top_r, local_blocks, causal ? 1 : 0,
                                    scale, row_ptr, col_idx, reinterpret_cast<float*>(ws),
                                    reinterpret_cast<float*>(ws + pooled_up),
-                                   reinterpret_cast<int*>(ws + 2 * pooled_up),
                                    static_cast<cudaStream_t>(stream)));
 }
 

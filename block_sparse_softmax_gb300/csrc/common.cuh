@@ -218,5 +218,5 @@ cudaError_t launch_watchdog_selftest(unsigned long long cycles, int* err, cudaSt
 int select_row_entries(int L, int top_r, int local, int causal);
 cudaError_t launch_select(int d, const void* q, const void* k, int B, int H, int Hkv, int L,
                           int n_lists, int top_r, int local, int causal, float scale, int* row_ptr,
-                          int* col_idx, float* qbar, float* kbar, int* prefix, cudaStream_t st);
+                          int* col_idx, float* qbar, float* kbar, cudaStream_t st);
 }  // namespace bss

@@ -9,30 +9,76 @@
 //   row a keeps the local window a, a-1, .., a-local+1 and the top_r other
 //   candidates (under a causal mask blocks 0..a), ties to the lower index,
 //   in ascending order.
-// Three small kernels: the block means (HBM-bound: Q and K are read once),
-// the row offsets (which depend on the shapes only), and one CTA per
-// (list, query block) that scores its candidates and picks the top_r by
-// repeated block-wide arg-max.
+// Two kernels: the block means of Q and K (HBM-bound: both are read once),
+// then one warp per (list, query block) that scores its candidates, picks the
+// top_r by repeated warp-wide arg-max and writes its row and row offset.
 #include "common.cuh"
 
 namespace bss {
 namespace {
 
-constexpr int kSelThreads = 256;
+constexpr int kPoolThreads = 256;
 
-// out[bh][c][:] = mean of rows c*128 .. min(L, c*128+128)-1 of x[bh] (bf16 -> fp32).
+// Block means of Q and of K in one launch: CTA x < n_q_items pools block
+// (bh, c) of q into qbar, the rest pool k into kbar.  out[bh][c][:] = mean of
+// rows c*128 .. min(L, c*128+128)-1 (bf16 -> fp32).  Each thread owns one
+// 8-column slice (16-byte loads) of every RG-th row, so a CTA has all of its
+// 32 KB (d=128) in flight at once; the RG partial sums meet in shared memory.
 template <int D>
-__global__ void __launch_bounds__(D) pool_blocks_kernel(const __nv_bfloat16* x, float* out, int L,
-                                                        int n) {
-  const long long bhc = blockIdx.x;
-  const long long bh = bhc / n;
-  const int c = static_cast<int>(bhc - bh * n);
+__global__ void __launch_bounds__(kPoolThreads) pool_blocks_kernel(const __nv_bfloat16* q,
+                                                                   const __nv_bfloat16* k,
+                                                                   float* qbar, float* kbar,
+                                                                   int L, int n,
+                                                                   long long n_q_items) {
+  constexpr int kVec = 8;                       // bf16 per 16-byte load
+  constexpr int kSlices = D / kVec;             // 16-byte slices per row
+  constexpr int kRG = kPoolThreads / kSlices;   // row groups
+  __shared__ float part[kRG][D];
+  long long item = blockIdx.x;
+  const __nv_bfloat16* x = q;
+  float* out = qbar;
+  if (item >= n_q_items) {
+    item -= n_q_items;
+    x = k;
+    out = kbar;
+  }
+  const long long bh = item / n;
+  const int c = static_cast<int>(item - bh * n);
   const int r0 = c * kTileN;
-  const int r1 = min(L, r0 + kTileN);
-  const __nv_bfloat16* src = x + (bh * L + r0) * D + threadIdx.x;
-  float s = 0.f;
-  for (int r = r0; r < r1; ++r, src += D) s += __bfloat162float(*src);
-  out[bhc * D + threadIdx.x] = s / static_cast<float>(r1 - r0);
+  const int rows = min(L, r0 + kTileN) - r0;
+  const int slice = threadIdx.x % kSlices;
+  const int rg = threadIdx.x / kSlices;
+  const __nv_bfloat16* base = x + (bh * L + r0) * D + slice * kVec;
+  float acc[kVec];
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) acc[e] = 0.f;
+  constexpr int kPerThread = kTileN / kRG;
+  uint4 v[kPerThread];
+#pragma unroll
+  for (int t = 0; t < kPerThread; ++t) {
+    const int r = rg + t * kRG;
+    v[t] = r < rows ? __ldg(reinterpret_cast<const uint4*>(base + static_cast<long long>(r) * D))
+                    : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int t = 0; t < kPerThread; ++t) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v[t]);
+#pragma unroll
+    for (int e = 0; e < kVec / 2; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      acc[2 * e] += f.x;
+      acc[2 * e + 1] += f.y;
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) part[rg][slice * kVec + e] = acc[e];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float s = 0.f;
+#pragma unroll
+    for (int g = 0; g < kRG; ++g) s += part[g][threadIdx.x];
+    out[(bh * n + c) * D + threadIdx.x] = s / static_cast<float>(rows);
+  }
 }
 
 // Keys a row keeps: the window and min(top_r, other candidates).
@@ -43,84 +89,148 @@ __device__ __host__ __forceinline__ int select_row_count(int a, int n, int top_r
   return window + min(top_r, last + 1 - window);
 }
 
-// prefix[a] = entries of rows 0..a-1 of one list; row_ptr[l][a] = l*prefix[n] + prefix[a].
-__global__ void __launch_bounds__(kSelThreads) select_rowptr_kernel(int* prefix, int* row_ptr,
-                                                                   int n_lists, int n, int top_r,
-                                                                   int local, int causal) {
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int a = 0; a < n; ++a) {
-      prefix[a] = acc;
-      acc += select_row_count(a, n, top_r, local, causal);
-    }
-    prefix[n] = acc;
-  }
-  __syncthreads();
-  const long long total = static_cast<long long>(n_lists) * (n + 1);
-  for (long long x = threadIdx.x; x < total; x += blockDim.x) {
-    const int l = static_cast<int>(x / (n + 1));
-    const int a = static_cast<int>(x - static_cast<long long>(l) * (n + 1));
-    row_ptr[x] = l * prefix[n] + prefix[a];
-  }
-}
-
 // True when (v1, i1) ranks before (v2, i2): larger score, then lower index.
 __device__ __forceinline__ bool ranks_before(float v1, int i1, float v2, int i2) {
   return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
+// One CTA per (list l, kSelWarps consecutive query blocks), one warp per
+// query block a.
+//   * The list's query heads l*hpl .. l*hpl+hpl-1 read K/V heads
+//     (b*H + h) / group, a run kv0 .. kv1 of consecutive K/V heads.  For each,
+//     every warp adds the query means of the heads sharing it into its row
+//     of qs, the CTA stages 32 key means at a time into shared memory (rows
+//     padded to D+1 floats, so that lane c reading row c hits bank (c+e) % 32)
+//     and lane c of each warp accumulates its query block's dot product with
+//     candidate c0 + c:  score(a, c) = scale * sum_j qsum_j . kbar[kv0 + j][c].
+//   * top_r rounds of warp-wide arg-max (larger score, then lower index); a
+//     picked block is marked NaN in the warp's score row, which no later round
+//     takes (scores themselves are NaN-free: a NaN score becomes -FLT_MAX).
+//   * The row (window and picks) is written in ascending order with ballots;
+//     row_ptr[l][a] = l * total + entries of rows 0 .. a-1, both counted here
+//     from the closed-form row sizes.
+constexpr int kSelWarps = 8;
+constexpr int kSelChunk = 32;       // key means staged per pass
+
 template <int D>
-__global__ void __launch_bounds__(kSelThreads) select_kernel(const float* qbar, const float* kbar,
-                                                            const int* prefix, int* col_idx, int n,
-                                                            int hpl, int top_r, int local,
-                                                            int causal, float scale, int H,
-                                                            int group) {
+constexpr size_t select_smem_bytes(int n) {
+  return (static_cast<size_t>(kSelChunk) * (D + 1) + static_cast<size_t>(kSelWarps) * D +
+          static_cast<size_t>(kSelWarps) * n) * sizeof(float);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
+    const float* qbar, const float* kbar, int* row_ptr, int* col_idx, int n, int hpl, int top_r,
+    int local, int causal, float scale, int group) {
+  constexpr int kThreads = kSelWarps * 32;
+  constexpr int kStride = D + 1;
   extern __shared__ float sel_smem[];
-  float* qs = sel_smem;               // [hpl][D] query block means of the list's heads
-  float* sc = sel_smem + hpl * D;     // [n] candidate scores (-inf: not a candidate)
-  __shared__ float red_v[kSelThreads / 32];
-  __shared__ int red_i[kSelThreads / 32];
-  __shared__ int picked[256];
-  const int l = blockIdx.x / n;
-  const int a = blockIdx.x - l * n;
+  float* ks = sel_smem;                                   // [kSelChunk][D+1] staged key means
+  float* qs = ks + kSelChunk * kStride;                   // [kSelWarps][D] summed query means
   const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int tiles = (n + kSelWarps - 1) / kSelWarps;
+  const int l = blockIdx.x / tiles;
+  const int a0 = (blockIdx.x - l * tiles) * kSelWarps;
+  const int a = a0 + warp;
+  const bool active = a < n;                              // tail warps only help stage
+  float* sc = qs + kSelWarps * D + static_cast<size_t>(warp) * n;   // this warp's score row
   const float NEG_INF = -__int_as_float(0x7f800000);
-  for (int i = tid; i < hpl * D; i += kSelThreads) {
-    const int x = i / D;
-    qs[i] = qbar[((static_cast<size_t>(l) * hpl + x) * n + a) * D + (i - x * D)];
-  }
-  __syncthreads();
   const int last = causal ? a : n - 1;
-  const int wlo = max(0, a - local + 1);
-  for (int c = tid; c < n; c += kSelThreads) {
-    float v = NEG_INF;
-    if (c <= last && !(c >= wlo && c <= a)) {
-      v = 0.f;
-      for (int x = 0; x < hpl; ++x) {
-        // query head (b, hq) = l*hpl + x reads the block means of K/V head hq / group
-        const int bhq = l * hpl + x;
-        const int bq = bhq / H;
-        const size_t bkv = static_cast<size_t>(bq) * (H / group) + (bhq - bq * H) / group;
-        const float* kr = kbar + (bkv * n + c) * D;
-        const float* qr = qs + x * D;
-        float dot = 0.f;
-#pragma unroll 8
-        for (int e = 0; e < D; ++e) dot = fmaf(qr[e], __ldg(kr + e), dot);
-        v += scale * dot;
+  const int n_cand = last + 1;
+  const int n_stage = causal ? min(n, a0 + kSelWarps) : n;   // candidates any warp scores
+  const long long h_lo = static_cast<long long>(l) * hpl;
+  const int kv0 = static_cast<int>(h_lo / group);
+  const int kv1 = static_cast<int>((h_lo + hpl - 1) / group);
+
+  for (int kvh = kv0; kvh <= kv1; ++kvh) {
+    if (active) {
+      const long long x0 = max(h_lo, static_cast<long long>(kvh) * group);
+      const long long x1 = min(h_lo + hpl, static_cast<long long>(kvh + 1) * group);
+      for (int e = lane; e < D; e += 32) {
+        float sum = 0.f;
+        for (long long x = x0; x < x1; ++x) sum += __ldg(qbar + (x * n + a) * D + e);
+        qs[warp * D + e] = sum;
       }
-      if (!(v == v)) v = -3.402823466e38f;   // a NaN score ranks last among candidates
+    }
+    const float* kb = kbar + static_cast<size_t>(kvh) * n * D;
+    for (int c0 = 0; c0 < n_stage; c0 += kSelChunk) {
+      __syncthreads();                  // the previous chunk is consumed
+      constexpr int kVecs = kSelChunk * D / 4;
+#pragma unroll
+      for (int f = tid; f < kVecs; f += kThreads) {
+        const int r = f / (D / 4);
+        const int col = (f - r * (D / 4)) * 4;
+        const int c = min(c0 + r, n - 1);
+        const float4 t = __ldg(reinterpret_cast<const float4*>(kb + static_cast<size_t>(c) * D + col));
+        float* dst = ks + r * kStride + col;
+        dst[0] = t.x;
+        dst[1] = t.y;
+        dst[2] = t.z;
+        dst[3] = t.w;
+      }
+      __syncthreads();
+      if (active && c0 < n_cand) {
+        const float* kr = ks + lane * kStride;
+        const float* qr = qs + warp * D;
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll 8
+        for (int e = 0; e < D; e += 4) {
+          const float4 qv = *reinterpret_cast<const float4*>(qr + e);
+          acc0 = fmaf(qv.x, kr[e], acc0);
+          acc1 = fmaf(qv.y, kr[e + 1], acc1);
+          acc2 = fmaf(qv.z, kr[e + 2], acc2);
+          acc3 = fmaf(qv.w, kr[e + 3], acc3);
+        }
+        const float dot = (acc0 + acc1) + (acc2 + acc3);
+        const int c = c0 + lane;
+        if (c < n) sc[c] = kvh == kv0 ? dot : sc[c] + dot;
+      }
+    }
+    __syncthreads();                    // qs is rewritten for the next K/V head
+  }
+  if (!active) return;
+
+  // row offsets: entries of rows 0 .. a-1 and of the whole list
+  int before = 0, total = 0;
+  for (int r = lane; r < n; r += 32) {
+    const int cnt = select_row_count(r, n, top_r, local, causal);
+    total += cnt;
+    if (r < a) before += cnt;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    before += __shfl_xor_sync(0xFFFFFFFFu, before, off);
+    total += __shfl_xor_sync(0xFFFFFFFFu, total, off);
+  }
+  const long long list_base = static_cast<long long>(l) * total;
+  if (lane == 0) {
+    row_ptr[static_cast<size_t>(l) * (n + 1) + a] = static_cast<int>(list_base + before);
+    if (a == n - 1) row_ptr[static_cast<size_t>(l) * (n + 1) + n] = static_cast<int>(list_base + total);
+  }
+
+  // final scores; window and non-candidates are -inf
+  const int wlo = max(0, a - local + 1);
+  for (int c = lane; c < n; c += 32) {
+    float v = NEG_INF;
+    if (c < n_cand && !(c >= wlo && c <= a)) {
+      v = scale * sc[c];
+      // a NaN or -inf score ranks last among candidates (and stays one)
+      if (!(v == v) || v == NEG_INF) v = -3.402823466e38f;
     }
     sc[c] = v;
   }
-  __syncthreads();
+  __syncwarp();
   const int window = min(a + 1, local);
-  const int k = min(top_r, last + 1 - window);
+  const int k = min(top_r, n_cand - window);
+  const float NAN_MARK = __int_as_float(0x7fc00000);
   for (int round = 0; round < k; ++round) {
     float bv = NEG_INF;
     int bi = 0x7fffffff;
-    for (int c = tid; c <= last; c += kSelThreads) {
+    for (int c = lane; c < n_cand; c += 32) {
       const float v = sc[c];
-      if (v != NEG_INF && ranks_before(v, c, bv, bi)) {
+      if (v != NEG_INF && ranks_before(v, c, bv, bi)) {   // NaN (picked) never ranks
         bv = v;
         bi = c;
       }
@@ -134,63 +244,47 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const float* qbar, 
         bi = oi;
       }
     }
-    if ((tid & 31) == 0) {
-      red_v[tid >> 5] = bv;
-      red_i[tid >> 5] = bi;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      for (int w = 1; w < kSelThreads / 32; ++w)
-        if (ranks_before(red_v[w], red_i[w], bv, bi)) {
-          bv = red_v[w];
-          bi = red_i[w];
-        }
-      picked[round] = bi;
-      sc[bi] = NEG_INF;
-    }
-    __syncthreads();
+    if (lane == 0 && bi < n_cand) sc[bi] = NAN_MARK;
+    __syncwarp();
   }
-  if (tid == 0) {
-    // window then picks, sorted ascending (insertion sort of at most 256)
-    int row[256];
-    int m = 0;
-    for (int c = wlo; c <= a && c <= last; ++c) row[m++] = c;
-    for (int r = 0; r < k; ++r) {
-      const int v = picked[r];
-      int j = m++;
-      while (j > 0 && row[j - 1] > v) {
-        row[j] = row[j - 1];
-        --j;
-      }
-      row[j] = v;
+  // ascending write of the window and the picks
+  int* dst = col_idx + list_base + before;
+  int written = 0;
+  for (int c0 = 0; c0 < n_cand; c0 += 32) {
+    const int c = c0 + lane;
+    bool keep = false;
+    if (c < n_cand) {
+      const float v = sc[c];
+      keep = (c >= wlo && c <= a) || !(v == v);
     }
-    int* dst = col_idx + static_cast<size_t>(l) * prefix[n] + prefix[a];
-    for (int j = 0; j < m; ++j) dst[j] = row[j];
+    const unsigned ballot = __ballot_sync(0xFFFFFFFFu, keep);
+    if (keep) dst[written + __popc(ballot & ((1u << lane) - 1u))] = c;
+    written += __popc(ballot);
   }
 }
 
 template <int D>
 cudaError_t launch_select_d(const __nv_bfloat16* q, const __nv_bfloat16* k, int B, int H, int Hkv,
                             int L, int n_lists, int top_r, int local, int causal, float scale,
-                            int* row_ptr, int* col_idx, float* qbar, float* kbar, int* prefix,
+                            int* row_ptr, int* col_idx, float* qbar, float* kbar,
                             cudaStream_t st) {
   const int n = (L + kTileN - 1) / kTileN;
   const long long bhn = static_cast<long long>(B) * H * n;
   const long long bkvn = static_cast<long long>(B) * Hkv * n;
-  pool_blocks_kernel<D><<<static_cast<unsigned>(bhn), D, 0, st>>>(q, qbar, L, n);
-  pool_blocks_kernel<D><<<static_cast<unsigned>(bkvn), D, 0, st>>>(k, kbar, L, n);
+  pool_blocks_kernel<D><<<static_cast<unsigned>(bhn + bkvn), kPoolThreads, 0, st>>>(
+      q, k, qbar, kbar, L, n, bhn);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  select_rowptr_kernel<<<1, kSelThreads, 0, st>>>(prefix, row_ptr, n_lists, n, top_r, local, causal);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int group = H / Hkv;
   const int hpl = static_cast<int>(static_cast<long long>(B) * H / n_lists);
-  const size_t smem = (static_cast<size_t>(hpl) * D + n) * sizeof(float);
+  const size_t smem = select_smem_bytes<D>(n);
   auto kern = select_kernel<D>;
   if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(smem))) != cudaSuccess)
     return e;
-  kern<<<static_cast<unsigned>(static_cast<long long>(n_lists) * n), kSelThreads, smem, st>>>(
-      qbar, kbar, prefix, col_idx, n, hpl, top_r, local, causal, scale, H, H / Hkv);
+  const long long tiles = (n + kSelWarps - 1) / kSelWarps;
+  kern<<<static_cast<unsigned>(n_lists * tiles), kSelWarps * 32, smem, st>>>(
+      qbar, kbar, row_ptr, col_idx, n, hpl, top_r, local, causal, scale, group);
   return cudaGetLastError();
 }
 
@@ -205,15 +299,15 @@ int select_row_entries(int L, int top_r, int local, int causal) {
 
 cudaError_t launch_select(int d, const void* q, const void* k, int B, int H, int Hkv, int L,
                           int n_lists, int top_r, int local, int causal, float scale, int* row_ptr,
-                          int* col_idx, float* qbar, float* kbar, int* prefix, cudaStream_t st) {
+                          int* col_idx, float* qbar, float* kbar, cudaStream_t st) {
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
   const auto* kk = static_cast<const __nv_bfloat16*>(k);
   if (d == 64)
     return launch_select_d<64>(qq, kk, B, H, Hkv, L, n_lists, top_r, local, causal, scale, row_ptr,
-                               col_idx, qbar, kbar, prefix, st);
+                               col_idx, qbar, kbar, st);
   if (d == 128)
     return launch_select_d<128>(qq, kk, B, H, Hkv, L, n_lists, top_r, local, causal, scale, row_ptr,
-                                col_idx, qbar, kbar, prefix, st);
+                                col_idx, qbar, kbar, st);
   return cudaErrorInvalidValue;
 }
 

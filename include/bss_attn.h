@@ -188,18 +188,19 @@ attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, 
  * it chooses an exact set: selected blocks united with a mandatory local
  * window; 'Fixed pooling: a cheap proxy, not the true block mass') and
  * section 6 (query heads that share a KV head share the block choice).
- *   q, k [B,H,L,d] bf16 (device).  Per 128-row block the query and key rows
- *   are averaged (fp32); query block a scores key block c by the sum, over
- *   the heads that share a list, of scale * qbar_a . kbar_c (the block pair's
- *   mean logit).  Row a keeps the local window a, a-1, .., a-local_blocks+1
+ *   q [B,H,L,d], k [B,H_kv,L,d] bf16 (device).  Per 128-row block the query
+ *   and key rows are averaged (fp32); query block a scores key block c by the
+ *   sum, over the query heads that share a list, of scale * qbar_a . kbar_c
+ *   (the block pair's mean logit), query head h pooling the keys of K/V head
+ *   h / (H / H_kv).  Row a keeps the local window a, a-1, .., a-local_blocks+1
  *   (those >= 0) and the top_r other candidates (under a causal mask only
  *   blocks <= a), larger score first, the lower index on equal scores, listed
  *   in ascending order.  n_lists as in attn_fwd_blocksparse.
  *   Out (device): row_ptr [n_lists][n+1] (offsets into col_idx),
  *   col_idx [attn_select_blocks_nnz(...)] int32 - the input format of
  *   attn_fwd_blocksparse and attn_bwd_blocksparse.
- *   block must be 128; top_r + local_blocks <= 256; the heads of one list
- *   times d, plus n, must fit 200 KB of fp32 (else ATTN_ERR_UNSUPPORTED).
+ *   block must be 128; top_r + local_blocks <= 256; ceil(L/128) <= 4096 and
+ *   n_lists * entries per list < 2^31 (else ATTN_ERR_UNSUPPORTED).
  *   workspace: device, 16-byte aligned, >= attn_select_blocks_workspace_bytes.
  */
 size_t attn_select_blocks_workspace_bytes(int B, int H, int L, int d);

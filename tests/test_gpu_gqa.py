@@ -25,12 +25,8 @@ def bss():
 
 
 def gqa_inputs(w: Workload, Hkv: int):
-    """q (and do) with w.H heads; k, v with Hkv heads from a draw of their own."""
-    cpu = make_inputs(w)
-    kv = make_inputs(Workload(w.name, w.B, Hkv, w.L, w.d, w.causal, w.seed + 1000,
-                              w.value_scale))
-    cpu["k"], cpu["v"] = kv["k"], kv["v"]
-    return cpu
+    """q (and do) with w.H heads, k and v with Hkv heads, drawn in that order."""
+    return make_inputs(w, Hkv=Hkv)
 
 
 def _repeat(t, G):

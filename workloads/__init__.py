@@ -46,6 +46,7 @@ class Workload:
     backward: bool = False
     description: str = ""
     Lq: Optional[int] = None  # decode-shaped: only the last Lq rows of the draw are queries
+    Hkv: Optional[int] = None  # grouped key/value heads (None: Hkv = H)
 
     @property
     def scale(self) -> float:
@@ -82,15 +83,24 @@ DECODE_16K = Workload("decode_B4_H16_Lq16_Lk16384_d128", 4, 16, 16384, 128, True
                       description="decode-shaped forward: 16 queries at the end of a 16384-key "
                                   "causal cache, 16 KV chunks merged")
 
-ALL = [DENSE_SMALL, CAUSAL_4K, SPARSE_16K, SPLITKV_128K, BWD_8K, CAUSAL_16K, DECODE_16K]
+# Grouped key/value heads: the L=16384 causal shape with 4 key/value heads, each
+# shared by 4 query heads; forward and backward.
+GQA_16K = Workload("gqa_B2_H16_Hkv4_L16384_d128", 2, 16, 16384, 128, True, 6, backward=True,
+                   Hkv=4,
+                   description="causal forward + backward, 16 query heads over 4 shared "
+                               "key/value heads, L=16384 d=128")
+
+ALL = [DENSE_SMALL, CAUSAL_4K, SPARSE_16K, SPLITKV_128K, BWD_8K, CAUSAL_16K, DECODE_16K, GQA_16K]
 BY_NAME = {w.name: w for w in ALL}
 
 
-def randn_bf16(shape, seed: int, count: int, value_scale: float = 1.0) -> List[torch.Tensor]:
-    """``count`` tensors of ``shape`` drawn in order from one seeded CPU generator."""
+def randn_bf16(shape, seed: int, count: int, value_scale: float = 1.0,
+               shapes=None) -> List[torch.Tensor]:
+    """``count`` tensors of ``shape`` (or of the listed ``shapes``) drawn in order
+    from one seeded CPU generator."""
     g = torch.Generator("cpu").manual_seed(seed)
     out = []
-    for _ in range(count):
+    for shape in (shapes if shapes is not None else [shape] * count):
         t = torch.randn(shape, generator=g, dtype=torch.float32)
         if value_scale != 1.0:
             t = t * value_scale
@@ -99,17 +109,20 @@ def randn_bf16(shape, seed: int, count: int, value_scale: float = 1.0) -> List[t
 
 
 def make_inputs(w: Workload, L: Optional[int] = None, B: Optional[int] = None,
-                H: Optional[int] = None) -> Dict[str, torch.Tensor]:
-    """bf16 CPU tensors q, k, v (and do for backward workloads), shape [B,H,L,d].
+                H: Optional[int] = None, Hkv: Optional[int] = None) -> Dict[str, torch.Tensor]:
+    """bf16 CPU tensors q, k, v (and do for backward workloads): q and do
+    [B,H,L,d], k and v [B,Hkv,L,d] (Hkv = H unless the workload groups heads).
 
-    ``L``, ``B``, ``H`` override the workload's sizes for reduced test cases;
-    the distribution and draw order stay the same.
+    ``L``, ``B``, ``H``, ``Hkv`` override the workload's sizes for reduced test
+    cases; the distribution and draw order stay the same.
     """
     B = w.B if B is None else B
     H = w.H if H is None else H
     L = w.L if L is None else L
+    Hkv = (w.Hkv if w.Hkv is not None else H) if Hkv is None else Hkv
     n = 4 if w.backward else 3
-    ts = randn_bf16((B, H, L, w.d), w.seed, n, w.value_scale)
+    qs, kvs = (B, H, L, w.d), (B, Hkv, L, w.d)
+    ts = randn_bf16(None, w.seed, n, w.value_scale, shapes=[qs, kvs, kvs, qs][:n])
     names = ["q", "k", "v", "do"][:n]
     out = dict(zip(names, ts))
     if w.Lq is not None:                 # decode-shaped: queries are the last Lq positions

@@ -94,39 +94,48 @@ __device__ __forceinline__ bool ranks_before(float v1, int i1, float v2, int i2)
   return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
-// One CTA per (list l, kSelWarps consecutive query blocks), one warp per
-// query block a.
+// One CTA per (list l, kSelWarps consecutive query blocks a0 .. a0+7).
 //   * The list's query heads l*hpl .. l*hpl+hpl-1 read K/V heads
 //     (b*H + h) / group, a run kv0 .. kv1 of consecutive K/V heads.  For each,
-//     every warp adds the query means of the heads sharing it into its row
-//     of qs, the CTA stages 32 key means at a time into shared memory (rows
-//     padded to D+1 floats, so that lane c reading row c hits bank (c+e) % 32)
-//     and lane c of each warp accumulates its query block's dot product with
-//     candidate c0 + c:  score(a, c) = scale * sum_j qsum_j . kbar[kv0 + j][c].
-//   * top_r rounds of warp-wide arg-max (larger score, then lower index); a
-//     picked block is marked NaN in the warp's score row, which no later round
-//     takes (scores themselves are NaN-free: a NaN score becomes -FLT_MAX).
+//     warp w adds the query means of the heads sharing it into row w of qs;
+//     then warp w copies the key means of candidates c0 + 16*w .. +15 into its
+//     slice of shared memory (one coalesced 512-byte row per load, rows padded
+//     by 4 floats so that 16-byte reads of eight consecutive rows hit distinct
+//     banks), and lane i takes candidate c0 + 16*w + i%16 and half i/16 of the
+//     d dimensions and accumulates it against all eight query rows, so each
+//     key value feeds eight fused multiply-adds.  The two halves meet by one
+//     shuffle and the scores land in the rows' score arrays:
+//     score(a, c) = scale * sum_j qsum_j . kbar[kv0 + j][c].
+//   * Warp w then owns query block a0 + w: top_r rounds of warp-wide arg-max
+//     (larger score, then lower index); a picked block is marked NaN in the
+//     row, which no later round takes (scores themselves are NaN-free: a NaN
+//     score becomes -FLT_MAX).
 //   * The row (window and picks) is written in ascending order with ballots;
 //     row_ptr[l][a] = l * total + entries of rows 0 .. a-1, both counted here
 //     from the closed-form row sizes.
 constexpr int kSelWarps = 8;
-constexpr int kSelChunk = 32;       // key means staged per pass
+constexpr int kSelRows = 16;                        // candidates per warp and pass
+constexpr int kSelPass = kSelWarps * kSelRows;      // candidates scored per pass
 
 template <int D>
-constexpr size_t select_smem_bytes(int n) {
-  return (static_cast<size_t>(kSelChunk) * (D + 1) + static_cast<size_t>(kSelWarps) * D +
-          static_cast<size_t>(kSelWarps) * n) * sizeof(float);
+__host__ __device__ constexpr int select_kstride() { return D + 4; }
+
+template <int D>
+__host__ __device__ constexpr size_t select_smem_bytes(int n) {
+  return (static_cast<size_t>(kSelWarps) * kSelRows * select_kstride<D>() +
+          static_cast<size_t>(kSelWarps) * D + static_cast<size_t>(kSelWarps) * n) * sizeof(float);
 }
 
 template <int D>
 __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
     const float* qbar, const float* kbar, int* row_ptr, int* col_idx, int n, int hpl, int top_r,
     int local, int causal, float scale, int group) {
-  constexpr int kThreads = kSelWarps * 32;
-  constexpr int kStride = D + 1;
+  constexpr int kHalf = D / 2;
+  constexpr int kStride = select_kstride<D>();
   extern __shared__ float sel_smem[];
-  float* ks = sel_smem;                                   // [kSelChunk][D+1] staged key means
-  float* qs = ks + kSelChunk * kStride;                   // [kSelWarps][D] summed query means
+  float* ks = sel_smem;                                   // [kSelWarps][kSelRows][D+4] key means
+  float* qs = ks + kSelWarps * kSelRows * kStride;        // [kSelWarps][D] summed query means
+  float* scs = qs + kSelWarps * D;                        // [kSelWarps][n] score rows
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -134,15 +143,17 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
   const int l = blockIdx.x / tiles;
   const int a0 = (blockIdx.x - l * tiles) * kSelWarps;
   const int a = a0 + warp;
-  const bool active = a < n;                              // tail warps only help stage
-  float* sc = qs + kSelWarps * D + static_cast<size_t>(warp) * n;   // this warp's score row
+  const bool active = a < n;                              // tail warps only help score
+  float* sc = scs + static_cast<size_t>(warp) * n;        // this warp's score row
   const float NEG_INF = -__int_as_float(0x7f800000);
   const int last = causal ? a : n - 1;
   const int n_cand = last + 1;
-  const int n_stage = causal ? min(n, a0 + kSelWarps) : n;   // candidates any warp scores
+  const int n_stage = causal ? min(n, a0 + kSelWarps) : n;   // candidates any row scores
+  const int rows = min(kSelWarps, n - a0);
   const long long h_lo = static_cast<long long>(l) * hpl;
   const int kv0 = static_cast<int>(h_lo / group);
   const int kv1 = static_cast<int>((h_lo + hpl - 1) / group);
+  const int half = lane >> 4;
 
   for (int kvh = kv0; kvh <= kv1; ++kvh) {
     if (active) {
@@ -154,41 +165,70 @@ __global__ void __launch_bounds__(kSelWarps * 32) select_kernel(
         qs[warp * D + e] = sum;
       }
     }
+    __syncthreads();                    // qs complete
     const float* kb = kbar + static_cast<size_t>(kvh) * n * D;
-    for (int c0 = 0; c0 < n_stage; c0 += kSelChunk) {
-      __syncthreads();                  // the previous chunk is consumed
-      constexpr int kVecs = kSelChunk * D / 4;
+    float* kw = ks + warp * kSelRows * kStride;
+    for (int c0 = 0; c0 < n_stage; c0 += kSelPass) {
+      const int cw = c0 + warp * kSelRows;               // this warp's first candidate
+      if (cw >= n_stage) continue;
+      {
+        if constexpr (D == 128) {
+          float4 t[kSelRows];
 #pragma unroll
-      for (int f = tid; f < kVecs; f += kThreads) {
-        const int r = f / (D / 4);
-        const int col = (f - r * (D / 4)) * 4;
-        const int c = min(c0 + r, n - 1);
-        const float4 t = __ldg(reinterpret_cast<const float4*>(kb + static_cast<size_t>(c) * D + col));
-        float* dst = ks + r * kStride + col;
-        dst[0] = t.x;
-        dst[1] = t.y;
-        dst[2] = t.z;
-        dst[3] = t.w;
-      }
-      __syncthreads();
-      if (active && c0 < n_cand) {
-        const float* kr = ks + lane * kStride;
-        const float* qr = qs + warp * D;
-        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll 8
-        for (int e = 0; e < D; e += 4) {
-          const float4 qv = *reinterpret_cast<const float4*>(qr + e);
-          acc0 = fmaf(qv.x, kr[e], acc0);
-          acc1 = fmaf(qv.y, kr[e + 1], acc1);
-          acc2 = fmaf(qv.z, kr[e + 2], acc2);
-          acc3 = fmaf(qv.w, kr[e + 3], acc3);
+          for (int i = 0; i < kSelRows; ++i)
+            t[i] = __ldg(reinterpret_cast<const float4*>(
+                kb + static_cast<size_t>(min(cw + i, n - 1)) * D + lane * 4));
+#pragma unroll
+          for (int i = 0; i < kSelRows; ++i)
+            *reinterpret_cast<float4*>(kw + i * kStride + lane * 4) = t[i];
+        } else {
+          // D = 64: a row is 16 float4, two rows per load
+          float4 t[kSelRows / 2];
+#pragma unroll
+          for (int i = 0; i < kSelRows / 2; ++i) {
+            const int row = 2 * i + (lane >> 4);
+            t[i] = __ldg(reinterpret_cast<const float4*>(
+                kb + static_cast<size_t>(min(cw + row, n - 1)) * D + (lane & 15) * 4));
+          }
+#pragma unroll
+          for (int i = 0; i < kSelRows / 2; ++i) {
+            const int row = 2 * i + (lane >> 4);
+            *reinterpret_cast<float4*>(kw + row * kStride + (lane & 15) * 4) = t[i];
+          }
         }
-        const float dot = (acc0 + acc1) + (acc2 + acc3);
-        const int c = c0 + lane;
-        if (c < n) sc[c] = kvh == kv0 ? dot : sc[c] + dot;
       }
+      __syncwarp();
+      const int c = cw + (lane & 15);
+      const float* kr = kw + (lane & 15) * kStride + half * kHalf;
+      float acc[kSelWarps];
+#pragma unroll
+      for (int r = 0; r < kSelWarps; ++r) acc[r] = 0.f;
+#pragma unroll 4
+      for (int e = 0; e < kHalf; e += 4) {
+        const float4 kv = *reinterpret_cast<const float4*>(kr + e);
+#pragma unroll
+        for (int r = 0; r < kSelWarps; ++r) {
+          const float4 qv = *reinterpret_cast<const float4*>(qs + r * D + half * kHalf + e);
+          acc[r] = fmaf(qv.x, kv.x, acc[r]);
+          acc[r] = fmaf(qv.y, kv.y, acc[r]);
+          acc[r] = fmaf(qv.z, kv.z, acc[r]);
+          acc[r] = fmaf(qv.w, kv.w, acc[r]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kSelWarps; ++r) acc[r] += __shfl_xor_sync(0xFFFFFFFFu, acc[r], 16);
+      if (half == 0 && c < n_stage) {
+#pragma unroll
+        for (int r = 0; r < kSelWarps; ++r) {
+          if (r < rows) {
+            float* dst = scs + static_cast<size_t>(r) * n + c;
+            *dst = kvh == kv0 ? acc[r] : *dst + acc[r];
+          }
+        }
+      }
+      __syncwarp();                     // kw is refilled by the next pass
     }
-    __syncthreads();                    // qs is rewritten for the next K/V head
+    __syncthreads();                    // scores of this K/V head in; qs reusable
   }
   if (!active) return;
 

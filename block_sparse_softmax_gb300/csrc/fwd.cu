@@ -617,16 +617,17 @@ __global__ void __launch_bounds__(384, 1)
             for (int j = 0; j < 32; ++j)
               if (c * 32 + j > jl) s[c][j] = __float_as_uint(NEG_INF);
         }
-        // row max over 8 independent chains (short dependency chains)
+        // row max over 8 independent chains of three-input max (short chains)
         float mx[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) mx[u] = __uint_as_float(s[0][u]);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int j = (c == 0 ? 8 : 0); j < 32; j += 8)
+          for (int j = (c == 0 ? 8 : 0); j < 32; j += 16)
 #pragma unroll
-            for (int u = 0; u < 8; ++u) mx[u] = fmaxf(mx[u], __uint_as_float(s[c][j + u]));
+            for (int u = 0; u < 8; ++u)
+              mx[u] = fmax3(mx[u], __uint_as_float(s[c][j + u]), __uint_as_float(s[c][j + 8 + u]));
         const float mblk = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                  fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
         BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt + 1);
@@ -639,9 +640,11 @@ __global__ void __launch_bounds__(384, 1)
           moved = true;
         }
         const float mu = (m2 == NEG_INF) ? 0.f : m2;
-        float rs[4];
+        // pairs of columns: one packed FMA for the two exponents' arguments,
+        // one packed add into four pairs of running sums
+        float rs[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) rs[u] = 0.f;
+        for (int u = 0; u < 8; ++u) rs[u] = 0.f;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t pk[32];
@@ -650,15 +653,19 @@ __global__ void __launch_bounds__(384, 1)
             const int c = half * 2 + c2;
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-              const float p0 = ex2(fmaf(__uint_as_float(s[c][j]), sl2, -mu));
-              const float p1 = ex2(fmaf(__uint_as_float(s[c][j + 1]), sl2, -mu));
-              rs[(j >> 1) & 3] += p0 + p1;
+              float x0, x1;
+              ffma2(x0, x1, __uint_as_float(s[c][j]), __uint_as_float(s[c][j + 1]), sl2, sl2, -mu,
+                    -mu);
+              const float p0 = ex2(x0);
+              const float p1 = ex2(x1);
+              const int u = (j >> 1) & 3;
+              fadd2(rs[2 * u], rs[2 * u + 1], rs[2 * u], rs[2 * u + 1], p0, p1);
               pk[c2 * 16 + j / 2] = pack_bf16(p0, p1);
             }
           }
           tmem_st32(tP + half * 32, pk);
         }
-        l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+        l = l * alpha + (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
         BSS_TRACE_EV(p, trw, 2 + t, 4 * cnt + 2);
         // rescale O when this row's reference max moved and O already holds data
         const bool fix = moved && ci > 0;

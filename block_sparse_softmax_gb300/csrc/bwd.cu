@@ -430,17 +430,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const float scale = p.scale;
     const float INF = __int_as_float(0x7f800000);
     uint8_t* ds_row = smem + C::kDSOff + X * C::kChunkBytes + kr * 128;   // this key's dS row
-    // statistics of query tile i of query head hq0 + g
-    auto load_stats = [&](int g, int i, float& l2, float& dl) {
+    // statistics of query tile i of query head hq0 + g, negated so that
+    // P = ex2(S sl2 + nl2) and dP - D = dP scale + ndl are single FMAs
+    auto load_stats = [&](int g, int i, float& nl2, float& ndl) {
       const int q = i * kTileM + kr;
       if (i >= 0 && i < nq && q < L) {
         const size_t stat_base = static_cast<size_t>(bhq0 + g) * L;
         const float lse = __ldg(p.lse + stat_base + q);
-        l2 = (lse == -INF) ? INF : lse * kLog2e;      // an empty row contributes nothing
-        dl = __ldg(p.delta + stat_base + q) * scale;
+        nl2 = (lse == -INF) ? -INF : -(lse * kLog2e);  // an empty row contributes nothing
+        ndl = -(__ldg(p.delta + stat_base + q) * scale);
       } else {
-        l2 = INF;
-        dl = 0.f;
+        nl2 = -INF;
+        ndl = 0.f;
       }
     };
     if (X == 0) {
@@ -450,8 +451,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       stats[128 + kr] = dl;
       mbar_arrive(bar(C::kBarStat + 0));
     }
-    // Buffer (it & 1) holds the statistics of the it-th query tile met (LSE in
-    // log2 units, scale * D).  It is rewritten (for tile it + 2) at the end of tile
+    // Buffer (it & 1) holds the statistics of the it-th query tile met (minus
+    // the LSE in log2 units, minus scale * D).  It is rewritten (for tile it + 2) at the end of tile
     // it + 1 by half 0; by then dP^T(it + 1) has been issued, which waited for
     // dS(it) of both halves, so nobody reads it for tile it any more.
     bool ok = true;
@@ -476,9 +477,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       BSS_TRACE_EV(p, trw, 2, 4 * it);
       tc_fence_after();
       const bool key_ok = key < L;
-      // element mask: diagonal tile (query < key); the ragged tail (query >= L)
-      // has lse2 = +inf, so P is 0 there already
+      // element mask: diagonal tile (query < key) and keys past L; the ragged
+      // tail (query >= L) has -lse2 = -inf, so P is 0 there already
       const bool diag = CAUSAL && (i == j);
+      const bool need_mask = !key_ok || diag;
       // ---- phase 1: P (four chunks of 16 queries; chunk c+1's TMEM load is in
       // flight while chunk c is computed) ----
       float pf[4][16];
@@ -494,13 +496,18 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; e += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(lse2 + 16 * c + e);
-            const float la[4] = {l4.x, l4.y, l4.z, l4.w};
+            float x[4];
+            ffma2(x[0], x[1], __uint_as_float(sv[cur][e]), __uint_as_float(sv[cur][e + 1]), sl2,
+                  sl2, l4.x, l4.y);
+            ffma2(x[2], x[3], __uint_as_float(sv[cur][e + 2]), __uint_as_float(sv[cur][e + 3]),
+                  sl2, sl2, l4.z, l4.w);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              float pv = ex2(fmaf(__uint_as_float(sv[cur][e + u]), sl2, -la[u]));
-              if (!key_ok || (diag && col + e + u < kr)) pv = 0.f;
-              pf[c][e + u] = pv;
-            }
+            for (int u = 0; u < 4; ++u) pf[c][e + u] = ex2(x[u]);
+          }
+          if (need_mask) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (!key_ok || col + e < kr) pf[c][e] = 0.f;
           }
           uint32_t pk[8];
 #pragma unroll
@@ -532,10 +539,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; e += 4) {
             const float4 d4 = *reinterpret_cast<const float4*>(dlt + 16 * c + e);
-            const float da[4] = {d4.x, d4.y, d4.z, d4.w};
             float ds[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) ds[u] = pf[c][e + u] * fmaf(__uint_as_float(dv[cur][e + u]), scale, -da[u]);
+            ffma2(ds[0], ds[1], __uint_as_float(dv[cur][e]), __uint_as_float(dv[cur][e + 1]), scale,
+                  scale, d4.x, d4.y);
+            ffma2(ds[2], ds[3], __uint_as_float(dv[cur][e + 2]), __uint_as_float(dv[cur][e + 3]),
+                  scale, scale, d4.z, d4.w);
+            fmul2(ds[0], ds[1], pf[c][e], pf[c][e + 1], ds[0], ds[1]);
+            fmul2(ds[2], ds[3], pf[c][e + 2], pf[c][e + 3], ds[2], ds[3]);
             dk[e / 2] = pack_bf16(ds[0], ds[1]);
             dk[e / 2 + 1] = pack_bf16(ds[2], ds[3]);
           }

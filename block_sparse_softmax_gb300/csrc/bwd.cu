@@ -66,12 +66,12 @@ struct BwdCfg {
   static constexpr int kBarDOFull = kBarQEmpty + kStagesQ;
   static constexpr int kBarDOEmpty = kBarDOFull + kStagesDO;
   static constexpr int kBarSFull = kBarDOEmpty + kStagesDO;   // S^T of a query tile in TMEM
-  static constexpr int kBarDPFull = kBarSFull + 1;            // dP^T in TMEM
-  static constexpr int kBarPReady = kBarDPFull + 1;           // P^T written (S^T read)
+  static constexpr int kBarDPFull = kBarSFull + 1;            // [2]: dP^T query half h in TMEM
+  static constexpr int kBarPReady = kBarDPFull + 2;           // P^T written (S^T read)
   static constexpr int kBarDSReady = kBarPReady + 1;          // dS in shared memory (dP^T read)
   static constexpr int kBarDQFull = kBarDSReady + 1;
-  static constexpr int kBarDQFree = kBarDQFull + 1;
-  static constexpr int kBarDKVFull = kBarDQFree + 1;
+  static constexpr int kBarDQFree = kBarDQFull + 1;           // [2]: dQ d-columns [64r, 64r+64) read
+  static constexpr int kBarDKVFull = kBarDQFree + 2;
   static constexpr int kBarMmaDone = kBarDKVFull + 1;
   static constexpr int kBarStat = kBarMmaDone + 1;     // [2]: LSE/D of a query tile staged
   static constexpr int kBarStaged = kBarStat + 2;      // dQ round written to the staging buffer
@@ -241,10 +241,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     mbar_init(bar(C::kBarSFull), 1);
     mbar_init(bar(C::kBarDPFull), 1);
+    mbar_init(bar(C::kBarDPFull + 1), 1);
     mbar_init(bar(C::kBarPReady), 256);
     mbar_init(bar(C::kBarDSReady), 256);
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQFree), 128);
+    mbar_init(bar(C::kBarDQFree + 1), 128);
     mbar_init(bar(C::kBarDKVFull), 1);
     mbar_init(bar(C::kBarMmaDone), 1);
     mbar_init(bar(C::kBarStat + 0), 128);
@@ -339,8 +341,29 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mma_commit(bar(C::kBarSFull));
         return true;
       };
-      // dP^T(it) = V_j dO^T
+      // dP^T(it) = V_j dO^T, in two halves of 64 queries (N = 64) when dQ
+      // shares dP^T's columns: half h overwrites dQ's d-columns [64h, 64h+64),
+      // which round h of the drain frees, and feeds P/dS half X = h alone.
+      constexpr uint32_t kIdescTHalf = idesc_bf16_f32(kTileM, kTileN / 2, false, false);
+      auto issue_dp_half = [&](int it, int h) -> bool {
+        if (h == 0) {
+          if (!wait_bar(bar(C::kBarDOFull + it % C::kStagesDO), (it / C::kStagesDO) & 1, abort_flag,
+                        p.err))
+            return false;
+        }
+        tc_fence_after();
+        const uint32_t doa = doaddr(it) + h * (kTileN / 2) * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+          mma_ss(tmem + C::kColDPT + h * (kTileN / 2), sdesc_sw128(va + off, 16, 1024),
+                 sdesc_sw128(doa + off, 16, 1024), kIdescTHalf, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kBarDPFull + h));
+        return true;
+      };
       auto issue_dp = [&](int it) -> bool {
+        if (C::kDQOverDP) return issue_dp_half(it, 0) && issue_dp_half(it, 1);
         if (!wait_bar(bar(C::kBarDOFull + it % C::kStagesDO), (it / C::kStagesDO) & 1, abort_flag, p.err))
           return false;
         tc_fence_after();
@@ -352,6 +375,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
                  kIdescT, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kBarDPFull));
+        mma_commit(bar(C::kBarDPFull + 1));
         return true;
       };
       bool ok = wait_bar(bar(C::kBarKV), 0, abort_flag, p.err);
@@ -375,7 +399,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         if (more && !issue_s(it + 1)) break;
         // the P/dS warps run for a while: poll gently so that the issue slots
         // they share with this warp stay theirs
-        if (!wait_bar_relaxed<64>(bar(C::kBarDSReady), it & 1, abort_flag, p.err)) break;
+        if (!wait_bar_relaxed(bar(C::kBarDSReady), it & 1, abort_flag, p.err)) break;
         BSS_TRACE_EV(p, tr, 1, 4 * it + 1);
         tc_fence_after();
         // dQ_i = dS K_j  (M = queries, N = d, K dimension = the 128 keys); with
@@ -400,10 +424,17 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mma_commit(bar(C::kBarQEmpty + it % C::kStagesQ));
         BSS_TRACE_EV(p, tr, 1, 4 * it + 2);
         if (more) {
-          // dP^T(i+1) over dQ(i): only once dQ(i) has been read out
-          if (C::kDQOverDP && !wait_bar(bar(C::kBarDQFree), it & 1, abort_flag, p.err)) break;
-          BSS_TRACE_EV(p, tr, 1, 4 * it + 3);
-          if (!issue_dp(it + 1)) break;
+          if (C::kDQOverDP) {
+            // dP^T(i+1) over dQ(i): each half once its columns have been read out
+            if (!wait_bar(bar(C::kBarDQFree), it & 1, abort_flag, p.err)) break;
+            if (!issue_dp_half(it + 1, 0)) break;
+            if (!wait_bar(bar(C::kBarDQFree + 1), it & 1, abort_flag, p.err)) break;
+            BSS_TRACE_EV(p, tr, 1, 4 * it + 3);
+            if (!issue_dp_half(it + 1, 1)) break;
+          } else {
+            BSS_TRACE_EV(p, tr, 1, 4 * it + 3);
+            if (!issue_dp(it + 1)) break;
+          }
         }
       }
       mma_commit(bar(C::kBarDKVFull));
@@ -520,7 +551,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       mbar_arrive(bar(C::kBarPReady));
       BSS_TRACE_EV(p, trw, 2, 4 * it + 1);
       // ---- phase 2: dS = P o (dP - D), into shared memory ----
-      if (!wait_bar(bar(C::kBarDPFull), it & 1, abort_flag, p.err)) {
+      if (!wait_bar(bar(C::kBarDPFull + X), it & 1, abort_flag, p.err)) {
         ok = false;
         break;
       }
@@ -634,11 +665,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tmem_ld32(tDQ + 64 * r + 32, v1);
         tmem_ld_wait(v0);
         tmem_ld_wait(v1);
-        if (r == kRounds - 1) {
-          tc_fence_before();
-          mbar_arrive(bar(C::kBarDQFree));          // every TMEM read of this tile is done
-          BSS_TRACE_EV(p, tr && qr == 0, 3, 3 * it + 1);
-        }
+        // d-columns [64r, 64r + 64) of this tile are read (at d=128 dP^T's
+        // half r may overwrite them; at d=64 the next dQ may)
+        tc_fence_before();
+        mbar_arrive(bar(C::kBarDQFree + r));
+        if (r == kRounds - 1) BSS_TRACE_EV(p, tr && qr == 0, 3, 3 * it + 1);
         // The reduce of the previous round must have read the staging buffer
         // before it is rewritten.
         if (g > 0) {

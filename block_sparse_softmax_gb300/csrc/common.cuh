@@ -21,6 +21,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // second at GB300 clocks) gives up, records ATTN_ERR_TIMEOUT and the kernel
 // unwinds.
 constexpr long long kWaitLimitCycles = 1ll << 31;
+constexpr uint32_t kWaitSuspendNs = 20000;   // longest single hardware suspension of a wait
 
 // Record the first error code in the library's device status word.
 __device__ __forceinline__ void record_error(int* err, int code) {
@@ -34,7 +35,8 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    // suspended until the phase completes (or ~20 us pass): no polling traffic
+    if (mbar_try_wait_suspend(bar, parity, kWaitSuspendNs)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       *abort_flag = 1;
@@ -119,17 +121,17 @@ constexpr int kTraceEvents = 1024;
 #define BSS_TRACE_EV(p, on, role, idx) ((void)0)
 #endif
 
-// Bounded wait for roles off the critical path: polls with a short sleep in
-// between so that waiting warps leave the issue slots to the computing ones.
-template <unsigned kSleepNs = 256>
+// Bounded wait for roles off the critical path: the thread is suspended in
+// hardware for up to kSleepNs at a time, so that waiting warps leave the
+// issue slots and the shared-memory pipe to the computing ones.
+template <unsigned kSleepNs = kWaitSuspendNs>
 __device__ __forceinline__ bool wait_bar_relaxed(uint32_t bar, uint32_t parity,
                                                  volatile int* abort_flag, int* err,
                                                  long long limit = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    __nanosleep(kSleepNs);
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_suspend(bar, parity, kSleepNs)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       *abort_flag = 1;

@@ -111,9 +111,9 @@ struct BwdCfg {
 // a thread).
 template <int D>
 struct BwdRegs {
-  static constexpr uint32_t kLow = 72;
+  static constexpr uint32_t kLow = 88;
   static constexpr uint32_t kMid = 160;
-  static constexpr uint32_t kHigh = 120;
+  static constexpr uint32_t kHigh = 104;
   static constexpr uint32_t kLaunchRegs = 128;
   static_assert(kLow + 2 * kMid + kHigh <= 512, "register split exceeds an SM sub-partition");
   static_assert(128 * (kLow + 2 * kMid + kHigh) <= 512 * kLaunchRegs, "register split exceeds the launch");
@@ -442,6 +442,31 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       drain_bar(bar(C::kBarMmaDone), 0);   // every MMA issued has completed
     }
   }
+#ifdef BSS_TRACE
+  else if (warp == 2 && lane == 0 && tr) {
+    // trace builds: watch the MMA groups complete (passive waits on the
+    // barriers their commits arrive at) for the pipeline trace
+    for (int it = 0; it < n_it && it < kTraceEvents / 8; ++it) {
+      const bool more = it + 1 < n_it;
+      if (!drain_bar(bar(C::kBarDOEmpty + it % C::kStagesDO), (it / C::kStagesDO) & 1, 1ll << 28)) break;
+      BSS_TRACE_EV(p, true, 4, 8 * it + 0);          // dV(it) done
+      if (more) {
+        if (!drain_bar(bar(C::kBarSFull), (it + 1) & 1, 1ll << 28)) break;
+        BSS_TRACE_EV(p, true, 4, 8 * it + 1);        // S^T(it+1) done
+      }
+      if (!drain_bar(bar(C::kBarDQFull), it & 1, 1ll << 28)) break;
+      BSS_TRACE_EV(p, true, 4, 8 * it + 2);          // dQ(it) done
+      if (!drain_bar(bar(C::kBarQEmpty + it % C::kStagesQ), (it / C::kStagesQ) & 1, 1ll << 28)) break;
+      BSS_TRACE_EV(p, true, 4, 8 * it + 3);          // dK(it) done
+      if (more) {
+        if (!drain_bar(bar(C::kBarDPFull), (it + 1) & 1, 1ll << 28)) break;
+        BSS_TRACE_EV(p, true, 4, 8 * it + 4);        // dP^T(it+1) half 0 done
+        if (!drain_bar(bar(C::kBarDPFull + 1), (it + 1) & 1, 1ll << 28)) break;
+        BSS_TRACE_EV(p, true, 4, 8 * it + 5);        // dP^T(it+1) half 1 done
+      }
+    }
+  }
+#endif
   } else if (warp < 12) {
     regs_set<BwdRegs<D>::kMid, BwdRegs<D>::kLaunchRegs>();
     // =================== P^T / dS: two warpgroups, thread = key row ===================

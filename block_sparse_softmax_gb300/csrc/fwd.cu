@@ -451,13 +451,13 @@ __global__ void __launch_bounds__(384, 1)
             if (!wait_bar(bar(C::kBarQFull + t), qn[t] & 1, abort_flag, p.err)) return false;
             qready[t] = true;
           }
-          const uint32_t qa = sbase + C::kQOff + t * C::kTileBytes;
-          const uint32_t ka = sbase + C::kKOff + sk * C::kTileBytes;
+          const uint64_t dq = sdesc_sw128(sbase + C::kQOff + t * C::kTileBytes, 16, 1024);
+          const uint64_t dk = sdesc_sw128(sbase + C::kKOff + sk * C::kTileBytes, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-            mma_ss(tmem + C::kColS + t * 128, sdesc_sw128(qa + off, 16, 1024),
-                   sdesc_sw128(ka + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::kColS + t * 128, sdesc_add(dq, off), sdesc_add(dk, off), kIdescQK,
+                   kk > 0 ? 1u : 0u);
           }
           mma_commit(bar(C::kBarSFull + t));
           // Q of this tile is free for the next item once its last S lands.
@@ -470,11 +470,11 @@ __global__ void __launch_bounds__(384, 1)
             if (!wait_bar(bar(C::kBarOEmpty + t), (on[t] - 1) & 1, abort_flag, p.err)) return false;
             tc_fence_after();
           }
-          const uint32_t va = sbase + C::kVOff + sv * C::kTileBytes;
+          const uint64_t dv = sdesc_sw128(sbase + C::kVOff + sv * C::kTileBytes, C::kChunkBytes, 1024);
 #pragma unroll
           for (int kk = 0; kk < kTileN / 16; ++kk) {
             mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * 128 + C::kColP + kk * 8,
-                   sdesc_sw128(va + kk * 16 * 128, C::kChunkBytes, 1024), kIdescPV,
+                   sdesc_add(dv, kk * 16 * 128), kIdescPV,
                    (ostarted[t] || kk > 0) ? 1u : 0u);
           }
           ostarted[t] = true;

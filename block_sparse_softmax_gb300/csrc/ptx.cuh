@@ -188,6 +188,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The descriptor of the same tile `byte_off` bytes further on: the 14-bit
+// start-address field holds address / 16 and shared memory is below 256 KB,
+// so a plain add cannot carry out of it.  Built once per MMA group from the
+// tile base, this keeps the issuing thread's work per MMA to one add.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t byte_off) {
+  return desc + static_cast<uint64_t>(byte_off >> 4);
+}
+
 // D[tmem] (+)= A[smem desc] * B[smem desc]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {

@@ -100,15 +100,16 @@ attn_status_t make_map(CUtensorMap* map, const void* ptr, int B, int H, long lon
 }
 
 // The fp32 dQ accumulator [B, H, L, d] as a 4-D tensor (d, L, H, B) with boxes
-// of 32 fp32 (128 bytes, swizzled) by 128 rows, the target of the backward's
-// bulk reduce-adds (rows past L are never written).
-attn_status_t make_map_f32(CUtensorMap* map, void* ptr, int B, int H, long long L, int d) {
+// of 32 fp32 (128 bytes, swizzled) by `box_rows` rows, the target of the
+// backward's bulk reduce-adds (rows past L are never written).
+attn_status_t make_map_f32(CUtensorMap* map, void* ptr, int B, int H, long long L, int d,
+                           int box_rows) {
   if (L < 1) L = 1;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
                         static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(L) * d * 4,
                            static_cast<cuuint64_t>(H) * L * d * 4};
-  cuuint32_t box[4] = {32, 128, 1, 1};
+  cuuint32_t box[4] = {32, static_cast<cuuint32_t>(box_rows), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -262,7 +263,7 @@ attn_status_t bwd_common(const void* q, const void* k, const void* v, const void
   if ((s = make_map(&tk, k, B, Hkv, L, d)) != ATTN_OK) return s;
   if ((s = make_map(&tv, v, B, Hkv, L, d)) != ATTN_OK) return s;
   if ((s = make_map(&tdo, dout, B, H, L, d)) != ATTN_OK) return s;
-  if ((s = make_map_f32(&tdq, workspace, B, H, L, d)) != ATTN_OK) return s;
+  if ((s = make_map_f32(&tdq, workspace, B, H, L, d, bwd_dq_box_rows(d))) != ATTN_OK) return s;
   p.B = B;
   p.H = H;
   p.Hkv = Hkv;

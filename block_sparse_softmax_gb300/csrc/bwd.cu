@@ -74,9 +74,15 @@ struct BwdCfg {
   static constexpr int kBarDKVFull = kBarDQFree + 2;
   static constexpr int kBarMmaDone = kBarDKVFull + 1;
   static constexpr int kBarStat = kBarMmaDone + 1;     // [2]: LSE/D of a query tile staged
-  static constexpr int kBarStaged = kBarStat + 2;      // dQ round written to the staging buffer
-  static constexpr int kBarStageFree = kBarStaged + 1; // staging buffer read by the reduce
+  static constexpr int kBarStaged = kBarStat + 2;      // dQ round staged (CTA-wide drain)
+  static constexpr int kBarStageFree = kBarStaged + 1; // staging read by the reduce (CTA-wide drain)
   static constexpr int kNumBars = kBarStageFree + 1;
+  // dQ drain: at d=128 each drain warp reduces its own 32 rows (no barrier
+  // among the four warps, which frees dQ's columns for dP^T sooner); at d=64,
+  // with one round per tile and a shorter period, one thread reduces all 128
+  // rows in two larger boxes after a CTA-wide barrier (measured faster there).
+  static constexpr bool kDrainPerWarp = (D == 128);
+  static constexpr int kDrainBoxRows = kDrainPerWarp ? 32 : 128;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   // Alignment slack for the 1024-byte aligned layout.  At d=128 the layout
   // leaves less than 1024 bytes: the kernel then relies on the dynamic shared
@@ -247,12 +253,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(bar(C::kBarDQFull), 1);
     mbar_init(bar(C::kBarDQFree), 128);
     mbar_init(bar(C::kBarDQFree + 1), 128);
+    mbar_init(bar(C::kBarStaged), 128);
+    mbar_init(bar(C::kBarStageFree), 1);
     mbar_init(bar(C::kBarDKVFull), 1);
     mbar_init(bar(C::kBarMmaDone), 1);
     mbar_init(bar(C::kBarStat + 0), 128);
     mbar_init(bar(C::kBarStat + 1), 128);
-    mbar_init(bar(C::kBarStaged), 128);
-    mbar_init(bar(C::kBarStageFree), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -661,23 +667,26 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     regs_set<BwdRegs<D>::kHigh, BwdRegs<D>::kLaunchRegs>();
     // =================== dQ: warps 12-15, thread = query row ===================
     // Each round moves 64 d-columns of the tile's dQ from TMEM to a
-    // 128-byte-swizzled fp32 staging buffer (two TMA boxes of 32 columns);
-    // one thread then adds the boxes into the fp32 accumulator in global
-    // memory with bulk tensor reduce-adds.  dQ's TMEM columns are handed back
-    // after the last round's reads.  (On the bench shapes, handing them back
-    // before any staging, streaming 16 KB boxes through two slots, or vector
-    // red.global from registers all measured slower: the reduce stream, not
-    // the TMEM hand-back, sets the pace.)
+    // 128-byte-swizzled fp32 staging buffer, from which bulk tensor
+    // reduce-adds (boxes of 32 columns) add it into the fp32 accumulator in
+    // global memory; dQ's TMEM columns of a round are handed back right after
+    // their reads.  Per-warp drain (d=128): each warp reduces its own 32 rows
+    // and reuses its staging rows once its own previous reduces have read them
+    // (bulk groups are per thread).  CTA-wide drain (d=64): one thread reduces
+    // the 128 rows after all four warps have staged them.  (On the bench
+    // shapes, vector red.global from registers, for all of dQ or for one
+    // round, measured slower: the reduce stream sets the pace.)
+    constexpr bool kPerWarp = C::kDrainPerWarp;
     const int wq = warp & 3;
     const int qr = wq * 32 + lane;
     const uint32_t tDQ = tmem + (static_cast<uint32_t>(wq * 32) << 16) + C::kColDQ;
-    const uint32_t stage = sbase + C::kStageOff;
-    uint8_t* stage_ptr = smem + C::kStageOff;
     constexpr int kRounds = D / 64;
-    constexpr int kBoxBytes = kTileM * 32 * 4;    // one TMA box: 128 rows x 32 fp32
-    static_assert(2 * kBoxBytes == C::kStageBytes, "two boxes fill the staging buffer");
+    constexpr int kBoxBytes = kTileM * 32 * 4;    // 128 rows x 32 fp32: one box column
+    static_assert(2 * kBoxBytes == C::kStageBytes, "two box columns fill the staging buffer");
+    const uint32_t stage = sbase + C::kStageOff + (kPerWarp ? wq * 32 * 128 : 0);
+    uint8_t* stage_ptr = smem + C::kStageOff;
     bool ok = true;
-    int g = 0;                                    // global round counter
+    int g = 0;                                    // staged rounds (CTA-wide drain)
     int gq, i;                                    // query head of the group, query tile
     walk.start(gq, i);
     for (int it = 0; i >= 0 && ok; walk.advance(gq, i), ++it) {
@@ -695,9 +704,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(C::kBarDQFree + r));
         if (r == kRounds - 1) BSS_TRACE_EV(p, tr && qr == 0, 3, 3 * it + 1);
-        // The reduce of the previous round must have read the staging buffer
-        // before it is rewritten.
-        if (g > 0) {
+        // the staging rows must have been read by the reduces that used them
+        if constexpr (kPerWarp) {
+          if (lane == 0) bulk_wait_read_all();
+          __syncwarp();
+        } else if (g > 0) {
           if (qr == 0) {
             bulk_wait_read_all();
             mbar_arrive(bar(C::kBarStageFree));
@@ -708,32 +719,42 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           }
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {               // box 0: columns 0..31 of the round
+        for (int u = 0; u < 8; ++u) {               // box column 0: columns 0..31 of the round
           *reinterpret_cast<uint4*>(stage_ptr + qr * 128 + ((u ^ (qr & 7)) * 16)) =
               make_uint4(v0[4 * u], v0[4 * u + 1], v0[4 * u + 2], v0[4 * u + 3]);
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {               // box 1: columns 32..63
+        for (int u = 0; u < 8; ++u) {               // box column 1: columns 32..63
           *reinterpret_cast<uint4*>(stage_ptr + kBoxBytes + qr * 128 + ((u ^ (qr & 7)) * 16)) =
               make_uint4(v1[4 * u], v1[4 * u + 1], v1[4 * u + 2], v1[4 * u + 3]);
         }
         fence_proxy_async_smem();
-        mbar_arrive(bar(C::kBarStaged));
-        if (qr == 0) {
-          if (!wait_bar(bar(C::kBarStaged), g & 1, abort_flag, p.err)) {
-            ok = false;
-            break;
+        if constexpr (kPerWarp) {
+          __syncwarp();
+          if (lane == 0) {
+            const int row = i * kTileM + wq * 32;
+            tma_reduce_add_4d(&tmDQ, stage, 64 * r, row, hq0 + gq, b);
+            tma_reduce_add_4d(&tmDQ, stage + kBoxBytes, 64 * r + 32, row, hq0 + gq, b);
+            bulk_commit_group();
           }
-          const int row = i * kTileM;
-          tma_reduce_add_4d(&tmDQ, stage, 64 * r, row, hq0 + gq, b);
-          tma_reduce_add_4d(&tmDQ, stage + kBoxBytes, 64 * r + 32, row, hq0 + gq, b);
-          bulk_commit_group();
+        } else {
+          mbar_arrive(bar(C::kBarStaged));
+          if (qr == 0) {
+            if (!wait_bar(bar(C::kBarStaged), g & 1, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            const int row = i * kTileM;
+            tma_reduce_add_4d(&tmDQ, stage, 64 * r, row, hq0 + gq, b);
+            tma_reduce_add_4d(&tmDQ, stage + kBoxBytes, 64 * r + 32, row, hq0 + gq, b);
+            bulk_commit_group();
+          }
         }
         __syncwarp();                               // reconverge before the next TMEM load
       }
       BSS_TRACE_EV(p, tr && qr == 0, 3, 3 * it + 2);
     }
-    if (qr == 0) bulk_wait_all();                   // every reduction has landed
+    if (kPerWarp ? lane == 0 : qr == 0) bulk_wait_all();   // every reduction has landed
   }
 
   tc_fence_before();
@@ -861,6 +882,10 @@ __global__ void __launch_bounds__(256) attn_blocklist_columns_kernel(
 }
 
 }  // namespace
+
+int bwd_dq_box_rows(int d) {
+  return d == 128 ? BwdCfg<128>::kDrainBoxRows : BwdCfg<64>::kDrainBoxRows;
+}
 
 cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int n_lists, int n_qblk,
                                      int nnz, int causal, uint32_t* bitmap, int words, int* err,

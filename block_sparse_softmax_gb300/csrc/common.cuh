@@ -218,6 +218,9 @@ cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int
                                      cudaStream_t st);
 cudaError_t launch_watchdog_selftest(unsigned long long cycles, int* err, cudaStream_t st);
 int select_row_entries(int L, int top_r, int local, int causal);
+// Rows of the dQ accumulator's tensor-map box that the backward's drain
+// reduces with one bulk copy at head dimension d.
+int bwd_dq_box_rows(int d);
 cudaError_t launch_select(int d, const void* q, const void* k, int B, int H, int Hkv, int L,
                           int n_lists, int top_r, int local, int causal, float scale, int* row_ptr,
                           int* col_idx, float* qbar, float* kbar, cudaStream_t st);

@@ -20,6 +20,7 @@ data-path collective; weak scaling); time is the max over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -194,6 +195,26 @@ def dist_setup():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def rank_workload(w: Workload, rank: int) -> Workload:
+    """This rank's share of an N-rank job: the same shape with a batch of its
+    own (seed offset by the rank), so that N ranks process N independent
+    batches and no data moves between them (weak scaling)."""
+    return w if rank == 0 else dataclasses.replace(w, seed=w.seed + 1000 * rank)
+
+
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over the ranks of the default process group."""
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job TFLOP/s: the work of every rank over the slowest rank's time."""
+    return world * flops_per_rank / ms_max / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -494,7 +515,7 @@ def run_gpu(args):
     import block_sparse_softmax_gb300 as bss
     bss.library()
     peaks = load_peaks()
-    w = CAUSAL_4K
+    w = rank_workload(CAUSAL_4K, rank)
     step = Step(bss, w, dev)
     # warm-up, then the timed region (device-resident inputs); every row of
     # every step is bracketed by CUDA events on the launching stream
@@ -524,10 +545,7 @@ def run_gpu(args):
     row_avg = {k: statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for ev in events)
                for k in step.flops}
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step = float(t.item())
+        ms_step = max_over_ranks(ms_step, dev)
 
     # end to end through the public API: pinned host inputs in, results out
     names_in = ["q", "k", "v", "do"]
@@ -550,19 +568,18 @@ def run_gpu(args):
 
     ms_e2e = time_loop(e2e_step, max(3, args.steps // 2), 2, sync_all)
     if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+        ms_e2e = max_over_ranks(ms_e2e, dev)
     status = bss.attn_poll_status()
 
     fwd_tf = step.flops["fwd"] / row_avg["fwd"] / 1e9
     bwd_tf = step.flops["bwd"] / row_avg["bwd"] / 1e9
-    value = world * step.total_flops / ms_step / 1e9
+    value = job_throughput(step.total_flops, ms_step, world)
     # dominant kernel: the largest share of the step's time
     dom = max(row_avg, key=row_avg.get)
     dom_tf = step.flops[dom] / row_avg[dom] / 1e9
     traffic, traffic_note = dram_traffic(dom)
-    extra = {} if args.quick else measure_configs(bss, dev, peaks)
+    # the per-workload table is one GPU's measurement: rank 0 alone takes it
+    extra = {} if (args.quick or rank != 0) else measure_configs(bss, dev, peaks)
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -595,7 +612,7 @@ def run_gpu(args):
                      "peak_kind": f"bf16 sustained ({peaks['source']})",
                      "traffic": traffic, "traffic_note": traffic_note},
         "clocks": clock_info,
-        "e2e": {"value": round(world * step.total_flops / ms_e2e / 1e9, 2), "unit": UNIT,
+        "e2e": {"value": round(job_throughput(step.total_flops, ms_e2e, world), 2), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(ms_e2e, 4)},
         "gpu_launches": step.launches_per_step * args.steps,

@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const int lane = static_cast<int>(lane_id());
   const int tid = static_cast<int>(threadIdx.x);
   const bool tr = BSS_TRACE_ON(p, blockIdx.x);
+  BSS_TRACE_EV(p, tr && tid == 0, 5, 0);             // kernel entry
   (void)tr;
   if (*reinterpret_cast<volatile int*>(p.err) == ATTN_ERR_TIMEOUT) return;
 
@@ -261,6 +262,12 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     mbar_init(bar(C::kBarStat + 1), 128);
     *abort_flag = 0;
     fence_barrier_init();
+    // K_j and V_j go out at once: their load overlaps the rest of the set-up
+    mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTileBytes);
+    for (int c = 0; c < C::kChunks; ++c) {
+      tma_load_4d(sbase + C::kKOff + c * C::kChunkBytes, &tmK, bar(C::kBarKV), c * 64, j * kTileN, h, b);
+      tma_load_4d(sbase + C::kVOff + c * C::kChunkBytes, &tmV, bar(C::kBarKV), c * 64, j * kTileN, h, b);
+    }
   }
   if (warp == 0) {
     tmem_alloc(sbase + C::kMiscOff, C::kTmemCols);
@@ -270,6 +277,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  BSS_TRACE_EV(p, tr && tid == 0, 5, 1);             // set-up done
 
   if (warp < 4) {
   regs_set<BwdRegs<D>::kLow, BwdRegs<D>::kLaunchRegs>();
@@ -278,11 +286,6 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmDO);
-      mbar_arrive_expect_tx(bar(C::kBarKV), 2 * C::kTileBytes);
-      for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_4d(sbase + C::kKOff + c * C::kChunkBytes, &tmK, bar(C::kBarKV), c * 64, j * kTileN, h, b);
-        tma_load_4d(sbase + C::kVOff + c * C::kChunkBytes, &tmV, bar(C::kBarKV), c * 64, j * kTileN, h, b);
-      }
       int nq_ld = 0, ndo_ld = 0;
       int g, i;
       walk.start(g, i);
@@ -385,6 +388,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         return true;
       };
       bool ok = wait_bar(bar(C::kBarKV), 0, abort_flag, p.err);
+      BSS_TRACE_EV(p, tr, 5, 2);                       // K and V landed
       if (ok && n_it > 0) ok = issue_s(0) && issue_dp(0);
       int g, i;
       walk.start(g, i);
@@ -635,32 +639,37 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     // ---- epilogue: half 0 stores dK rows, half 1 stores dV rows ----
     if (ok) ok = wait_bar(bar(C::kBarDKVFull), 0, abort_flag, p.err);
+    BSS_TRACE_EV(p, tr && kr == 0 && X == 0, 5, 3);   // dK and dV complete
     tc_fence_after();
+    ok = __all_sync(0xFFFFFFFFu, ok);
     if (ok) {
-      const size_t row_g = static_cast<size_t>(bh) * L + (key < L ? key : 0);
+      // one 128-byte line (64 columns as bf16 pairs) of this thread's key row
+      // at a time; after the octet transpose every store writes whole lines
       const uint32_t tsrc = tmem + lane_base + (X == 0 ? C::kColDK : C::kColDV);
-      __nv_bfloat16* dst = (X == 0 ? p.dk : p.dv) + row_g * D;
+      const int wrow0 = j * kTileN + wq * 32;          // this warp's first key row
+      const uint32_t valid = __ballot_sync(0xFFFFFFFFu, key < L);
+      uint8_t* base = reinterpret_cast<uint8_t*>((X == 0 ? p.dk : p.dv) +
+                                                 (static_cast<size_t>(bh) * L + wrow0) * D);
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
+      for (int g2 = 0; g2 < D / 64; ++g2) {
+        uint32_t a[32], c[32];
         if (n_it > 0) {
-          tmem_ld32(tsrc + c * 32, o);
-          tmem_ld_wait(o);
+          tmem_ld32(tsrc + g2 * 64, a);
+          tmem_ld32(tsrc + g2 * 64 + 32, c);
+          tmem_ld_wait(a);
+          tmem_ld_wait(c);
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
+          for (int e = 0; e < 32; ++e) a[e] = c[e] = 0u;
         }
-        if (key < L) {
+        uint32_t w[32];
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(o[e + 0]), __uint_as_float(o[e + 1]));
-            w.y = pack_bf16(__uint_as_float(o[e + 2]), __uint_as_float(o[e + 3]));
-            w.z = pack_bf16(__uint_as_float(o[e + 4]), __uint_as_float(o[e + 5]));
-            w.w = pack_bf16(__uint_as_float(o[e + 6]), __uint_as_float(o[e + 7]));
-            *reinterpret_cast<uint4*>(dst + c * 32 + e) = w;
-          }
+        for (int k = 0; k < 16; ++k) {
+          w[k] = pack_bf16(__uint_as_float(a[2 * k]), __uint_as_float(a[2 * k + 1]));
+          w[16 + k] = pack_bf16(__uint_as_float(c[2 * k]), __uint_as_float(c[2 * k + 1]));
         }
+        transpose_octets(w, lane);
+        store_octet_lines(w, base + g2 * 128, D * 2, valid, lane);
       }
     }
   } else {
@@ -759,6 +768,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  BSS_TRACE_EV(p, tr && tid == 0, 5, 4);             // every role done
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();

@@ -797,6 +797,14 @@ def run_profile_case(kind: str):
     import block_sparse_softmax_gb300 as bss
     bss.library()
     dev = torch.device("cuda", 0)
+    if kind == "select":
+        # the selector on the block-sparse workload: one list per head,
+        # 4 local blocks + the 4 best-scoring earlier blocks per query block
+        w = SPARSE_16K
+        x = {k: t.to(dev) for k, t in make_inputs(w).items()}
+        fn = lambda: bss.attn_select_blocks(x["q"], x["k"], 4, local_blocks=4, causal=True,
+                                            n_lists=w.B * w.H, scale=w.scale)
+        return _run_profile_fn(kind, fn)
     w = CAUSAL_16K if kind == "fwd16k" else CAUSAL_4K
     w = Workload(w.name, w.B, w.H, w.L, w.d, True, w.seed, backward=True)
     x = {k: t.to(dev) for k, t in make_inputs(w).items()}
@@ -811,6 +819,11 @@ def run_profile_case(kind: str):
         o, lse = bss.attn_fwd(x["q"], x["k"], x["v"], causal=True, scale=w.scale)
         fn = lambda: bss.attn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], causal=True,
                                   scale=w.scale)
+    elif kind == "splitkv":
+        ws = torch.empty(bss.attn_fwd_splitkv_workspace_bytes(w.B, w.H, w.L, w.L, w.d, 8),
+                         device=dev, dtype=torch.uint8)
+        fn = lambda: bss.attn_fwd_splitkv(x["q"], x["k"], x["v"], 8, causal=True,
+                                          scale=w.scale, workspace=ws)
     elif kind in ("partial", "merge"):
         bounds = chunk_bounds(w.L, 8)
         kc = [x["k"][:, :, s:e].contiguous() for s, e in bounds]
@@ -831,6 +844,11 @@ def run_profile_case(kind: str):
             fn = lambda: bss.attn_merge_states(m, l_, acc)
     else:
         raise SystemExit(f"unknown profile case {kind}")
+    _run_profile_fn(kind, fn)
+
+
+def _run_profile_fn(kind: str, fn):
+    import block_sparse_softmax_gb300 as bss
     for _ in range(2):
         fn()
     torch.cuda.synchronize()
@@ -842,7 +860,8 @@ def run_profile_case(kind: str):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["fwd", "fwd16k", "sparse", "bwd", "partial", "merge"],
+    ap.add_argument("--profile", choices=["fwd", "fwd16k", "sparse", "bwd", "partial", "merge",
+                                            "splitkv", "select"],
                     default=None,
                     help="run one small case of one kernel (for ncu) and exit")
     ap.add_argument("--gpus", type=int, default=1)

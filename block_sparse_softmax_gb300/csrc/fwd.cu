@@ -27,6 +27,10 @@
 //   * the two tiles alternate on the tensor core (P V of tile 0, S of tile 0's
 //     next block, P V of tile 1, S of tile 1's next block), so one warpgroup's
 //     exponentials overlap the other tile's MMAs;
+//   * a pair with a single query tile (short query blocks: decoding, a ragged
+//     last pair) puts the same rows in both slots and deals the key blocks to
+//     them in turn, then merges the two states per row in the epilogue, so the
+//     overlap above is kept;
 //   * exponentials are base 2 with scale*log2(e) folded in; the running max is
 //     only moved (and O rescaled in TMEM) when it grows by more than 2^8, which
 //     keeps the result exact because l and A always share the same reference m;
@@ -67,7 +71,9 @@ struct FwdCfg {
   static constexpr int kBarItemEmpty = kBarItemFull + 2;
   static constexpr int kBarClc = kBarItemEmpty + 2;
   static constexpr int kBarMmaDone = kBarClc + 1;
-  static constexpr int kNumBars = kBarMmaDone + 1;
+  static constexpr int kBarXFull = kBarMmaDone + 1;    // tile 1's row state handed over
+  static constexpr int kBarXEmpty = kBarXFull + 1;     // ... and read by tile 0
+  static constexpr int kNumBars = kBarXEmpty + 1;
   // 16-byte aligned: cancel answer (16) | TMEM base | abort flag | next item [2]
   static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;
   static constexpr int kClcOff = kMiscOff;
@@ -76,7 +82,13 @@ struct FwdCfg {
   static constexpr int kNextItemOff = kMiscOff + 24;
   static constexpr int kBitmapWords = kMaxKBlocks / 32;
   static constexpr int kBitmapOff = kMiscOff + 32;
-  static constexpr int kSmemBytes = kBitmapOff + 2 * kBitmapWords * 4 + 1024;
+  // A dense launch has no bitmaps; the same bytes carry the (m, mt, l) rows
+  // one softmax warpgroup hands to the other (three arrays of 128 floats).
+  static constexpr int kXchOff = kBitmapOff;
+  static constexpr int kXchBytes = 3 * kTileM * 4;
+  static constexpr int kBitmapRegion =
+      2 * kBitmapWords * 4 > kXchBytes ? 2 * kBitmapWords * 4 : kXchBytes;
+  static constexpr int kSmemBytes = kBitmapOff + kBitmapRegion + 1024;
   static_assert(kSmemBytes <= 232448, "forward shared memory exceeds the 227 KB a CTA may use");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;                      // S_t at t*128
@@ -118,12 +130,20 @@ struct FwdItem {
   long long koff;  // absolute position of the chunk's first key (causal mask)
   int r0[2];       // first query row of each tile
   int kbmax[2];    // last key block (of the chunk) each tile can see (-1: none)
+  // Alternating item: the pair has a single query tile (its second tile lies
+  // past the last row) and a dense key range of at least two blocks.  Both
+  // tile slots then hold the SAME query rows and take the key blocks in turn
+  // (slot 0 the even blocks, slot 1 the odd ones), so that one slot's softmax
+  // overlaps the other slot's MMAs as in a full pair; the two partial states
+  // of each row are merged in the epilogue.  Short query blocks (decoding)
+  // are all of this kind.
+  bool alt;
 };
 
 // Items are numbered row-pair-major, then key chunk, then head: under a
 // causal mask the last pair (whose rows see the most keys) comes first, and
 // the heads of one pair and chunk sit side by side.
-template <bool CAUSAL>
+template <bool CAUSAL, bool ALT>
 __device__ __forceinline__ FwdItem fwd_item(int item, const FwdParams& p) {
   FwdItem it;
   const int BH = p.B * p.H;
@@ -154,6 +174,11 @@ __device__ __forceinline__ FwdItem fwd_item(int item, const FwdParams& p) {
       it.kbmax[t] = nk - 1;
     }
   }
+  it.alt = ALT && it.r0[1] >= p.Lq && it.kbmax[0] >= 1;
+  if (it.alt) {
+    it.r0[1] = it.r0[0];
+    it.kbmax[1] = it.kbmax[0];
+  }
   return it;
 }
 
@@ -163,12 +188,14 @@ struct Schedule {
   int kbmax0, kbmax1;          // last block a tile can see (-1: none)
   const uint32_t* bm0;         // block-sparse bitmaps (nullptr: dense prefix)
   const uint32_t* bm1;
+  bool alt;                    // alternating item: block kb belongs to slot kb & 1
 
   __device__ __forceinline__ Schedule(const FwdItem& it, const uint32_t* bitmap, int words)
       : kbmax0(it.kbmax[0]), kbmax1(it.kbmax[1]), bm0(bitmap),
-        bm1(bitmap ? bitmap + words : nullptr) {}
+        bm1(bitmap ? bitmap + words : nullptr), alt(it.alt) {}
 
   __device__ __forceinline__ int member(int kb) const {
+    if (alt) return kb <= kbmax0 ? 1 << (kb & 1) : 0;
     int m = 0;
     if (kb <= kbmax0 && (bm0 == nullptr || ((bm0[kb >> 5] >> (kb & 31)) & 1u))) m |= 1;
     if (kb <= kbmax1 && (bm1 == nullptr || ((bm1[kb >> 5] >> (kb & 31)) & 1u))) m |= 2;
@@ -194,6 +221,7 @@ struct Schedule {
   }
   // The last block tile t computes (-1: none).
   __device__ __forceinline__ int last(int t) const {
+    if (alt) return ((kbmax0 & 1) == t) ? kbmax0 : kbmax0 - 1;
     const int lim = t ? kbmax1 : kbmax0;
     const uint32_t* bm = t ? bm1 : bm0;
     if (bm == nullptr || lim < 0) return lim;
@@ -216,11 +244,12 @@ struct Schedule {
 // mask).  The producer passes each next item index to the other roles through
 // a two-slot ring in shared memory.  A block-sparse launch runs one item per
 // CTA (its bitmaps are built per item at set-up).
-template <int D, bool CAUSAL, bool SPARSE, bool PARTIAL>
+template <int D, bool CAUSAL, bool SPARSE, bool PARTIAL, bool ALT>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
+  constexpr bool kAlt = ALT && !SPARSE;   // single-tile pairs may alternate
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -264,6 +293,8 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(bar(C::kBarClc), 1);
     mbar_init(bar(C::kBarMmaDone), 1);
+    mbar_init(bar(C::kBarXFull), 4 * 32);
+    mbar_init(bar(C::kBarXEmpty), 4 * 32);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -273,7 +304,7 @@ __global__ void __launch_bounds__(384, 1)
   }
   BSS_TRACE_EV(p, tr && tid == 0, 6, 0);
   if (SPARSE) {
-    const FwdItem it0 = fwd_item<CAUSAL>(blockIdx.x, p);
+    const FwdItem it0 = fwd_item<CAUSAL, kAlt>(blockIdx.x, p);
     const int nk = (p.Lk + kTileN - 1) / kTileN;
     for (int i = tid; i < 2 * C::kBitmapWords; i += C::kThreads) bitmap[i] = 0u;
     __syncthreads();
@@ -326,7 +357,7 @@ __global__ void __launch_bounds__(384, 1)
         clc_out = true;
       };
       while (ok) {
-        const FwdItem it = fwd_item<CAUSAL>(item, p);
+        const FwdItem it = fwd_item<CAUSAL, kAlt>(item, p);
         const Schedule sch(it, sched_bm, C::kBitmapWords);
         bool qloaded[2] = {false, false};
         for (int kb = sch.next(-1); kb >= 0;) {
@@ -440,7 +471,7 @@ __global__ void __launch_bounds__(384, 1)
       int on[2] = {0, 0};       // O accumulations handed to the epilogue per tile
       bool ok = true;
       while (ok) {
-        const FwdItem it = fwd_item<CAUSAL>(item, p);
+        const FwdItem it = fwd_item<CAUSAL, kAlt>(item, p);
         const Schedule sch(it, sched_bm, C::kBitmapWords);
         const int lastkb[2] = {sch.last(0), sch.last(1)};
         bool qready[2] = {false, false};
@@ -481,6 +512,37 @@ __global__ void __launch_bounds__(384, 1)
           return true;
         };
 
+        if (kAlt && it.alt) {
+          // Each key block serves one slot (kb & 1): S0(0) S1(1), then for
+          // every block its slot's P V followed by that slot's S two blocks on.
+          const int nb = it.kbmax[0] + 1;
+          auto alt_qk = [&](const int t, int kb) -> bool {
+            const int j = i + kb;
+            const int sk = j % C::kStagesK;
+            if (!wait_bar(bar(C::kBarKFull + sk), (j / C::kStagesK) & 1, abort_flag, p.err)) return false;
+            tc_fence_after();
+            if (!issue_qk(t, sk, kb)) return false;
+            mma_commit(bar(C::kBarKEmpty + sk));
+            return true;
+          };
+          auto alt_step = [&](const int t, int kb) -> bool {
+            const int j = i + kb;
+            const int sv = j % C::kStagesV;
+            if (!wait_bar(bar(C::kBarVFull + sv), (j / C::kStagesV) & 1, abort_flag, p.err)) return false;
+            if (!wait_bar(bar(C::kBarPFull + t), pcount[t] & 1, abort_flag, p.err)) return false;
+            ++pcount[t];
+            tc_fence_after();
+            if (!issue_pv(t, sv)) return false;
+            mma_commit(bar(C::kBarVEmpty + sv));
+            return kb + 2 < nb ? alt_qk(t, kb + 2) : true;
+          };
+          ok = alt_qk(0, 0) && alt_qk(1, 1);
+          for (int kb = 0; kb < nb && ok; kb += 2) {
+            ok = alt_step(0, kb);
+            if (ok && kb + 1 < nb) ok = alt_step(1, kb + 1);
+          }
+          i += nb;
+        } else {
         int kb = sch.next(-1);
         int mask = kb >= 0 ? sch.member(kb) : 0;
         if (kb >= 0) {
@@ -535,6 +597,7 @@ __global__ void __launch_bounds__(384, 1)
           mask = nmask;
           ++i;
         }
+        }
         if (!ok) break;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -572,13 +635,16 @@ __global__ void __launch_bounds__(384, 1)
     const bool trw = tr && lane == 0 && wq == 0;
     (void)trw;
 
+    float* xch = reinterpret_cast<float*>(smem + C::kXchOff);
+
     int item = static_cast<int>(blockIdx.x);
     int n = 0;          // items finished
     int cnt = 0;        // S tiles consumed (over all items)
-    int on = 0;         // O accumulations read back
+    int on0 = 0, on1 = 0;  // O accumulations completed per slot (both warpgroups count both)
+    int nx = 0;         // row states handed over (alternating items)
     bool ok = true;
     while (ok) {
-      const FwdItem it = fwd_item<CAUSAL>(item, p);
+      const FwdItem it = fwd_item<CAUSAL, kAlt>(item, p);
       const Schedule sch(it, sched_bm, C::kBitmapWords);
       const int r0 = t ? it.r0[1] : it.r0[0];
       const int row = r0 + row_in_tile;
@@ -690,11 +756,68 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
 
+      if (kAlt && it.alt && t == 1) {
+        // Alternating item: this row's state over the odd key blocks goes to
+        // tile 0's warpgroup, which merges it with the even blocks' state (and
+        // reads O_1 from tensor memory) and writes the row.
+        if (nx > 0 &&
+            !__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarXEmpty), (nx - 1) & 1, abort_flag, p.err)))
+          break;
+        xch[row_in_tile] = m2;
+        xch[kTileM + row_in_tile] = mt;
+        xch[2 * kTileM + row_in_tile] = l;
+        mbar_arrive(bar(C::kBarXFull));
+        ++nx;
+      } else {
       // ---- epilogue: O_t is read out of TMEM at once and released to the
       // next item's P V before the global stores ----
       uint32_t o[D / 32][32];
+      if (kAlt && it.alt) {
+        // merge the two slots' states of this row: both are (m, l, A) over
+        // disjoint key blocks, rescaled to the larger reference max; the
+        // merged A goes back into O_0, which the epilogue below reads
+        if (!__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarXFull), nx & 1, abort_flag, p.err))) break;
+        const float m2b = xch[row_in_tile];
+        const float mtb = xch[kTileM + row_in_tile];
+        const float lb = xch[2 * kTileM + row_in_tile];
+        mbar_arrive(bar(C::kBarXEmpty));
+        ++nx;
+        const float mm = fmaxf(m2, m2b);
+        const float a0 = (m2 == NEG_INF) ? 0.f : ex2(m2 - mm);
+        const float a1 = (m2b == NEG_INF) ? 0.f : ex2(m2b - mm);
+        m2 = mm;
+        mt = fmaxf(mt, mtb);
+        l = l * a0 + lb * a1;
+        if (!__all_sync(0xFFFFFFFFu,
+                        wait_bar(bar(C::kBarOFull + 0), on0 & 1, abort_flag, p.err) &&
+                            wait_bar(bar(C::kBarOFull + 1), on1 & 1, abort_flag, p.err)))
+          break;
+        tc_fence_after();
+        const uint32_t tO1 = tmem + lane_base + C::kColO + D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t x[32], y[32];
+          tmem_ld32(tO + c * 32, x);
+          tmem_ld32(tO1 + c * 32, y);
+          tmem_ld_wait(x);
+          tmem_ld_wait(y);
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            float x0, x1;
+            fmul2(x0, x1, __uint_as_float(x[j]), __uint_as_float(x[j + 1]), a0, a0);
+            ffma2(x0, x1, __uint_as_float(y[j]), __uint_as_float(y[j + 1]), a1, a1, x0, x1);
+            x[j] = __float_as_uint(x0);
+            x[j + 1] = __float_as_uint(x1);
+          }
+          tmem_st32(tO + c * 32, x);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(C::kBarOEmpty + 1));
+      }
       if (ci > 0) {
-        if (!__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarOFull + t), on & 1, abort_flag, p.err))) break;
+        if (!__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarOFull + t), (t ? on1 : on0) & 1, abort_flag, p.err)))
+          break;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + c * 32, o[c]);
@@ -702,7 +825,6 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < D / 32; ++c) tmem_ld_wait(o[c]);
         tc_fence_before();
         mbar_arrive(bar(C::kBarOEmpty + t));
-        ++on;
       } else {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c)
@@ -754,6 +876,9 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (inb) p.lse[row_g] = l > 0.f ? (m2 + __log2f(l)) * kLn2 : NEG_INF;
       }
+      }
+      on0 += sch.last(0) >= 0 ? 1 : 0;
+      on1 += sch.last(1) >= 0 ? 1 : 0;
       BSS_TRACE_EV(p, trw, 4 + t, 2 * n + 1);
       // ---- next item ----
       const int s = n & 1;
@@ -777,11 +902,11 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool SPARSE, bool PARTIAL>
+template <int D, bool CAUSAL, bool SPARSE, bool PARTIAL, bool ALT>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<D>;
-  auto kern = attn_fwd_kernel<D, CAUSAL, SPARSE, PARTIAL>;
+  auto kern = attn_fwd_kernel<D, CAUSAL, SPARSE, PARTIAL, ALT>;
   constexpr int kMaxDev = 64;
   static bool configured[kMaxDev] = {};  // the attribute is per device and function
   int dev = 0;
@@ -805,21 +930,30 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                        cudaStream_t st) {
-#define BSS_FWD_CASE(DD, CA, SP, PA)                                   \
-  if (d == DD && causal == CA && sparse == SP && partial == PA)        \
-    return launch_one<DD, CA, SP, PA>(tq, tk, tv, p, st);
-  BSS_FWD_CASE(64, false, false, false)
-  BSS_FWD_CASE(64, true, false, false)
-  BSS_FWD_CASE(128, false, false, false)
-  BSS_FWD_CASE(128, true, false, false)
-  BSS_FWD_CASE(64, false, false, true)
-  BSS_FWD_CASE(64, true, false, true)
-  BSS_FWD_CASE(128, false, false, true)
-  BSS_FWD_CASE(128, true, false, true)
-  BSS_FWD_CASE(64, false, true, false)
-  BSS_FWD_CASE(64, true, true, false)
-  BSS_FWD_CASE(128, false, true, false)
-  BSS_FWD_CASE(128, true, true, false)
+  // The alternating schedule of single-tile pairs is compiled into every dense
+  // kernel without a partial output; the partial-state kernels have a second
+  // instantiation without it, which launches with full pairs only run.
+  const bool single_tile_pair = (p.Lq % (2 * kTileM)) != 0 && (p.Lq % (2 * kTileM)) <= kTileM;
+  const bool alt = !sparse && (!partial || single_tile_pair);
+#define BSS_FWD_CASE(DD, CA, SP, PA, AL)                                         \
+  if (d == DD && causal == CA && sparse == SP && partial == PA && alt == AL)     \
+    return launch_one<DD, CA, SP, PA, AL>(tq, tk, tv, p, st);
+  BSS_FWD_CASE(64, false, false, false, true)
+  BSS_FWD_CASE(64, true, false, false, true)
+  BSS_FWD_CASE(128, false, false, false, true)
+  BSS_FWD_CASE(128, true, false, false, true)
+  BSS_FWD_CASE(64, false, false, true, true)
+  BSS_FWD_CASE(64, true, false, true, true)
+  BSS_FWD_CASE(128, false, false, true, true)
+  BSS_FWD_CASE(128, true, false, true, true)
+  BSS_FWD_CASE(64, false, false, true, false)
+  BSS_FWD_CASE(64, true, false, true, false)
+  BSS_FWD_CASE(128, false, false, true, false)
+  BSS_FWD_CASE(128, true, false, true, false)
+  BSS_FWD_CASE(64, false, true, false, false)
+  BSS_FWD_CASE(64, true, true, false, false)
+  BSS_FWD_CASE(128, false, true, false, false)
+  BSS_FWD_CASE(128, true, true, false, false)
 #undef BSS_FWD_CASE
   return cudaErrorInvalidValue;
 }

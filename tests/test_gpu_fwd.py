@@ -62,6 +62,63 @@ def test_causal_offsets_nonsquare(bss, d, Lq, Lk, q0, k0):
     compare_forward(o, lse, O_ref, l_ref, f"Lq={Lq} Lk={Lk} q0={q0} k0={k0}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Lq,Lk,q0,causal", [
+    (100, 300, 100, True),    # rows 100-127 see block 0 only: the odd-block state is empty
+    (128, 640, 0, False),     # five key blocks: the even slot takes one more
+    (64, 512, 448, True),     # four key blocks, every row sees all of them
+    (40, 256, 0, False),      # exactly two key blocks
+    (1, 1000, 999, True),     # one query row
+    (300, 700, 400, True),    # a full pair, then a single-tile pair
+])
+def test_single_tile_pairs(bss, d, Lq, Lk, q0, causal):
+    """A pair whose second query tile lies past the last row takes its key blocks
+    in turn in both tile slots and merges the two states per row; the result is
+    the same attention."""
+    g = torch.Generator().manual_seed(Lq * 11 + Lk + d)
+    q = torch.randn(2, 2, Lq, d, generator=g).bfloat16()
+    k = torch.randn(2, 2, Lk, d, generator=g).bfloat16()
+    v = torch.randn(2, 2, Lk, d, generator=g).bfloat16()
+    scale = d ** -0.5
+    o = torch.full((2, 2, Lq, d), float("nan"), device="cuda").bfloat16()
+    lse = torch.full((2, 2, Lq), float("nan"), device="cuda")
+    bss.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale, q_offset=q0, out=o,
+                 lse=lse)
+    torch.cuda.synchronize()
+    O_ref, l_ref = oracle.attention_forward(to_f64(q), to_f64(k), to_f64(v), scale,
+                                            causal=causal, q_offset=q0)
+    compare_forward(o, lse, O_ref, l_ref, f"Lq={Lq} Lk={Lk} q0={q0} causal={causal}")
+    assert bss.attn_poll_status() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_single_tile_pair_partial_state(bss, d):
+    """The partial state (m, l, acc) of a single-tile pair, where some rows'
+    keys all fall in the even blocks, against the oracle's state."""
+    Lq, Lk, q0 = 100, 300, 100
+    g = torch.Generator().manual_seed(d)
+    q = torch.randn(1, 2, Lq, d, generator=g).bfloat16()
+    k = torch.randn(1, 2, Lk, d, generator=g).bfloat16()
+    v = torch.randn(1, 2, Lk, d, generator=g).bfloat16()
+    scale = d ** -0.5
+    m, l, acc = bss.attn_fwd_partial(q.cuda(), k.cuda(), v.cuda(), causal=True, scale=scale,
+                                     q_offset=q0)
+    torch.cuda.synchronize()
+    for h in range(2):
+        M = oracle.allowed_rows(np.arange(Lq) + q0, Lk, causal=True)
+        mr, lr, Ar = oracle.partial_state(to_f64(q)[0, h], to_f64(k)[0, h], to_f64(v)[0, h],
+                                          scale, M)
+        mg = m[0, h].double().cpu().numpy()
+        lg = l[0, h].double().cpu().numpy()
+        Ag = acc[0, h].double().cpu().numpy()
+        assert not np.any(np.isneginf(mr)) and not np.any(np.isneginf(mg))
+        assert np.abs(mg - mr).max() <= TOL_LSE
+        assert np.abs((Ag / lg[:, None]) - (Ar / lr[:, None])).max() <= TOL_O
+        assert np.abs((mg + np.log(lg)) - (mr + np.log(lr))).max() <= TOL_LSE
+        assert lg.min() >= 1.0 - 1e-3      # the max element contributes e^0 = 1
+    assert bss.attn_poll_status() == 0
+
+
 def test_empty_key_set_gives_empty_rows(bss):
     q = torch.randn(1, 1, 100, 64).bfloat16().cuda()
     k = torch.randn(1, 1, 64, 64).bfloat16().cuda()

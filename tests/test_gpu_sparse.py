@@ -7,7 +7,8 @@ import pytest
 import torch
 
 import oracle
-from tests.parity import compare_forward, oracle_forward, tile_edge_rows, to_cuda
+from tests.parity import (TOL_LSE, TOL_O, compare_forward, oracle_forward, tile_edge_rows,
+                          to_cuda)
 from workloads import (SPARSE_16K, Workload, local_global_random_blocklist, make_inputs,
                        random_blocklist)
 
@@ -78,8 +79,13 @@ def test_order_and_duplicates_are_bit_identical(bss):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_all_blocks_listed_equals_dense_kernel(bss, causal):
-    L, d = 777, 64
+@pytest.mark.parametrize("L", [700, 777])
+def test_all_blocks_listed_equals_dense_kernel(bss, causal, L):
+    """Where a pair of query tiles is full, both kernels visit the same blocks in
+    the same order and agree bit for bit.  A last pair with a single tile (rows
+    768-776 at L=777) is split over both tile slots by the dense kernel, which
+    sums its blocks in another order: those rows agree within the tolerance."""
+    d = 64
     n = (L + 127) // 128
     if causal:
         rows = [list(range(a + 1)) for a in range(n)]
@@ -91,7 +97,12 @@ def test_all_blocks_listed_equals_dense_kernel(bss, causal):
     o_s, l_s = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=causal)
     o_d, l_d = bss.attn_fwd(inp["q"], inp["k"], inp["v"], causal=causal)
     torch.cuda.synchronize()
-    assert torch.equal(o_s, o_d) and torch.equal(l_s, l_d)
+    full = (L // 256) * 256 if 0 < L % 256 <= 128 else L    # rows in full pairs
+    assert torch.equal(o_s[:, :, :full], o_d[:, :, :full])
+    assert torch.equal(l_s[:, :, :full], l_d[:, :, :full])
+    if full < L:
+        assert (o_s[:, :, full:].float() - o_d[:, :, full:].float()).abs().max().item() <= TOL_O
+        assert (l_s[:, :, full:] - l_d[:, :, full:]).abs().max().item() <= TOL_LSE
 
 
 def test_future_blocks_contribute_nothing(bss):

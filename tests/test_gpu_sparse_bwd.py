@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from tests.parity import TOL_GRAD, to_cuda
+from tests.parity import TOL_GRAD, TOL_LSE, TOL_O, to_cuda
 from workloads import (SPARSE_16K, Workload, local_global_random_blocklist, make_inputs,
                        random_blocklist, to_f64)
 
@@ -100,8 +100,11 @@ def test_unlisted_key_blocks_get_zero_gradients(bss):
 
 def test_every_block_listed_equals_dense_backward(bss):
     """With every block listed the sparse walk visits the dense causal tiles in
-    the same order: dK, dV and D are identical to attn_bwd's; dQ (added in by
-    reduce operations whose order is not fixed) agrees within the tolerance."""
+    the same order: given the same O and LSE, dK, dV and D are identical to
+    attn_bwd's; dQ (added in by reduce operations whose order is not fixed)
+    agrees within the tolerance.  The forwards agree bit for bit on rows in full
+    pairs of query tiles; the last pair here (rows 1024-1099) has a single tile,
+    whose blocks the dense forward sums in another order."""
     L, d = 1100, 128
     n = (L + 127) // 128
     rp = (np.arange(n + 1) * n).astype(np.int32)
@@ -110,10 +113,13 @@ def test_every_block_listed_equals_dense_backward(bss):
     inp = to_cuda(make_inputs(w))
     o, lse, dq, dk, dv, delta = _fwd_bwd(bss, inp, rp, ci, True, w.scale)
     o2, lse2 = bss.attn_fwd(inp["q"], inp["k"], inp["v"], causal=True, scale=w.scale)
-    ref = bss.attn_bwd(inp["q"], inp["k"], inp["v"], o2, lse2, inp["do"], causal=True,
+    ref = bss.attn_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], causal=True,
                        scale=w.scale)
     torch.cuda.synchronize()
-    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    full = 1024
+    assert torch.equal(o[:, :, :full], o2[:, :, :full]) and torch.equal(lse[..., :full], lse2[..., :full])
+    assert (o.float() - o2.float()).abs().max().item() <= TOL_O
+    assert (lse - lse2).abs().max().item() <= TOL_LSE
     assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2]) and torch.equal(delta, ref[3])
     assert (dq.float() - ref[0].float()).abs().max().item() <= TOL_GRAD
 

@@ -44,15 +44,20 @@
 namespace bss {
 namespace {
 
-template <int D>
+// DEC: every query block is a single tile (Lq <= 128, decoding).  Both tile
+// slots then compute on the same query rows, so one Q buffer serves both and
+// the second becomes one more K stage (deeper key prefetch for a stream that
+// is bound by memory latency rather than by the tensor core).
+template <int D, bool DEC = false>
 struct FwdCfg {
   static constexpr int kChunks = D / 64;                   // 128-byte swizzle atoms across d
   static constexpr int kChunkBytes = kTileM * 128;         // 128 rows x 128 bytes
   static constexpr int kTileBytes = kTileM * D * 2;
-  static constexpr int kStagesK = (D == 128) ? 2 : 4;
+  static constexpr int kQSlots = DEC ? 1 : 2;
+  static constexpr int kStagesK = ((D == 128) ? 2 : 4) + (DEC ? 1 : 0);
   static constexpr int kStagesV = (D == 128) ? 3 : 4;   // V is consumed last: deeper prefetch
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQOff + 2 * kTileBytes;
+  static constexpr int kKOff = kQOff + kQSlots * kTileBytes;
   static constexpr int kVOff = kKOff + kStagesK * kTileBytes;
   static constexpr int kBarOff = kVOff + kStagesV * kTileBytes;
   // q_full[2] q_empty[2] k_full[SK] k_empty[SK] v_full[SV] v_empty[SV] s_full[2]
@@ -244,12 +249,13 @@ struct Schedule {
 // mask).  The producer passes each next item index to the other roles through
 // a two-slot ring in shared memory.  A block-sparse launch runs one item per
 // CTA (its bitmaps are built per item at set-up).
-template <int D, bool CAUSAL, bool SPARSE, bool PARTIAL, bool ALT>
+template <int D, bool CAUSAL, bool SPARSE, bool PARTIAL, bool ALT, bool DEC>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = FwdCfg<D>;
   constexpr bool kAlt = ALT && !SPARSE;   // single-tile pairs may alternate
+  constexpr bool kDec = DEC && kAlt;      // one Q buffer for both slots
+  using C = FwdCfg<D, kDec>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -367,20 +373,21 @@ __global__ void __launch_bounds__(384, 1)
           const int mask = sch.member(kb);
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (((mask >> t) & 1) && !qloaded[t] && ok) {
-              if (qn[t] > 0 &&
-                  !wait_bar(bar(C::kBarQEmpty + t), (qn[t] - 1) & 1, abort_flag, p.err)) {
+            const int q = kDec ? 0 : t;   // the Q buffer tile slot t reads
+            if (((mask >> t) & 1) && !qloaded[q] && ok) {
+              if (qn[q] > 0 &&
+                  !wait_bar(bar(C::kBarQEmpty + q), (qn[q] - 1) & 1, abort_flag, p.err)) {
                 ok = false;
                 break;
               }
-              const uint32_t qs = sbase + C::kQOff + t * C::kTileBytes;
-              mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
+              const uint32_t qs = sbase + C::kQOff + q * C::kTileBytes;
+              mbar_arrive_expect_tx(bar(C::kBarQFull + q), C::kTileBytes);
 #pragma unroll
               for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(qs + c * C::kChunkBytes, &tmQ, bar(C::kBarQFull + t), c * 64, it.r0[t],
+                tma_load_4d(qs + c * C::kChunkBytes, &tmQ, bar(C::kBarQFull + q), c * 64, it.r0[t],
                             it.h, it.b);
-              ++qn[t];
-              qloaded[t] = true;
+              ++qn[q];
+              qloaded[q] = true;
             }
           }
           if (!ok) break;
@@ -477,12 +484,15 @@ __global__ void __launch_bounds__(384, 1)
         bool qready[2] = {false, false};
         bool ostarted[2] = {false, false};
 
+        // the item's last S of any tile frees a Q buffer shared by both slots
+        const int qlast = lastkb[0] > lastkb[1] ? lastkb[0] : lastkb[1];
         auto issue_qk = [&](int t, int sk, int kb) -> bool {
-          if (!qready[t]) {
-            if (!wait_bar(bar(C::kBarQFull + t), qn[t] & 1, abort_flag, p.err)) return false;
-            qready[t] = true;
+          const int q = kDec ? 0 : t;
+          if (!qready[q]) {
+            if (!wait_bar(bar(C::kBarQFull + q), qn[q] & 1, abort_flag, p.err)) return false;
+            qready[q] = true;
           }
-          const uint64_t dq = sdesc_sw128(sbase + C::kQOff + t * C::kTileBytes, 16, 1024);
+          const uint64_t dq = sdesc_sw128(sbase + C::kQOff + q * C::kTileBytes, 16, 1024);
           const uint64_t dk = sdesc_sw128(sbase + C::kKOff + sk * C::kTileBytes, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -492,7 +502,7 @@ __global__ void __launch_bounds__(384, 1)
           }
           mma_commit(bar(C::kBarSFull + t));
           // Q of this tile is free for the next item once its last S lands.
-          if (kb == lastkb[t]) mma_commit(bar(C::kBarQEmpty + t));
+          if (kb == (kDec ? qlast : lastkb[t])) mma_commit(bar(C::kBarQEmpty + q));
           return true;
         };
         auto issue_pv = [&](int t, int sv) -> bool {
@@ -902,11 +912,11 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D, bool CAUSAL, bool SPARSE, bool PARTIAL, bool ALT>
+template <int D, bool CAUSAL, bool SPARSE, bool PARTIAL, bool ALT, bool DEC>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, cudaStream_t st) {
-  using C = FwdCfg<D>;
-  auto kern = attn_fwd_kernel<D, CAUSAL, SPARSE, PARTIAL, ALT>;
+  using C = FwdCfg<D, DEC && ALT && !SPARSE>;
+  auto kern = attn_fwd_kernel<D, CAUSAL, SPARSE, PARTIAL, ALT, DEC>;
   constexpr int kMaxDev = 64;
   static bool configured[kMaxDev] = {};  // the attribute is per device and function
   int dev = 0;
@@ -932,28 +942,35 @@ cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUte
                        cudaStream_t st) {
   // The alternating schedule of single-tile pairs is compiled into every dense
   // kernel without a partial output; the partial-state kernels have a second
-  // instantiation without it, which launches with full pairs only run.
+  // instantiation without it, which launches with full pairs only run.  A
+  // launch whose query rows fit one tile (decoding) runs the instantiation
+  // with a single Q buffer and one more K stage.
   const bool single_tile_pair = (p.Lq % (2 * kTileM)) != 0 && (p.Lq % (2 * kTileM)) <= kTileM;
   const bool alt = !sparse && (!partial || single_tile_pair);
-#define BSS_FWD_CASE(DD, CA, SP, PA, AL)                                         \
-  if (d == DD && causal == CA && sparse == SP && partial == PA && alt == AL)     \
-    return launch_one<DD, CA, SP, PA, AL>(tq, tk, tv, p, st);
-  BSS_FWD_CASE(64, false, false, false, true)
-  BSS_FWD_CASE(64, true, false, false, true)
-  BSS_FWD_CASE(128, false, false, false, true)
-  BSS_FWD_CASE(128, true, false, false, true)
-  BSS_FWD_CASE(64, false, false, true, true)
-  BSS_FWD_CASE(64, true, false, true, true)
-  BSS_FWD_CASE(128, false, false, true, true)
-  BSS_FWD_CASE(128, true, false, true, true)
-  BSS_FWD_CASE(64, false, false, true, false)
-  BSS_FWD_CASE(64, true, false, true, false)
-  BSS_FWD_CASE(128, false, false, true, false)
-  BSS_FWD_CASE(128, true, false, true, false)
-  BSS_FWD_CASE(64, false, true, false, false)
-  BSS_FWD_CASE(64, true, true, false, false)
-  BSS_FWD_CASE(128, false, true, false, false)
-  BSS_FWD_CASE(128, true, true, false, false)
+  const bool dec = alt && p.Lq >= 1 && p.Lq <= kTileM;
+#define BSS_FWD_CASE(DD, CA, SP, PA, AL, DE)                                              \
+  if (d == DD && causal == CA && sparse == SP && partial == PA && alt == AL && dec == DE) \
+    return launch_one<DD, CA, SP, PA, AL, DE>(tq, tk, tv, p, st);
+#define BSS_FWD_CASE_D(DD, CA, SP, PA, AL) \
+  BSS_FWD_CASE(DD, CA, SP, PA, AL, false)  \
+  BSS_FWD_CASE(DD, CA, SP, PA, AL, true)
+  BSS_FWD_CASE_D(64, false, false, false, true)
+  BSS_FWD_CASE_D(64, true, false, false, true)
+  BSS_FWD_CASE_D(128, false, false, false, true)
+  BSS_FWD_CASE_D(128, true, false, false, true)
+  BSS_FWD_CASE_D(64, false, false, true, true)
+  BSS_FWD_CASE_D(64, true, false, true, true)
+  BSS_FWD_CASE_D(128, false, false, true, true)
+  BSS_FWD_CASE_D(128, true, false, true, true)
+  BSS_FWD_CASE(64, false, false, true, false, false)
+  BSS_FWD_CASE(64, true, false, true, false, false)
+  BSS_FWD_CASE(128, false, false, true, false, false)
+  BSS_FWD_CASE(128, true, false, true, false, false)
+  BSS_FWD_CASE(64, false, true, false, false, false)
+  BSS_FWD_CASE(64, true, true, false, false, false)
+  BSS_FWD_CASE(128, false, true, false, false, false)
+  BSS_FWD_CASE(128, true, true, false, false, false)
+#undef BSS_FWD_CASE_D
 #undef BSS_FWD_CASE
   return cudaErrorInvalidValue;
 }

@@ -81,21 +81,25 @@ def test_queries_before_every_key_are_empty(bss):
 
 
 def test_decode_workload_full_size(bss):
-    """B=4 H=16, 16 queries at the end of a 16384-key causal cache, 16 chunks (the
-    benchmark's launch configuration): every row against the oracle for two heads,
-    and all heads against the unsplit kernel."""
+    """B=4 H=16, 16 queries at the end of a 16384-key causal cache, in the
+    benchmark's launch configuration (2 chunks) and in 16 chunks: every row
+    against the oracle for two heads, and all heads against the unsplit kernel."""
     w = DECODE_16K
     cpu = make_inputs(w)
     inp = to_cuda(cpu)
     qo = w.L - w.Lq
-    o, lse = bss.attn_fwd_splitkv(inp["q"], inp["k"], inp["v"], w.chunks, causal=True,
-                                  scale=w.scale, q_offset=qo)
     o1, l1 = bss.attn_fwd(inp["q"], inp["k"], inp["v"], causal=True, scale=w.scale, q_offset=qo)
-    torch.cuda.synchronize()
-    assert bss.attn_poll_status() == 0
-    assert (o.float() - o1.float()).abs().max().item() <= TOL_O
-    assert (lse - l1).abs().max().item() <= TOL_LSE
     heads = [(0, 0), (3, 15)]
     O_ref, l_ref = oracle_forward(cpu, w.scale, heads=heads, causal=True, q_offset=qo)
+    for chunks in (w.chunks, 16):
+        o, lse = bss.attn_fwd_splitkv(inp["q"], inp["k"], inp["v"], chunks, causal=True,
+                                      scale=w.scale, q_offset=qo)
+        torch.cuda.synchronize()
+        assert bss.attn_poll_status() == 0
+        assert (o.float() - o1.float()).abs().max().item() <= TOL_O
+        assert (lse - l1).abs().max().item() <= TOL_LSE
+        for n_, (b, h) in enumerate(heads):
+            compare_forward(o[b, h], lse[b, h], O_ref[n_], l_ref[n_],
+                            f"head {(b, h)}, {chunks} chunks")
     for n_, (b, h) in enumerate(heads):
-        compare_forward(o[b, h], lse[b, h], O_ref[n_], l_ref[n_], f"head {(b, h)}")
+        compare_forward(o1[b, h], l1[b, h], O_ref[n_], l_ref[n_], f"unsplit head {(b, h)}")

@@ -77,11 +77,12 @@ CAUSAL_16K = Workload("causal_B2_H16_L16384_d128", 2, 16, 16384, 128, True, 1,
 
 # Decode-shaped split-KV forward (the Ring combine's other use): the queries
 # are the last 16 positions of the draw (q_offset = L - 16, causal) against a
-# 16384-key cache cut into 16 chunks.
-DECODE_16K = Workload("decode_B4_H16_Lq16_Lk16384_d128", 4, 16, 16384, 128, True, 5, chunks=16,
+# 16384-key cache cut into 2 chunks, so that the 64 heads give 128 work items:
+# one wave on the 148 SMs, one item boundary per SM.
+DECODE_16K = Workload("decode_B4_H16_Lq16_Lk16384_d128", 4, 16, 16384, 128, True, 5, chunks=2,
                       Lq=16,
                       description="decode-shaped forward: 16 queries at the end of a 16384-key "
-                                  "causal cache, 16 KV chunks merged")
+                                  "causal cache, 2 KV chunks merged")
 
 # Grouped key/value heads: the L=16384 causal shape with 4 key/value heads, each
 # shared by 4 query heads; forward and backward.

@@ -797,6 +797,15 @@ def run_profile_case(kind: str):
     import block_sparse_softmax_gb300 as bss
     bss.library()
     dev = torch.device("cuda", 0)
+    if kind == "decode":
+        # 16 queries at the end of a 16384-key causal cache, split as the bench row splits it
+        w = DECODE_16K
+        x = {k: t.to(dev) for k, t in make_inputs(w).items()}
+        ws = torch.empty(bss.attn_fwd_splitkv_workspace_bytes(w.B, w.H, w.Lq, w.L, w.d, w.chunks),
+                         device=dev, dtype=torch.uint8)
+        fn = lambda: bss.attn_fwd_splitkv(x["q"], x["k"], x["v"], w.chunks, causal=True,
+                                          scale=w.scale, q_offset=w.L - w.Lq, workspace=ws)
+        return _run_profile_fn(kind, fn)
     if kind == "select":
         # the selector on the block-sparse workload: one list per head,
         # 4 local blocks + the 4 best-scoring earlier blocks per query block
@@ -861,7 +870,7 @@ def _run_profile_fn(kind: str, fn):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile", choices=["fwd", "fwd16k", "sparse", "bwd", "partial", "merge",
-                                            "splitkv", "select"],
+                                            "splitkv", "select", "decode"],
                     default=None,
                     help="run one small case of one kernel (for ncu) and exit")
     ap.add_argument("--gpus", type=int, default=1)

@@ -33,6 +33,8 @@ def _decode_inputs(B, H, Lq, Lk, d, seed):
     (2, 2, 200, 2048, 128, 4),      # more queries than a tile
     (1, 2, 7, 300, 128, 16),        # more chunks asked than key blocks: 3 chunks
     (1, 1, 5, 100, 64, 4),          # fewer keys than one block
+    (2, 4, 16, 1100, 128, 8),       # chunks of 256 keys and a last one of 76:
+    (1, 4, 100, 1100, 64, 8),       # two-block items beside a one-block item
 ])
 def test_decode_shapes_match_oracle(bss, B, H, Lq, Lk, d, chunks):
     w, cpu = _decode_inputs(B, H, Lq, Lk, d, seed=Lq + Lk)

@@ -403,6 +403,18 @@ def measure_configs(bss, dev, peaks):
     """Each workload shape of the study, timed on its own (not part of `value`)."""
     out = {}
     pk = peaks["bf16_burst"]
+    # the exponential unit: the forward takes one ex2 per pair, a second
+    # ceiling beside the tensor core's (4 d FLOPs per pair at the ex2 rate)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    blocks, iters = sms * 8, 2048
+    sink = torch.zeros(1, device=dev)
+    n_ex2 = blocks * 256 * 8 * iters
+    ms_x = bench_kernel(lambda: bss.attn_probe_ex2_rate(blocks, iters, sink=sink), reps=10)
+    ex2_rate = n_ex2 / (ms_x * 1e-3)
+    out["ex2_rate"] = {"ex2_per_s": float(f"{ex2_rate:.4g}"),
+                       "per_sm_per_clock_at_2070mhz": round(ex2_rate / (sms * 2070e6), 2),
+                       "fwd_tflops_ceiling": {"d64": round(4 * 64 * ex2_rate / 1e12, 1),
+                                              "d128": round(4 * 128 * ex2_rate / 1e12, 1)}}
     # dense L=256 d=64: latency
     w = DENSE_SMALL
     x = {k: t.to(dev) for k, t in make_inputs(w).items()}
@@ -419,6 +431,7 @@ def measure_configs(bss, dev, peaks):
     tf = fl / ms / 1e9
     out[w.name] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_burst": round(tf / pk, 4),
                    "frac_sustained": round(tf / peaks["bf16_sustained"], 4),
+                   "frac_ex2_ceiling": round(tf / (4 * w.d * ex2_rate / 1e12), 4),
                    "target_frac": 0.6}
     del x, o, lse
     # block-sparse L'=16320
@@ -545,7 +558,8 @@ def measure_configs(bss, dev, peaks):
     pairs = w.B * w.H * causal_pairs(w.L, w.L)
     out[w.name] = {"fwd_ms": round(ms_f, 4), "bwd_ms": round(ms_b, 4),
                    "fwd_tflops": round(4 * w.d * pairs / ms_f / 1e9, 1),
-                   "bwd_tflops": round(10 * w.d * pairs / ms_b / 1e9, 1)}
+                   "bwd_tflops": round(10 * w.d * pairs / ms_b / 1e9, 1),
+                   "fwd_frac_ex2_ceiling": round(pairs / (ms_f * 1e-3) / ex2_rate, 4)}
     del x, o, lse, ws, g, dl
     # grouped key/value heads: 16 query heads over 4 shared K/V heads, L=16384
     w = GQA_16K
@@ -564,7 +578,8 @@ def measure_configs(bss, dev, peaks):
     out[w.name] = {"fwd_ms": round(ms_f, 4), "bwd_ms": round(ms_b, 4),
                    "fwd_tflops": round(4 * w.d * pairs / ms_f / 1e9, 1),
                    "bwd_tflops": round(10 * w.d * pairs / ms_b / 1e9, 1),
-                   "fwd_frac_burst": round(4 * w.d * pairs / ms_f / 1e9 / pk, 4)}
+                   "fwd_frac_burst": round(4 * w.d * pairs / ms_f / 1e9 / pk, 4),
+                   "fwd_frac_ex2_ceiling": round(pairs / (ms_f * 1e-3) / ex2_rate, 4)}
     return out
 
 

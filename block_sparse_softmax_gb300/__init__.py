@@ -25,7 +25,8 @@ __all__ = [
     "attn_fwd_blocksparse", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_blocksparse",
     "attn_bwd_blocksparse_workspace_bytes", "attn_bwd_noalloc",
     "attn_poll_status",
-    "attn_watchdog_selftest", "attn_fwd_splitkv", "attn_fwd_splitkv_workspace_bytes",
+    "attn_watchdog_selftest", "attn_probe_ex2_rate", "attn_fwd_splitkv",
+    "attn_fwd_splitkv_workspace_bytes",
     "attn_select_blocks", "attn_select_blocks_workspace_bytes", "attn_select_blocks_nnz", "library",
 ]
 
@@ -356,6 +357,18 @@ def attn_poll_status(device=None) -> int:
     """Synchronise the current stream and return (and clear) the kernels' error word."""
     stream = torch.cuda.current_stream(device).cuda_stream
     return int(_lib.load().attn_poll_status(stream))
+
+
+def attn_probe_ex2_rate(blocks: int, iters: int, sink: Optional[torch.Tensor] = None,
+                        device=None) -> int:
+    """Launch the exponential-rate kernel on the current stream; returns the
+    number of exponentials it evaluates (the caller times the launch)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    sink = torch.zeros(1, device=dev, dtype=torch.float32) if sink is None else sink
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    _check(_lib.load().attn_probe_ex2_rate(sink.data_ptr(), int(blocks), int(iters), stream),
+           "attn_probe_ex2_rate")
+    return int(blocks) * 256 * 8 * int(iters)
 
 
 def attn_watchdog_selftest(timeout_cycles: int = 1 << 20, device=None) -> None:

@@ -336,6 +336,10 @@ SplitLayout split_layout(int B, int H, int Lq, int Lk, int d, int n_chunks) {
 }
 
 }  // namespace
+
+// the exponential-unit rate kernel (merge.cu, beside the other small kernels)
+cudaError_t launch_ex2_rate(float* sink, int blocks, int iters, cudaStream_t st);
+
 }  // namespace bss
 
 using namespace bss;
@@ -605,6 +609,12 @@ attn_status_t attn_poll_status(void* stream) {
     if (e != cudaSuccess) return cuda_status("status reset", e);
   }
   return static_cast<attn_status_t>(value);
+}
+
+attn_status_t attn_probe_ex2_rate(float* sink, int blocks, int iters, void* stream) {
+  if (!sink || !aligned4(sink) || blocks <= 0 || iters <= 0) return ATTN_ERR_INVALID_ARG;
+  return cuda_status("ex2 rate probe launch",
+                     launch_ex2_rate(sink, blocks, iters, static_cast<cudaStream_t>(stream)));
 }
 
 attn_status_t attn_watchdog_selftest(unsigned long long timeout_cycles, void* stream) {

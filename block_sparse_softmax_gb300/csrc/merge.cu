@@ -67,7 +67,32 @@ __global__ void watchdog_selftest_kernel(unsigned long long cycles, int* err) {
     wait_bar(smem_u32(&never_arrived), 0, &abort_flag, err, static_cast<long long>(cycles));
 }
 
+// Exponential-unit rate: every thread runs eight independent chains of
+// y <- 2^(-y - 1/2), whose values stay in [2^-1.5, 2^-0.5], so the number of
+// ex2.approx instructions in flight, not their latency, sets the time.  Each
+// thread evaluates 8 * iters exponentials.  `sink` is written only when the
+// sum is negative, which it never is; the branch keeps the work alive.
+__global__ void __launch_bounds__(256) ex2_rate_kernel(float* sink, int iters) {
+  float y[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) y[k] = 0.5f + 0.03125f * static_cast<float>(k) +
+                                     1e-4f * static_cast<float>(threadIdx.x & 31);
+  for (int n = 0; n < iters; ++n) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) y[k] = ex2(-y[k] - 0.5f);
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) s += y[k];
+  if (s < 0.f) *sink = s;
+}
+
 }  // namespace
+
+cudaError_t launch_ex2_rate(float* sink, int blocks, int iters, cudaStream_t st) {
+  ex2_rate_kernel<<<blocks, 256, 0, st>>>(sink, iters);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge(int d, const MergeParams& p, int* err, cudaStream_t st) {
   (void)err;

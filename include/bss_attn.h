@@ -301,6 +301,20 @@ attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, cons
 attn_status_t attn_poll_status(void* stream);
 
 /*
+ * attn_probe_ex2_rate - measurement aid for the softmax's second ceiling:
+ * the forward evaluates one exponential per pair ("FlashAttention: Fast and
+ * Memory Efficient Exact Attention with IO Awareness", section 5.1, the
+ * online softmax), so pairs/s cannot exceed the SMs' ex2 rate.  Launches
+ * `blocks` blocks of 256 threads on `stream`; every thread evaluates
+ * 8 * `iters` independent ex2.approx exponentials, blocks * 256 * 8 * iters
+ * in all.  The caller times the launch.  `sink`: one device float,
+ * 4-byte aligned, never written in practice (it keeps the work alive).
+ * Returns ATTN_ERR_INVALID_ARG for a null sink or non-positive sizes, else
+ * the launch status.
+ */
+attn_status_t attn_probe_ex2_rate(float* sink, int blocks, int iters, void* stream);
+
+/*
  * attn_watchdog_selftest - launch one block that waits on a barrier nobody
  * arrives at, with a limit of `timeout_cycles` SM clock cycles; the wait gives
  * up, records ATTN_ERR_TIMEOUT and the block returns.  Lets a test observe the

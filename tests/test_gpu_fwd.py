@@ -280,3 +280,24 @@ def test_watchdog_gives_up_and_reports(bss):
     assert bss.attn_poll_status() == 0
     x = torch.ones(4, device="cuda")
     assert x.sum().item() == 4.0
+
+
+def test_ex2_rate_probe(bss):
+    """The exponential-rate kernel runs clean, rejects bad arguments, and its
+    rate lies between 1 and 64 exponentials per clock per SM at 1-2.2 GHz."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    sink = torch.zeros(1, device="cuda")
+    with pytest.raises(bss.AttnError):
+        bss.attn_probe_ex2_rate(0, 16, sink=sink)
+    n = bss.attn_probe_ex2_rate(sms * 8, 64, sink=sink)       # warm-up
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(1_000_000)
+    a.record()
+    n = bss.attn_probe_ex2_rate(sms * 8, 1024, sink=sink)
+    b.record()
+    torch.cuda.synchronize()
+    rate = n / (a.elapsed_time(b) * 1e-3)
+    assert sms * 1.0 * 1e9 <= rate <= sms * 64 * 2.2e9
+    assert sink.item() == 0.0
+    assert bss.attn_poll_status() == 0

@@ -31,7 +31,8 @@
 //   * a pair with a single query tile (short query blocks: decoding, a ragged
 //     last pair) puts the same rows in both slots and deals the key blocks to
 //     them in turn, then merges the two states per row in the epilogue, so the
-//     overlap above is kept;
+//     overlap above is kept; when every query block is one tile (decoding) a
+//     single Q buffer serves both slots and the other becomes a third K stage;
 //   * exponentials are base 2 with scale*log2(e) folded in; the running max is
 //     only moved (and O rescaled in TMEM) when it grows by more than 2^8, which
 //     keeps the result exact because l and A always share the same reference m;

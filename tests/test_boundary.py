@@ -171,3 +171,20 @@ def test_binding_fails_loudly_on_cpu_tensors():
     q = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError, match="CUDA"):
         bss.attn_fwd(q, q, q)
+
+
+@pytest.mark.parametrize("L,top_r,local,causal,n_lists", [
+    (1000, 2, 3, True, 1), (1000, 2, 3, False, 2), (129, 4, 1, True, 1), (600, 0, 2, True, 3),
+    (900, 9, 0, False, 1), (2560, 4, 4, True, 2), (128, 3, 4, True, 1)])
+def test_select_entry_count_matches_the_oracle(lib, L, top_r, local, causal, n_lists):
+    """The selector's list sizes do not depend on the scores: the library's
+    closed-form count equals the entries of the oracle's lists."""
+    import numpy as np
+    from oracle.select import select_blocks
+    rng = np.random.default_rng(L + top_r)
+    q = rng.standard_normal((1, 6, L, 8)).astype(np.float32)
+    k = rng.standard_normal((1, 3, L, 8)).astype(np.float32)
+    _, col_idx, _ = select_blocks(q, k, 0.35, top_r=top_r, local=local, causal=causal,
+                                  n_lists=n_lists)
+    assert lib.attn_select_blocks_nnz(L, top_r, local, int(causal), n_lists) == len(col_idx)
+    assert lib.attn_select_blocks_nnz(L, top_r, local, int(causal), 0) == -1

@@ -25,7 +25,7 @@ score matrix S and the probability matrix P for the rows it evaluates.  Rows are
 processed in groups only to bound memory; every row is computed from its full
 definition.
 
-Readings where the pages are silent (each also listed in the design notes):
+Readings where the pages are silent, each taken here as stated:
   * masked pairs contribute exactly zero (mask value -inf, not a large finite
     number);
   * a row with no allowed key has O = 0 and LSE = -inf and gets zero gradient;
@@ -312,13 +312,43 @@ def attention_backward(q, k, v, do, scale, *, causal=False, block=None, row_ptr=
 # ---------------------------------------------------------------------------
 
 def logical_pairs(M: np.ndarray) -> int:
+    """Number of allowed (query, key) token pairs of a realised mask: the
+    logical work of the operator ([BSP]: build the count from logical token
+    pairs, not from the padded tiles)."""
     return int(M.sum())
 
 
 def executed_tiles(M: np.ndarray, tile: int = 128) -> int:
-    """Number of (query tile, key tile) pairs with at least one allowed pair."""
+    """Number of (query tile, key tile) pairs with at least one allowed pair:
+    the tile work a kernel that skips empty tiles executes ([BSP]: executed
+    lanes differ from logical pairs)."""
     Lq, Lk = M.shape
     nq, nk = (Lq + tile - 1) // tile, (Lk + tile - 1) // tile
     pad = np.zeros((nq * tile, nk * tile), dtype=bool)
     pad[:Lq, :Lk] = M
     return int(pad.reshape(nq, tile, nk, tile).any(axis=(1, 3)).sum())
+
+
+def blocklist_stats(row_ptr, col_idx, L: int, *, causal: bool, block: int = 128) -> dict:
+    """What a block list asks for on a square sequence of L tokens ([BSP],
+    "Count active blocks and acknowledge the changed operator": report the
+    logical allowed pairs and the executed tile work; under a causal mask the
+    token-level rule applies inside every listed block, so a listed block that
+    lies wholly in the causal future contributes nothing).
+
+      listed    listed (query block, key block) pairs, duplicates counted once
+      executed  listed pairs whose tile holds at least one allowed token pair
+      future    listed pairs with no allowed token pair under the causal mask
+                (every key of the block after every query of the block)
+      pairs     allowed token pairs of the realised mask
+    """
+    n = (L + block - 1) // block
+    sets = blocklist_sets(row_ptr, col_idx, n)
+    M = allowed_mask(L, L, causal=causal, block=block, row_ptr=row_ptr, col_idx=col_idx)
+    future = 0
+    if causal:
+        for a, s in enumerate(sets):
+            last_query = min(L, (a + 1) * block) - 1
+            future += sum(1 for c in s if c * block > last_query)
+    return {"listed": sum(len(s) for s in sets), "executed": executed_tiles(M, block),
+            "future": future, "pairs": logical_pairs(M)}

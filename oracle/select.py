@@ -16,7 +16,7 @@ It follows "Exact Blocks, Rings, and Sparsity" (g-u-n.github.io blog):
   * section 6 (under grouped heads, query heads that share a KV head share the
     block choice).
 
-Readings where the pages are silent (also listed in the design notes):
+Readings where the pages are silent, each taken here as stated:
   * the score of query block a against key block c is the mean logit over the
     pair of blocks, scale * qbar_a . kbar_c, with qbar and kbar the means of
     the block's query and key rows (the mean of the per-query pooled scores of

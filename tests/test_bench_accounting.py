@@ -51,3 +51,11 @@ def test_block_sparse_workload_counts_per_head():
     pairs, tiles = bench.sparse_counts(L, rp, ci, True)
     assert tiles == 836
     assert abs(pairs - 1.261e7) <= 0.0005e7
+
+
+@pytest.mark.parametrize("L,seed", [(1000, 7), (16320, 2)])
+def test_sparse_counts_equal_the_oracles_pinned_counts(L, seed):
+    n = (L + 127) // 128
+    rp, ci = local_global_random_blocklist(n, seed=seed)
+    s = oracle.blocklist_stats(rp, ci, L, causal=True)
+    assert bench.sparse_counts(L, rp, ci, True) == (s["pairs"], s["executed"])

@@ -7,8 +7,11 @@ There is no CPU fallback: calls fail loudly when the library is not built or
 the tensors are not on a CUDA device.
 
 Functions carry the C names: ``attn_fwd``, ``attn_fwd_partial``,
-``attn_merge_states``, ``attn_blocklist_normalize``, ``attn_fwd_blocksparse``,
-``attn_bwd``, ``attn_poll_status``, ``attn_watchdog_selftest``.
+``attn_merge_states``, ``attn_fwd_splitkv``, ``attn_blocklist_normalize``,
+``attn_blocklist_stats``, ``attn_fwd_blocksparse``, ``attn_select_blocks``,
+``attn_bwd``, ``attn_bwd_blocksparse``, ``attn_bwd_noalloc``, ``attn_poll_status``,
+``attn_watchdog_selftest``, ``attn_probe_ex2_rate``.  Each call runs on the
+device of its tensors and on that device's current stream.
 """
 from __future__ import annotations
 
@@ -21,13 +24,12 @@ import torch
 from . import _lib
 
 __all__ = [
-    "AttnError", "attn_fwd", "attn_fwd_partial", "attn_merge_states", "attn_blocklist_normalize",
-    "attn_fwd_blocksparse", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_blocksparse",
-    "attn_bwd_blocksparse_workspace_bytes", "attn_bwd_noalloc",
-    "attn_poll_status",
-    "attn_watchdog_selftest", "attn_probe_ex2_rate", "attn_fwd_splitkv",
-    "attn_fwd_splitkv_workspace_bytes",
-    "attn_select_blocks", "attn_select_blocks_workspace_bytes", "attn_select_blocks_nnz", "library",
+    "AttnError", "attn_fwd", "attn_fwd_partial", "attn_merge_states", "attn_fwd_splitkv",
+    "attn_fwd_splitkv_workspace_bytes", "attn_blocklist_normalize", "attn_blocklist_stats",
+    "attn_fwd_blocksparse", "attn_select_blocks", "attn_select_blocks_workspace_bytes",
+    "attn_select_blocks_nnz", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_blocksparse",
+    "attn_bwd_blocksparse_workspace_bytes", "attn_bwd_noalloc", "attn_poll_status",
+    "attn_watchdog_selftest", "attn_probe_ex2_rate", "library",
 ]
 
 OK = 0
@@ -93,9 +95,10 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, causal: bool 
     lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32) if lse is None else lse
     _need(out, "out", torch.bfloat16, (B, H, Lq, d))
     _need(lse, "lse", torch.float32, (B, H, Lq))
-    st = _lib.load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                              lse.data_ptr(), B, H, Hkv, Lq, Lk, d, _scale(scale, d), int(causal),
-                              int(q_offset), int(k_offset), _stream_of(q))
+    with torch.cuda.device(q.device):
+        st = _lib.load().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                  lse.data_ptr(), B, H, Hkv, Lq, Lk, d, _scale(scale, d), int(causal),
+                                  int(q_offset), int(k_offset), _stream_of(q))
     _check(st, "attn_fwd")
     return out, lse
 
@@ -115,10 +118,11 @@ def attn_fwd_partial(q, k, v, *, causal: bool = False, scale: Optional[float] = 
     _need(m, "m", torch.float32, (B, H, Lq))
     _need(l, "l", torch.float32, (B, H, Lq))
     _need(acc, "acc", torch.float32, (B, H, Lq, d))
-    st = _lib.load().attn_fwd_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), m.data_ptr(),
-                                      l.data_ptr(), acc.data_ptr(), B, H, Hkv, Lq, Lk, d,
-                                      _scale(scale, d), int(causal), int(q_offset), int(k_offset),
-                                      _stream_of(q))
+    with torch.cuda.device(q.device):
+        st = _lib.load().attn_fwd_partial(q.data_ptr(), k.data_ptr(), v.data_ptr(), m.data_ptr(),
+                                          l.data_ptr(), acc.data_ptr(), B, H, Hkv, Lq, Lk, d,
+                                          _scale(scale, d), int(causal), int(q_offset), int(k_offset),
+                                          _stream_of(q))
     _check(st, "attn_fwd_partial")
     return m, l, acc
 
@@ -133,9 +137,10 @@ def attn_merge_states(m: torch.Tensor, l: torch.Tensor, acc: torch.Tensor, *, ou
     lse = torch.empty((B, H, L), device=acc.device, dtype=torch.float32) if lse is None else lse
     _need(out, "out", torch.bfloat16, (B, H, L, d))
     _need(lse, "lse", torch.float32, (B, H, L))
-    st = _lib.load().attn_merge_states(C, m.data_ptr(), l.data_ptr(), acc.data_ptr(),
-                                       out.data_ptr(), lse.data_ptr(), B, H, L, d,
-                                       _stream_of(acc))
+    with torch.cuda.device(acc.device):
+        st = _lib.load().attn_merge_states(C, m.data_ptr(), l.data_ptr(), acc.data_ptr(),
+                                           out.data_ptr(), lse.data_ptr(), B, H, L, d,
+                                           _stream_of(acc))
     _check(st, "attn_merge_states")
     return out, lse
 
@@ -162,10 +167,11 @@ def attn_fwd_splitkv(q, k, v, chunks: int, *, causal: bool = False, scale: Optio
     nbytes = attn_fwd_splitkv_workspace_bytes(B, H, Lq, Lk, d, chunks)
     if workspace is None:
         workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
-    st = _lib.load().attn_fwd_splitkv(
-        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-        workspace.data_ptr(), workspace.numel() * workspace.element_size(), B, H, Hkv, Lq, Lk,
-        d, _scale(scale, d), int(causal), int(q_offset), int(k_offset), int(chunks), _stream_of(q))
+    with torch.cuda.device(q.device):
+        st = _lib.load().attn_fwd_splitkv(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(), B, H, Hkv, Lq, Lk,
+            d, _scale(scale, d), int(causal), int(q_offset), int(k_offset), int(chunks), _stream_of(q))
     _check(st, "attn_fwd_splitkv")
     return out, lse
 
@@ -199,11 +205,12 @@ def attn_select_blocks(q, k, top_r: int, *, local_blocks: int = 1, causal: bool 
     nbytes = attn_select_blocks_workspace_bytes(B, H, L, d)
     if workspace is None:
         workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
-    st = lib.attn_select_blocks(q.data_ptr(), k.data_ptr(), B, H, Hkv, L, d, _scale(scale, d),
-                                int(causal), int(block), int(top_r), int(local_blocks),
-                                int(n_lists), row_ptr.data_ptr(), col_idx.data_ptr(),
-                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                _stream_of(q))
+    with torch.cuda.device(q.device):
+        st = lib.attn_select_blocks(q.data_ptr(), k.data_ptr(), B, H, Hkv, L, d, _scale(scale, d),
+                                    int(causal), int(block), int(top_r), int(local_blocks),
+                                    int(n_lists), row_ptr.data_ptr(), col_idx.data_ptr(),
+                                    workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                    _stream_of(q))
     _check(st, "attn_select_blocks")
     return row_ptr, col_idx[:nnz]
 
@@ -253,12 +260,35 @@ def attn_fwd_blocksparse(q, k, v, row_ptr, col_idx, *, causal: bool = False,
     lse = torch.empty((B, H, L), device=q.device, dtype=torch.float32) if lse is None else lse
     _need(out, "out", torch.bfloat16, (B, H, L, d))
     _need(lse, "lse", torch.float32, (B, H, L))
-    st = _lib.load().attn_fwd_blocksparse(
-        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Hkv, L,
-        d, _scale(scale, d), int(causal), int(block), rp.data_ptr(), ci.data_ptr(), n_lists, n_qblk,
-        nnz, _stream_of(q))
+    with torch.cuda.device(q.device):
+        st = _lib.load().attn_fwd_blocksparse(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Hkv, L,
+            d, _scale(scale, d), int(causal), int(block), rp.data_ptr(), ci.data_ptr(), n_lists, n_qblk,
+            nnz, _stream_of(q))
     _check(st, "attn_fwd_blocksparse")
     return out, lse
+
+
+STATS_FIELDS = ("listed", "executed", "future", "pairs")
+
+
+def attn_blocklist_stats(row_ptr, col_idx, L: int, *, causal: bool = False, block: int = 128,
+                         device=None, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """What each block list asks for, counted on the GPU: int64 [n_lists, 4] on the
+    device with, per list, the listed (query block, key block) pairs (duplicates
+    once), the executed tiles, the listed blocks wholly in the causal future
+    (skipped by the kernels) and the logical allowed pairs (``STATS_FIELDS``)."""
+    dev = (row_ptr.device if torch.is_tensor(row_ptr) and row_ptr.is_cuda else
+           torch.device("cuda", torch.cuda.current_device()) if device is None else device)
+    rp, ci, nnz, n_lists, n_qblk = _csr_on_device(row_ptr, col_idx, dev)
+    out = torch.empty((n_lists, 4), device=dev, dtype=torch.int64) if out is None else out
+    _need(out, "out", torch.int64, (n_lists, 4))
+    with torch.cuda.device(dev):
+        st = _lib.load().attn_blocklist_stats(rp.data_ptr(), ci.data_ptr(), n_lists, n_qblk, nnz,
+                                              int(L), int(causal), int(block), out.data_ptr(),
+                                              torch.cuda.current_stream(dev).cuda_stream)
+    _check(st, "attn_blocklist_stats")
+    return out
 
 
 def attn_bwd_workspace_bytes(B: int, H: int, L: int, d: int) -> int:
@@ -282,11 +312,12 @@ def attn_bwd(q, k, v, o, lse, dout, *, causal: bool = False, scale: Optional[flo
     nbytes = attn_bwd_workspace_bytes(B, H, L, d)
     if workspace is None:
         workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
-    st = _lib.load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                              lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                              dv.data_ptr(), delta.data_ptr(), workspace.data_ptr(),
-                              workspace.numel() * workspace.element_size(), B, H, Hkv, L,
-                              d, _scale(scale, d), int(causal), _stream_of(q))
+    with torch.cuda.device(q.device):
+        st = _lib.load().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                  dv.data_ptr(), delta.data_ptr(), workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(), B, H, Hkv, L,
+                                  d, _scale(scale, d), int(causal), _stream_of(q))
     _check(st, "attn_bwd")
     return dq, dk, dv, delta
 
@@ -315,11 +346,12 @@ def attn_bwd_blocksparse(q, k, v, o, lse, dout, row_ptr, col_idx, *, causal: boo
     nbytes = attn_bwd_blocksparse_workspace_bytes(B, H, L, d, n_lists)
     if workspace is None:
         workspace = torch.empty(max(16, nbytes), device=q.device, dtype=torch.uint8)
-    st = _lib.load().attn_bwd_blocksparse(
-        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
-        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), B, H, Hkv, L, d, _scale(scale, d),
-        int(causal), int(block), rp.data_ptr(), ci.data_ptr(), n_lists, n_qblk, nnz, _stream_of(q))
+    with torch.cuda.device(q.device):
+        st = _lib.load().attn_bwd_blocksparse(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+            dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), B, H, Hkv, L, d, _scale(scale, d),
+            int(causal), int(block), rp.data_ptr(), ci.data_ptr(), n_lists, n_qblk, nnz, _stream_of(q))
     _check(st, "attn_bwd_blocksparse")
     return dq, dk, dv, delta
 
@@ -345,18 +377,22 @@ def attn_bwd_noalloc(q, k, v, o, lse, dout, *, causal: bool = False,
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
     delta = torch.empty((B, H, L), device=q.device, dtype=torch.float32) if delta is None else delta
-    st = _lib.load().attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                      lse.data_ptr(), dout.data_ptr(), dq.data_ptr(),
-                                      dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), B, H, Hkv,
-                                      L, d, _scale(scale, d), int(causal), _stream_of(q))
+    with torch.cuda.device(q.device):
+        st = _lib.load().attn_bwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                          lse.data_ptr(), dout.data_ptr(), dq.data_ptr(),
+                                          dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), B, H, Hkv,
+                                          L, d, _scale(scale, d), int(causal), _stream_of(q))
     _check(st, "attn_bwd_noalloc")
     return dq, dk, dv, delta
 
 
 def attn_poll_status(device=None) -> int:
-    """Synchronise the current stream and return (and clear) the kernels' error word."""
-    stream = torch.cuda.current_stream(device).cuda_stream
-    return int(_lib.load().attn_poll_status(stream))
+    """Synchronise the device's current stream and return (and clear) the
+    kernels' error word of that device (default: the current device)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream(dev).cuda_stream
+        return int(_lib.load().attn_poll_status(stream))
 
 
 def attn_probe_ex2_rate(blocks: int, iters: int, sink: Optional[torch.Tensor] = None,

@@ -41,6 +41,8 @@ _SIGNATURES = {
                                       _C.c_void_p, _C.c_size_t, _C.c_void_p]),
     "attn_blocklist_normalize": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int,
                                             _C.c_void_p, _C.c_void_p, _C.c_void_p]),
+    "attn_blocklist_stats": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int, _C.c_int,
+                                        _C.c_int, _C.c_int, _C.c_int, _C.c_void_p, _C.c_void_p]),
     "attn_fwd_blocksparse": (_C.c_int, [_C.c_void_p, _C.c_void_p, _C.c_void_p, _C.c_void_p,
                                         _C.c_void_p, _C.c_int, _C.c_int, _C.c_int, _C.c_int,
                                         _C.c_int, _C.c_float, _C.c_int, _C.c_int, _C.c_void_p,

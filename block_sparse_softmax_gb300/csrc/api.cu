@@ -46,7 +46,11 @@ attn_status_t status_word(int** out) {
     set_error("cudaGetDevice", e);
     return ATTN_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  if (dev < 0 || dev >= kMaxDevices) {
+    snprintf(g_last_error, sizeof(g_last_error),
+             "device %d is beyond the %d devices this library keeps state for", dev, kMaxDevices);
+    return ATTN_ERR_UNSUPPORTED;
+  }
   std::lock_guard<std::mutex> lk(g_mu);
   if (g_status_ptr[dev] == nullptr) {
     void* ptr = nullptr;
@@ -185,45 +189,6 @@ attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int
                                 static_cast<cudaStream_t>(stream)));
 }
 
-// ---------------------------------------------------------------------------
-// Static scratch for attn_bwd_noalloc.
-//
-// Some callers cannot allocate device memory at all: code running under an
-// allocator that forbids it (a serving process that has pinned its memory
-// budget up front, a plugin host that hands out no device allocations), or a
-// caller that cannot own a workspace buffer across calls.  For them the fp32
-// dQ accumulator of the backward lives in this file-scope array instead of a
-// caller-provided workspace.  Every GPU that loads this library holds the
-// array (kNoAllocScratchFloats * 4 bytes = 32 MiB) until the process exits.
-// In host code `g_bwd_noalloc_scratch` is only a stand-in for the symbol; its
-// device address is looked up once per device with cudaGetSymbolAddress.
-constexpr size_t kNoAllocScratchFloats = size_t(8) << 20;
-static __device__ __align__(256) float g_bwd_noalloc_scratch[kNoAllocScratchFloats];
-float* g_noalloc_scratch_ptr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch on the current device (looked up on first use).
-attn_status_t noalloc_scratch(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    set_error("cudaGetDevice", e);
-    return ATTN_ERR_CUDA;
-  }
-  if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (g_noalloc_scratch_ptr[dev] == nullptr) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_bwd_noalloc_scratch);
-    if (e != cudaSuccess) {
-      set_error("cudaGetSymbolAddress(g_bwd_noalloc_scratch)", e);
-      return ATTN_ERR_CUDA;
-    }
-    g_noalloc_scratch_ptr[dev] = static_cast<float*>(ptr);
-  }
-  *out = g_noalloc_scratch_ptr[dev];
-  return ATTN_OK;
-}
-
 // Workspace of the block-sparse backward: the fp32 dQ accumulator, then (at a
 // 256-byte boundary) the key-major bitmap of the block list.
 size_t bwd_bitmap_offset(size_t acc_bytes) { return (acc_bytes + 255) & ~static_cast<size_t>(255); }
@@ -239,6 +204,9 @@ size_t bwd_bitmap_bytes(int L) {
   const size_t nblk = (static_cast<size_t>(L < 0 ? 0 : L) + 127) / 128;
   return nblk * ((nblk + 31) / 32) * 4;
 }
+// The block-sparse backward's CTA order (int32, one per (b, head, key tile))
+// follows the bitmaps at a 256-byte boundary.
+size_t bwd_order_offset(size_t bitmap_bytes) { return (bitmap_bytes + 255) & ~static_cast<size_t>(255); }
 
 // The backward of attn_bwd and attn_bwd_blocksparse (row_ptr == nullptr: dense
 // or causal); the workspace size has been checked by the caller.
@@ -309,6 +277,14 @@ attn_status_t bwd_common(const void* q, const void* k, const void* v, const void
                                              p.col_bitmap_words, p.err,
                                              static_cast<cudaStream_t>(stream)));
     if (s != ATTN_OK) return s;
+    // the CTA launch order (longest key-tile columns first), after the bitmaps
+    int* order = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bm) +
+                                        bwd_order_offset(static_cast<size_t>(n_lists) * bwd_bitmap_bytes(L)));
+    p.cta_order = order;
+    s = cuda_status("attn_bwd_blocksparse CTA order",
+                    launch_bwd_cta_order(bm, p.col_bitmap_words, nblk, B, H, Hkv, p.heads_per_list,
+                                         p.head_group, order, static_cast<cudaStream_t>(stream)));
+    if (s != ATTN_OK) return s;
   }
   return cuda_status("attn_bwd launch", launch_bwd(d, sparse, tq, tk, tv, tdo, tdq, p,
                                                    static_cast<cudaStream_t>(stream)));
@@ -336,6 +312,10 @@ SplitLayout split_layout(int B, int H, int Lq, int Lk, int d, int n_chunks) {
 }
 
 }  // namespace
+
+// The calling thread's error text (read by attn_last_error_message), for the
+// entry points defined in other files.
+void set_error_text(const char* text) { snprintf(g_last_error, sizeof(g_last_error), "%s", text); }
 
 // the exponential-unit rate kernel (merge.cu, beside the other small kernels)
 cudaError_t launch_ex2_rate(float* sink, int blocks, int iters, cudaStream_t st);
@@ -444,6 +424,31 @@ attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, 
   return fwd_common(q, k, v, B, H, H_kv, L, L, d, scale, causal, 0, 0, true, false, p, stream);
 }
 
+attn_status_t attn_blocklist_stats(const int32_t* row_ptr, const int32_t* col_idx, int n_lists,
+                                   int n_qblk, int nnz, int L, int causal, int block,
+                                   int64_t* stats, void* stream) {
+  if (block != 128) return ATTN_ERR_UNSUPPORTED;
+  if (L < 0 || n_lists < 1) return ATTN_ERR_INVALID_ARG;
+  const long long nblk = (static_cast<long long>(L) + 127) / 128;
+  if (nblk > kMaxKBlocks) return ATTN_ERR_UNSUPPORTED;
+  if (n_qblk != nblk || nnz < 0) return ATTN_ERR_BAD_BLOCKLIST;
+  if (!row_ptr || (nnz > 0 && !col_idx) || !aligned4(row_ptr) || !aligned4(col_idx))
+    return ATTN_ERR_INVALID_ARG;
+  if (!stats || (reinterpret_cast<uintptr_t>(stats) & 7u) != 0) return ATTN_ERR_INVALID_ARG;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (L == 0)
+    return cuda_status("attn_blocklist_stats clear",
+                       cudaMemsetAsync(stats, 0, static_cast<size_t>(n_lists) * 4 * sizeof(int64_t),
+                                       st));
+  int* err = nullptr;
+  attn_status_t s = status_word(&err);
+  if (s != ATTN_OK) return s;
+  return cuda_status("attn_blocklist_stats launch",
+                     launch_blocklist_stats(row_ptr, col_idx, n_lists, n_qblk, nnz, L,
+                                            causal ? 1 : 0, reinterpret_cast<long long*>(stats),
+                                            err, st));
+}
+
 attn_status_t attn_merge_states(int C, const float* m, const float* l, const float* acc, void* o,
                                 float* lse, int B, int H, int L, int d, void* stream) {
   if (C < 1 || C > 64 || B < 1 || H < 1 || L < 0) return ATTN_ERR_INVALID_ARG;
@@ -542,7 +547,9 @@ size_t attn_bwd_workspace_bytes(int B, int H, int L, int d) {
 size_t attn_bwd_blocksparse_workspace_bytes(int B, int H, int L, int d, int n_lists) {
   const size_t acc = attn_bwd_workspace_bytes(B, H, L, d);
   if ((acc == 0 && L != 0) || heads_per_list(B, H, n_lists) == 0) return 0;
-  return bwd_bitmap_offset(acc) + static_cast<size_t>(n_lists) * bwd_bitmap_bytes(L);
+  const size_t nblk = (static_cast<size_t>(L) + 127) / 128;
+  return bwd_bitmap_offset(acc) + bwd_order_offset(static_cast<size_t>(n_lists) * bwd_bitmap_bytes(L)) +
+         static_cast<size_t>(B) * H * nblk * sizeof(int32_t);
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -572,26 +579,6 @@ attn_status_t attn_bwd_blocksparse(const void* q, const void* k, const void* v, 
     return ATTN_ERR_WORKSPACE;
   return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, delta, workspace, B, H, H_kv, L, d, scale,
                     causal, row_ptr, col_idx, n_lists, nnz, stream);
-}
-
-attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
-                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
-                               float* delta, int B, int H, int H_kv, int L, int d, float scale,
-                               int causal, void* stream) {
-  if (B < 1 || H < 1 || L < 0) return ATTN_ERR_INVALID_ARG;
-  const size_t need = static_cast<size_t>(B) * H * static_cast<size_t>(L) * (d > 0 ? d : 0);
-  if (need > kNoAllocScratchFloats) {
-    snprintf(g_last_error, sizeof(g_last_error),
-             "attn_bwd_noalloc: B*H*L*d = %zu exceeds the static scratch of %zu floats; "
-             "use attn_bwd with a caller-provided workspace",
-             need, kNoAllocScratchFloats);
-    return ATTN_ERR_WORKSPACE;
-  }
-  float* scratch = nullptr;
-  attn_status_t s = noalloc_scratch(&scratch);
-  if (s != ATTN_OK) return s;
-  return attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, delta, scratch,
-                  kNoAllocScratchFloats * sizeof(float), B, H, H_kv, L, d, scale, causal, stream);
 }
 
 attn_status_t attn_poll_status(void* stream) {

@@ -125,6 +125,21 @@ struct BwdRegs {
   static_assert(128 * (kLow + 2 * kMid + kHigh) <= 512 * kLaunchRegs, "register split exceeds the launch");
 };
 
+// The key tile and (b, K/V head) of CTA x in the head-grouped order: heads in
+// groups of head_group, and inside a group key tile major (under a causal mask
+// the first key tiles have the most query tiles, so they start first).  The
+// CTAs running at any moment then belong to a few heads, whose Q, dO and fp32
+// dQ accumulator stay in L2, so the dQ reduce-adds are read-modify-writes in
+// L2 rather than in DRAM.
+__device__ __forceinline__ void bwd_cta_tile(int x, int nq, int head_group, int BH, int& bh,
+                                             int& j) {
+  const int grp = x / (head_group * nq);
+  const int gsz = min(head_group, BH - grp * head_group);
+  const int within = x - grp * head_group * nq;
+  j = within / gsz;
+  bh = grp * head_group + (within - j * gsz);
+}
+
 // The query tiles a key tile meets, in ascending order: a dense range
 // [first, nq) or the set bits of the key tile's column of the block list
 // (kept in shared memory).  Every role walks it identically.
@@ -194,22 +209,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   (void)tr;
   if (*reinterpret_cast<volatile int*>(p.err) == ATTN_ERR_TIMEOUT) return;
 
-  // CTA order: heads in groups of p.head_group, and inside a group key tile
-  // major (under a causal mask the first key tiles have the most query tiles,
-  // so they start first).  The CTAs running at any moment then belong to a
-  // few heads, whose Q, dO and fp32 dQ accumulator stay in L2, so the dQ
-  // reduce-adds are read-modify-writes in L2 rather than in DRAM.
+  // CTA order (bwd_cta_tile): heads in groups of p.head_group, key tile major
+  // inside a group.  A block-sparse launch may instead read its order from
+  // p.cta_order, which starts the few key tiles with far more query tiles
+  // than the rest first and keeps the head-grouped order for the others.
   const int L = p.L;
   const int nq = (L + kTileM - 1) / kTileM;
   // heads here are K/V heads: the CTA owns a key tile of one (b, K/V head)
   // and meets the query tiles of the G query heads that read it
   const int BH = p.B * p.Hkv;
   const int G = p.H / p.Hkv;
-  const int grp = static_cast<int>(blockIdx.x) / (p.head_group * nq);
-  const int gsz = min(p.head_group, BH - grp * p.head_group);
-  const int within = static_cast<int>(blockIdx.x) - grp * p.head_group * nq;
-  const int j = within / gsz;                     // key tile owned by this CTA
-  const int bh = grp * p.head_group + (within - j * gsz);   // (b, K/V head)
+  int j, bh;                                      // key tile owned by this CTA; (b, K/V head)
+  if (SPARSE && p.cta_order != nullptr) {
+    const int lin = __ldg(p.cta_order + blockIdx.x);
+    bh = lin / nq;
+    j = lin - bh * nq;
+  } else {
+    bwd_cta_tile(static_cast<int>(blockIdx.x), nq, p.head_group, BH, bh, j);
+  }
   const int b = bh / p.Hkv;
   const int h = bh - b * p.Hkv;                   // K/V head
   const int hq0 = h * G;                          // first query head of the group
@@ -891,7 +908,107 @@ __global__ void __launch_bounds__(256) attn_blocklist_columns_kernel(
   }
 }
 
+// Launch order of the block-sparse backward's CTAs.  A key tile's CTA walks
+// the query tiles that list it, one after another, so a column listed by far
+// more query blocks than the others (a global block every row lists) runs
+// many times longer than the rest; started late in the head-grouped order it
+// would finish alone at the end.  Longest-first scheduling bounds that tail:
+// the columns whose length exceeds 4 times the mean (and 8 query tiles) go
+// first, in the head-grouped order, then all the others in that same order,
+// which keeps their heads' Q, dO and dQ accumulator together in L2.  One CTA
+// partitions the n_cta entries stably with block-wide prefix sums.
+constexpr int kOrderThreads = 1024;
+
+__device__ __forceinline__ int bwd_column_len(const uint32_t* bm, int words, int nq, int H, int G,
+                                              int Hkv, int heads_per_list, int bh, int j) {
+  const int b = bh / Hkv;
+  const int h = bh - b * Hkv;
+  const size_t list = static_cast<size_t>(b * H + h * G) / heads_per_list;
+  const uint32_t* col = bm + (list * nq + j) * words;
+  int n = 0;
+  for (int w = 0; w < words; ++w) n += __popc(__ldg(col + w));
+  return n;
+}
+
+// Exclusive prefix sum of one int per thread over the block; *total gets the sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = lane < kOrderThreads / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xFFFFFFFFu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;                      // inclusive sums of the warps
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  *total = warp_sums[kOrderThreads / 32 - 1];
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(kOrderThreads) attn_bwd_cta_order_kernel(
+    const uint32_t* bm, int words, int nq, int B, int H, int Hkv, int heads_per_list,
+    int head_group, int* order) {
+  __shared__ int warp_sums[32];
+  const int G = H / Hkv;
+  const int BH = B * Hkv;
+  const int n_cta = BH * nq;
+  // pass 1: total query tiles over all CTAs
+  long long total = 0;
+  for (int x0 = 0; x0 < n_cta; x0 += kOrderThreads) {
+    const int x = x0 + static_cast<int>(threadIdx.x);
+    int len = 0;
+    if (x < n_cta) {
+      int bh, j;
+      bwd_cta_tile(x, nq, head_group, BH, bh, j);
+      len = bwd_column_len(bm, words, nq, H, G, Hkv, heads_per_list, bh, j);
+    }
+    int t;
+    block_exclusive_scan(len, warp_sums, &t);
+    total += t;
+  }
+  // pass 2: the long columns, then the others, each in the head-grouped order
+  int n_long = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    int base = pass == 0 ? 0 : n_long;
+    for (int x0 = 0; x0 < n_cta; x0 += kOrderThreads) {
+      const int x = x0 + static_cast<int>(threadIdx.x);
+      int bh = 0, j = 0, sel = 0;
+      if (x < n_cta) {
+        bwd_cta_tile(x, nq, head_group, BH, bh, j);
+        const int len = bwd_column_len(bm, words, nq, H, G, Hkv, heads_per_list, bh, j);
+        const bool is_long = len >= 8 && static_cast<long long>(len) * n_cta > 4 * total;
+        sel = (pass == 0) == is_long ? 1 : 0;
+      }
+      int cnt;
+      const int pos = block_exclusive_scan(sel, warp_sums, &cnt);
+      if (sel) order[base + pos] = bh * nq + j;
+      base += cnt;
+    }
+    if (pass == 0) n_long = base;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_cta_order(const uint32_t* bitmap, int words, int nq, int B, int H, int Hkv,
+                                 int heads_per_list, int head_group, int* order, cudaStream_t st) {
+  attn_bwd_cta_order_kernel<<<1, kOrderThreads, 0, st>>>(bitmap, words, nq, B, H, Hkv,
+                                                         heads_per_list, head_group, order);
+  return cudaGetLastError();
+}
 
 int bwd_dq_box_rows(int d) {
   return d == 128 ? BwdCfg<128>::kDrainBoxRows : BwdCfg<64>::kDrainBoxRows;

@@ -197,6 +197,9 @@ struct BwdParams {
   const uint32_t* col_bitmap;   // [n_lists][n_kblk][col_bitmap_words]
   int col_bitmap_words;
   int heads_per_list;           // head (b*H + h) uses list (b*H + h) / heads_per_list
+  // block-sparse: CTA x owns key tile j of (b, K/V head) bh, cta_order[x] =
+  // bh * nq + j (nullptr: the head-grouped order)
+  const int* cta_order;
   int* err;
   long long* trace;        // trace builds only (nullptr otherwise)
   int trace_cta;
@@ -213,11 +216,18 @@ cudaError_t launch_merge(int d, const MergeParams& p, int* err, cudaStream_t st)
 cudaError_t launch_bwd(int d, bool sparse, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                        const BwdParams& p, cudaStream_t st);
+cudaError_t launch_bwd_cta_order(const uint32_t* bitmap, int words, int nq, int B, int H, int Hkv,
+                                 int heads_per_list, int head_group, int* order, cudaStream_t st);
 cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int n_lists, int n_qblk,
                                      int nnz, int causal, uint32_t* bitmap, int words, int* err,
                                      cudaStream_t st);
 cudaError_t launch_watchdog_selftest(unsigned long long cycles, int* err, cudaStream_t st);
+cudaError_t launch_blocklist_stats(const int* row_ptr, const int* col_idx, int n_lists, int n,
+                                   int nnz, int L, int causal, long long* stats, int* err,
+                                   cudaStream_t st);
 int select_row_entries(int L, int top_r, int local, int causal);
+// Sets the calling thread's text of attn_last_error_message (api.cu).
+void set_error_text(const char* text);
 // Rows of the dQ accumulator's tensor-map box that the backward's drain
 // reduces with one bulk copy at head dimension d.
 int bwd_dq_box_rows(int d);

@@ -12,6 +12,12 @@
 // Two kernels: the block means of Q and K (HBM-bound: both are read once),
 // then one warp per (list, query block) that scores its candidates, picks the
 // top_r by repeated warp-wide arg-max and writes its row and row offset.
+//
+// Also here: the accounting of a block list (attn_blocklist_stats), which
+// reports what a list asks the block-sparse kernels to do (block-sparse
+// attention patterns page, 'Count active blocks and acknowledge the changed
+// operator': logical allowed pairs beside the executed tiles, and listed
+// blocks wholly in the causal future, which contribute nothing).
 #include "common.cuh"
 
 namespace bss {
@@ -328,7 +334,95 @@ cudaError_t launch_select_d(const __nv_bfloat16* q, const __nv_bfloat16* k, int 
   return cudaGetLastError();
 }
 
+// Block-list accounting: one CTA per list, one warp per query block at a
+// time.  The warp turns the row's raw entries into a bitmap in shared memory
+// (duplicates collapse, order is irrelevant), then walks the set bits.  On the
+// square, unshifted sequence of the block-sparse kernels a listed block c of
+// query block a is wholly in the causal future exactly when c > a; every other
+// listed block holds allowed pairs: all (rows x keys) pairs before the
+// diagonal, n (n + 1) / 2 on the diagonal block of n tokens.  Malformed rows and
+// entries are skipped and reported as the block-sparse kernels report them.
+constexpr int kStatWarps = 8;
+constexpr int kStatWords = kMaxKBlocks / 32;
+
+__global__ void __launch_bounds__(kStatWarps * 32) blocklist_stats_kernel(
+    const int* row_ptr, const int* col_idx, int n, int nnz, int L, int causal,
+    long long* stats, int* err) {
+  __shared__ uint32_t bm[kStatWarps][kStatWords];
+  __shared__ unsigned long long part[kStatWarps][4];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int list = blockIdx.x;
+  const int* rp = row_ptr + static_cast<size_t>(list) * (n + 1);
+  const int words = (n + 31) / 32;
+  unsigned long long listed = 0, executed = 0, future = 0, pairs = 0;
+  for (int a = warp; a < n; a += kStatWarps) {
+    for (int w = lane; w < words; w += 32) bm[warp][w] = 0u;
+    __syncwarp();
+    const int beg = __ldg(rp + a);
+    const int end = __ldg(rp + a + 1);
+    if (beg < 0 || end < beg || end > nnz) {
+      if (lane == 0) record_error(err, ATTN_ERR_BAD_BLOCKLIST);
+    } else {
+      for (int e = beg + lane; e < end; e += 32) {
+        const int c = __ldg(col_idx + e);
+        if (c < 0 || c >= n) {
+          record_error(err, ATTN_ERR_BAD_BLOCKLIST);
+          continue;
+        }
+        atomicOr(&bm[warp][c >> 5], 1u << (c & 31));
+      }
+    }
+    __syncwarp();
+    const long long nq = min(L, (a + 1) * kTileN) - a * kTileN;
+    for (int w = lane; w < words; w += 32) {
+      uint32_t bits = bm[warp][w];
+      while (bits) {
+        const int c = 32 * w + __ffs(bits) - 1;
+        bits &= bits - 1u;
+        ++listed;
+        if (causal && c > a) {
+          ++future;
+          continue;
+        }
+        ++executed;
+        const long long nk = min(L, (c + 1) * kTileN) - c * kTileN;
+        pairs += (causal && c == a) ? nq * (nq + 1) / 2 : nq * nk;
+      }
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    listed += __shfl_xor_sync(0xFFFFFFFFu, listed, o);
+    executed += __shfl_xor_sync(0xFFFFFFFFu, executed, o);
+    future += __shfl_xor_sync(0xFFFFFFFFu, future, o);
+    pairs += __shfl_xor_sync(0xFFFFFFFFu, pairs, o);
+  }
+  if (lane == 0) {
+    part[warp][0] = listed;
+    part[warp][1] = executed;
+    part[warp][2] = future;
+    part[warp][3] = pairs;
+  }
+  __syncthreads();
+  if (threadIdx.x < 4) {
+    unsigned long long t = 0;
+    for (int w = 0; w < kStatWarps; ++w) t += part[w][threadIdx.x];
+    stats[static_cast<size_t>(list) * 4 + threadIdx.x] = static_cast<long long>(t);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_blocklist_stats(const int* row_ptr, const int* col_idx, int n_lists, int n,
+                                   int nnz, int L, int causal, long long* stats, int* err,
+                                   cudaStream_t st) {
+  if (n_lists <= 0) return cudaSuccess;
+  blocklist_stats_kernel<<<static_cast<unsigned>(n_lists), kStatWarps * 32, 0, st>>>(
+      row_ptr, col_idx, n, nnz, L, causal, stats, err);
+  return cudaGetLastError();
+}
 
 int select_row_entries(int L, int top_r, int local, int causal) {
   const int n = (L + kTileN - 1) / kTileN;

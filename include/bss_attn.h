@@ -168,7 +168,8 @@ attn_status_t attn_blocklist_normalize(const int32_t* row_ptr, const int32_t* co
  *   B*H (1: one list for every head; B*H: one per head; B*H_kv with grouped
  *   query heads: one per KV head).  Each list's row_ptr holds offsets into
  *   the one col_idx array (else ATTN_ERR_BAD_BLOCKLIST).  A listed block
- *   wholly in the causal future contributes nothing.  An entry outside
+ *   wholly in the causal future contributes nothing (attn_blocklist_stats
+ *   counts such blocks, with the list's pairs and tiles).  An entry outside
  *   [0, ceil(L/128)) is ignored and reported as ATTN_ERR_BAD_BLOCKLIST by
  *   attn_poll_status; so is a row whose row_ptr range is not inside [0, nnz]
  *   (that row is then treated as empty).  A query block with an empty list
@@ -179,6 +180,29 @@ attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, 
                                    int causal, int block, const int32_t* row_ptr,
                                    const int32_t* col_idx, int n_lists, int n_qblk, int nnz,
                                    void* stream);
+
+/*
+ * attn_blocklist_stats - what a block list asks the block-sparse kernels to do.
+ * Block-sparse attention patterns page, 'Count active blocks and acknowledge the
+ * changed operator' (report the logical allowed pairs beside the executed tile
+ * work; under a causal mask the token rule applies inside every listed block,
+ * so a listed block wholly in the causal future contributes nothing: it is
+ * flagged here, not rejected).
+ *   row_ptr, col_idx, n_lists, n_qblk, nnz, L, causal, block: as
+ *   attn_fwd_blocksparse (DEVICE int32 CSR, raw form accepted, block 128).
+ *   Out: stats, DEVICE int64 [n_lists][4], 8-byte aligned, per list:
+ *     [0] listed (query block, key block) pairs, duplicates counted once;
+ *     [1] executed tiles: listed pairs holding at least one allowed pair;
+ *     [2] listed pairs wholly in the causal future (key block after query
+ *         block; 0 without a causal mask), which the kernels skip;
+ *     [3] logical allowed (query, key) pairs of the realised mask.
+ *   [0] = [1] + [2].  Malformed rows and entries are skipped and reported as
+ *   ATTN_ERR_BAD_BLOCKLIST by attn_poll_status, as in attn_fwd_blocksparse.
+ *   One launch on the stream; stats is fully written (zeros when L = 0).
+ */
+attn_status_t attn_blocklist_stats(const int32_t* row_ptr, const int32_t* col_idx, int n_lists,
+                                   int n_qblk, int nnz, int L, int causal, int block,
+                                   int64_t* stats, void* stream);
 
 /*
  * attn_select_blocks - block lists for attn_fwd_blocksparse from mean-pooled
@@ -237,8 +261,9 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 /*
  * attn_bwd_blocksparse_workspace_bytes - size of the caller-provided workspace
  * of attn_bwd_blocksparse: the fp32 dQ accumulator (B*H*L*d elements, rounded
- * up to 256 bytes) followed by a key-major bitmap of each of the n_lists
- * block lists (ceil(L/128) columns of ceil(ceil(L/128)/32) 32-bit words);
+ * up to 256 bytes), a key-major bitmap of each of the n_lists block lists
+ * (ceil(L/128) columns of ceil(ceil(L/128)/32) 32-bit words, rounded up to
+ * 256 bytes) and the launch order of the key tiles (B*H*ceil(L/128) int32);
  * 0 when n_lists does not divide B*H.
  */
 size_t attn_bwd_blocksparse_workspace_bytes(int B, int H, int L, int d, int n_lists);
@@ -254,7 +279,8 @@ size_t attn_bwd_blocksparse_workspace_bytes(int B, int H, int L, int d, int n_li
  *   128, DEVICE int32 CSR, raw form accepted) and the same causal flag; lse
  *   must come from attn_fwd_blocksparse with that list.  Each key tile walks
  *   the query blocks that list it (the list's transpose, built in the
- *   workspace on the stream).  A key block no query block lists gets
+ *   workspace on the stream, with the key tiles' launch order: columns far
+ *   longer than the mean first).  A key block no query block lists gets
  *   dK = dV = 0; a query block with an empty list gets dQ = 0.  Malformed
  *   entries are handled and reported as in attn_fwd_blocksparse.  With
  *   grouped heads the query heads of one K/V head must share one list
@@ -275,17 +301,26 @@ attn_status_t attn_bwd_blocksparse(const void* q, const void* k, const void* v, 
  * may not call cudaMalloc or own a workspace (an allocator that forbids new
  * device allocations, a host process that hands out none).  The fp32 dQ
  * accumulator lives in a static device array inside the library, 32 MiB
- * (8388608 floats) per GPU that loads the library, held until the process
- * exits.  Arguments and results are those of attn_bwd without the workspace.
+ * (8388608 floats).  Arguments and results are those of attn_bwd without the
+ * workspace.
  *   - B*H*L*d above 8388608 is rejected with ATTN_ERR_WORKSPACE before any
  *     device work (attn_last_error_message says why).
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - The array sits in a module of its own.  Under lazy module loading (the
+ *     CUDA default) the driver reserves its 32 MiB on a device during the
+ *     first attn_bwd_noalloc call there, which also looks up the array's
+ *     address (cudaGetSymbolAddress); the device then holds it until the
+ *     process exits.  Processes that never call this entry do not hold it
+ *     (unless CUDA_MODULE_LOADING=EAGER, which loads it at context creation).
+ *     Make one first call per device before fixing a memory budget and before
+ *     any stream capture (L = 0 with non-null, 16-byte aligned pointers does
+ *     the set-up and no device work).
+ *   - The cached address assumes the device's context is not reset
+ *     (cudaDeviceReset) while the library is in use.
  *   - Every call shares the one array and clears it on the stream before use.
  *     Calls that can overlap on the GPU (different streams, no ordering) race
  *     on it and give wrong gradients; serialise them.
- *   - Nothing is allocated or freed (no cudaMalloc, cudaFree or allocating
- *     library routine).
+ *   - Nothing is allocated or freed by the call itself (no cudaMalloc, cudaFree
+ *     or allocating library routine).
  */
 attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                                const float* lse, const void* dout, void* dq, void* dk, void* dv,

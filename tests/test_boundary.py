@@ -146,11 +146,16 @@ def test_argument_errors_return_codes_before_any_device_work(lib):
     assert lib.attn_fwd_splitkv(*kv(n=65)) == 1
     assert lib.attn_fwd_splitkv(*kv(ws_=wsk - 4)) == 6           # workspace too small
     # block-sparse backward: workspace = accumulator (256-byte aligned) + bitmap
-    # of ceil(L/128) columns of ceil(ceil(L/128)/32) words
+    # of ceil(L/128) columns of ceil(ceil(L/128)/32) words per list (256-byte
+    # aligned) + the key tiles' launch order (B*H*ceil(L/128) int32)
+    up = lambda x: ((x + 255) // 256) * 256
     wss = lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64, 1)
     acc = 2 * 3 * 1000 * 64 * 4
-    assert wss == ((acc + 255) // 256) * 256 + 8 * 1 * 4
-    assert lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64, 6) == wss + 5 * 8 * 1 * 4
+    assert wss == up(acc) + up(8 * 1 * 4) + 2 * 3 * 8 * 4
+    assert lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64, 6) == (
+        up(acc) + up(6 * 8 * 1 * 4) + 2 * 3 * 8 * 4)
+    assert lib.attn_bwd_blocksparse_workspace_bytes(1, 2, 9000, 64, 2) == (
+        up(2 * 9000 * 64 * 4) + up(2 * 71 * 3 * 4) + 2 * 71 * 4)
     assert lib.attn_bwd_blocksparse_workspace_bytes(2, 3, 1000, 64, 4) == 0   # 4 does not divide 6
     sp = lambda block=128, nq=8, ws_=wss, rp=P: (P, P, P, P, P, P, P, P, P, P, P, ws_, 2, 3, 3,
                                                  1000, 64, 0.125, 1, block, rp, P, 1, nq, 4, None)

@@ -6,7 +6,8 @@ import pytest
 import torch
 
 import oracle
-from tests.parity import TOL_LSE, TOL_O, compare_forward, oracle_forward, to_cuda
+from tests.parity import (TOL_LSE, TOL_O, compare_forward, oracle_forward, tile_edge_rows,
+                          to_cuda)
 from workloads import SPLITKV_128K, Workload, chunk_bounds, make_inputs, sample_rows, to_f64
 
 pytestmark = pytest.mark.gpu
@@ -67,9 +68,12 @@ def test_split_kv_merge_equals_oracle_and_unsplit(bss, chunks, causal):
 
 
 def test_merge_order_does_not_matter(bss):
+    """Chunk states merged in three orders: each result matches the oracle's
+    unchunked attention, and the orders agree with each other."""
     L, d, C = 700, 64, 5
     w = Workload("o", 2, 2, L, d, True, seed=31)
-    inp = to_cuda(make_inputs(w))
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
     bounds = chunk_bounds(L, C)
     states = [bss.attn_fwd_partial(inp["q"], inp["k"][:, :, s:e].contiguous(),
                                    inp["v"][:, :, s:e].contiguous(), causal=True, k_offset=s)
@@ -81,9 +85,68 @@ def test_merge_order_does_not_matter(bss):
         a = torch.stack([states[i][2] for i in perm])
         outs.append(bss.attn_merge_states(m, l, a))
     torch.cuda.synchronize()
+    O_ref, l_ref = oracle_forward(cpu, w.scale, causal=True)
+    for n_, (o, lse) in enumerate(outs):
+        compare_forward(o, lse, O_ref, l_ref, f"merge order {n_}")
     for o, lse in outs[1:]:
         assert (o.float() - outs[0][0].float()).abs().max().item() <= 1e-2
         assert (lse - outs[0][1]).abs().max().item() <= 1e-5
+
+
+def _per_chunk(bss, inp, bounds, scale, q_offset=0):
+    """attn_fwd_partial once per key chunk (chunks copied out, as a Ring step
+    receives them), then attn_merge_states over the stacked states."""
+    q = inp["q"]
+    B, H, Lq, d = q.shape
+    C = len(bounds)
+    m = torch.empty(C, B, H, Lq, device="cuda")
+    l = torch.empty_like(m)
+    acc = torch.empty(C, B, H, Lq, d, device="cuda")
+    for c, (s, e) in enumerate(bounds):
+        bss.attn_fwd_partial(q, inp["k"][:, :, s:e].contiguous(), inp["v"][:, :, s:e].contiguous(),
+                             causal=True, scale=scale, q_offset=q_offset, k_offset=s, m=m[c],
+                             l=l[c], acc=acc[c])
+    o, lse = bss.attn_merge_states(m, l, acc)
+    return o, lse, m
+
+
+def test_per_chunk_partials_and_merge_against_the_oracle(bss):
+    """The Ring combine as separate launches: 8 chunk states of a causal
+    L = 4096 head set, merged, against the oracle on tile-edge and chunk-edge
+    rows.  Rows 0..511 see only the first chunk, so 7 of their 8 states are
+    empty."""
+    L, d = 4096, 128
+    w = Workload("pc", 1, 4, L, d, True, seed=33)
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    bounds = chunk_bounds(L, 8)
+    o, lse, m = _per_chunk(bss, inp, bounds, w.scale)
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    assert torch.isneginf(m[1:, :, :, :512]).all()          # empty chunk states
+    rows = tile_edge_rows(L, seed=5)
+    heads = [(0, 0), (0, 3)]
+    O_ref, l_ref = oracle_forward(cpu, w.scale, rows=rows, heads=heads, causal=True)
+    for n_, (b, h) in enumerate(heads):
+        compare_forward(o[b, h, rows], lse[b, h, rows], O_ref[n_], l_ref[n_], f"head {(b, h)}")
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+def test_per_chunk_merge_with_a_chunk_wholly_in_the_future(bss):
+    """Keys extend 512 positions past the last query: the ninth chunk is empty
+    for every row, the merge skips it, and the result is the oracle's."""
+    Lq, Lk, d = 1536, 2048, 64
+    w = Workload("pf", 1, 2, Lk, d, True, seed=34)
+    cpu = make_inputs(w)
+    cpu["q"] = cpu["q"][:, :, :Lq].contiguous()
+    inp = to_cuda(cpu)
+    bounds = chunk_bounds(Lk, 4)
+    o, lse, m = _per_chunk(bss, inp, bounds, w.scale)
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    assert torch.isneginf(m[3]).all()
+    O_ref, l_ref = oracle_forward(cpu, w.scale, causal=True)
+    compare_forward(o, lse, O_ref, l_ref, "future chunk")
 
 
 def test_merge_of_empty_states(bss):
@@ -121,3 +184,23 @@ def test_long_context_split_kv_full_size(bss):
     O_ref, l_ref = oracle_forward(cpu, w.scale, rows=rows, heads=heads, causal=True)
     for n_, (b, h) in enumerate(heads):
         compare_forward(o[b, h, rows], lse[b, h, rows], O_ref[n_], l_ref[n_], f"head {(b, h)}")
+
+
+def test_long_context_per_chunk_launches_full_size(bss):
+    """B=1 H=8 L=131072 d=128, the long workload as its description has it:
+    each of the 8 contiguous KV chunks attended separately (one
+    attn_fwd_partial launch each) and the states merged; against the oracle on
+    sampled rows of two heads."""
+    w = SPLITKV_128K
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    o, lse, m = _per_chunk(bss, inp, chunk_bounds(w.L, w.chunks), w.scale)
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    del m
+    rows = sample_rows(w.L, w.chunks, 96, seed=w.seed)
+    heads = [(0, 2), (0, 7)]
+    O_ref, l_ref = oracle_forward(cpu, w.scale, rows=rows, heads=heads, causal=True)
+    for n_, (b, h) in enumerate(heads):
+        compare_forward(o[b, h, rows], lse[b, h, rows], O_ref[n_], l_ref[n_], f"head {(b, h)}")
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()

@@ -1,21 +1,27 @@
 #!/usr/bin/env python
 """Benchmark of the GB300 attention path (one JSON line on rank 0).
 
-A step is one pass of the whole hot path over one batch of the causal
-B=4 H=16 L=4096 d=128 workload (bf16 inputs resident in HBM):
+A step is one pass of the whole hot path over one batch of the dense causal
+B=2 H=16 L=16384 d=128 workload (bf16 inputs resident in HBM; 537 MB of Q, K,
+V and dO, larger than the 129 MB L2):
   1. causal forward                    (attn_fwd: O, LSE)
-  2. split-KV forward: 8 KV chunks     (attn_fwd_partial x 8, attn_merge_states)
-  3. block-sparse forward              (attn_fwd_blocksparse, local+global+random list)
+  2. split-KV forward: 8 KV chunks     (attn_fwd_splitkv: the partial states of
+                                        every chunk in one launch, then
+                                        attn_merge_states)
+  3. block-sparse forward              (attn_fwd_blocksparse, the local + global
+                                        + random list over 128 blocks)
   4. backward by recomputation         (attn_bwd: D, dQ, dK, dV)
-`value` is the algorithmic TFLOP/s of the step (4d FLOPs per allowed pair for
-each forward, 10d per allowed pair for the backward).  The forward alone
-(the metric's own operation), sparse pairs/s, the L=16384 dense causal
-target and the other workload shapes are reported beside it.
+`value` is the metric's own quantity: the causal forward's algorithmic TFLOP/s
+(4d FLOPs per allowed pair) over its CUDA-event time inside the timed steps,
+summed over ranks.  `step_tflops` is the whole step's algorithmic TFLOP/s
+(10d per allowed pair for the backward).  Sparse pairs/s, the roofline of the
+step's dominant kernel and of the forward, and the other workload shapes are
+reported beside it.
 
---impl reference times the fp64 CPU oracle on a bounded sample of the same
-step (one head) on the host cores, with the same metric and unit.
-Multi-GPU (torchrun): every rank runs its own batch (independent heads, no
-data-path collective; weak scaling); time is the max over ranks.
+--impl reference times the fp64 CPU oracle's forward on a bounded sample of
+the same workload (rows of one head) on the host cores, with the same metric
+and unit.  Multi-GPU (torchrun): every rank runs its own batch (independent
+heads, no data-path collective; weak scaling); time is the max over ranks.
 """
 from __future__ import annotations
 
@@ -89,17 +95,20 @@ def load_peaks():
     return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
-# The kernel behind each row of the step, and the sources that define it (the
-# DRAM traffic recorded for a kernel is used only while they are unchanged).
+# The kernels behind each row of the step, and the sources that define the
+# kernel whose DRAM traffic is reported (the traffic recorded for a kernel is
+# used only while those sources are unchanged).
 KERNEL_OF_ROW = {
-    "fwd": "attn_fwd_kernel (causal, persistent)",
+    "fwd": "attn_fwd_kernel (causal, persistent): the whole attn_fwd call",
     "splitkv": "attn_fwd_kernel (partial, 8 key chunks in one launch) + merge_states_kernel",
     "sparse": "attn_fwd_kernel (block-sparse)",
-    "bwd": "attn_bwd_main_kernel (+ preprocess and dq_convert in the same call)",
+    "bwd": "attn_bwd call: attn_bwd_preprocess_kernel + attn_bwd_main_kernel + "
+           "attn_bwd_dq_convert_kernel (timed together)",
 }
 TRAFFIC_KERNEL = {"fwd": "attn_fwd_kernel", "bwd": "attn_bwd_main_kernel"}
 KERNEL_SOURCES = {"attn_fwd_kernel": ["fwd.cu", "common.cuh", "ptx.cuh"],
                   "attn_bwd_main_kernel": ["bwd.cu", "common.cuh", "ptx.cuh"]}
+STEP_WORKLOAD = CAUSAL_16K
 
 
 def kernel_source_hash(kernel: str) -> str:
@@ -120,9 +129,9 @@ def dram_traffic(row: str):
     if kernel is None or not os.path.exists(path):
         return None, "no ncu capture of this kernel"
     with open(path) as f:
-        rec = json.load(f).get(kernel)
+        rec = json.load(f).get(f"{kernel}@{STEP_WORKLOAD.name}")
     if rec is None:
-        return None, "no ncu capture of this kernel"
+        return None, "no ncu capture of this kernel on the step's workload"
     if rec.get("source_sha256") != kernel_source_hash(kernel):
         return None, "kernel changed since the ncu capture"
     return rec["dram_bytes_per_launch"], rec.get("capture", "")
@@ -144,7 +153,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
+                 "--format=csv,noheader,nounits", "-lms", "20"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -224,11 +233,14 @@ def job_throughput(flops_per_rank: float, ms_max: float, world: int) -> float:
 class Step:
     """All rows of the hot path on one batch; buffers preallocated."""
 
-    def __init__(self, bss, w: Workload, dev):
+    ROWS = ("fwd", "splitkv", "sparse", "bwd")
+
+    def __init__(self, bss, w: Workload, dev, cpu=None):
         self.bss = bss
         self.w = w
         B, H, L, d = w.B, w.H, w.L, w.d
-        cpu = make_inputs(Workload(w.name, B, H, L, d, True, w.seed, backward=True))
+        if cpu is None:
+            cpu = make_inputs(Workload(w.name, B, H, L, d, True, w.seed, backward=True))
         self.cpu = cpu
         self.dev = {k: v.to(dev) for k, v in cpu.items()}
         self.o = torch.empty_like(self.dev["q"])
@@ -261,15 +273,21 @@ class Step:
             "bwd": 10 * d * self.pairs_causal,
         }
         self.total_flops = sum(self.flops.values())
-        self.launches_per_step = 1 + 2 + 1 + 3
+        self.launches = {"fwd": 1, "splitkv": 2, "sparse": 1, "bwd": 3}
+        self.launches_per_step = sum(self.launches.values())
         self.events = None
+
+    def run_fwd(self):
+        d, w = self.dev, self.w
+        self.bss.attn_fwd(d["q"], d["k"], d["v"], causal=True, scale=w.scale, out=self.o,
+                          lse=self.lse)
 
     def run(self, timed_rows=False):
         bss, d, w = self.bss, self.dev, self.w
         ev = self.events if timed_rows else None
         if ev is not None:
             ev["fwd"][0].record()
-        bss.attn_fwd(d["q"], d["k"], d["v"], causal=True, scale=w.scale, out=self.o, lse=self.lse)
+        self.run_fwd()
         if ev is not None:
             ev["fwd"][1].record()
             ev["splitkv"][0].record()
@@ -310,13 +328,14 @@ def time_loop(fn, steps, warmup, sync_all):
     return start.elapsed_time(end) / steps
 
 
-def e2e_pipelined_ms(sets, host_in, host_outs, steps, warmup, sync_all):
+def e2e_pipelined_ms(sets, host_in, host_outs, out_names, compute_fn, steps, warmup, sync_all):
     """Milliseconds per step end to end through the public API: every step
-    uploads its inputs from pinned host memory and downloads its results
-    (O, LSE, dQ, dK, dV) to pinned host memory, all inside the timed region.
-    The copies run on one stream per direction and overlap the neighbouring
-    steps' compute: step k+1 uploads into one of two device buffer sets while
-    step k computes on the other and step k-1's results come down."""
+    uploads its inputs from pinned host memory and downloads its results to
+    pinned host memory, all inside the timed region.  The copies run on one
+    stream per direction and overlap the neighbouring steps' compute: step k+1
+    uploads into one of two device buffer sets while step k computes on the
+    other and step k-1's results come down.  ``compute_fn(set)`` runs a step's
+    calls on a buffer set; ``out_names`` are the set's result attributes."""
     comp = torch.cuda.current_stream()
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
     ev_up = [torch.cuda.Event() for _ in range(2)]      # set s: inputs uploaded
@@ -337,7 +356,7 @@ def e2e_pipelined_ms(sets, host_in, host_outs, steps, warmup, sync_all):
         comp.wait_event(ev_up[s])
         if k >= 2:
             comp.wait_event(ev_down[s])                 # set s's results already copied out
-        sets[s].run()
+        compute_fn(sets[s])
         ev_comp[s].record(comp)
 
     def download(k):
@@ -345,11 +364,8 @@ def e2e_pipelined_ms(sets, host_in, host_outs, steps, warmup, sync_all):
         st, ho = sets[s], host_outs[s]
         with torch.cuda.stream(down):
             down.wait_event(ev_comp[s])
-            ho["o"].copy_(st.o, non_blocking=True)
-            ho["lse"].copy_(st.lse, non_blocking=True)
-            ho["dq"].copy_(st.dq, non_blocking=True)
-            ho["dk"].copy_(st.dk, non_blocking=True)
-            ho["dv"].copy_(st.dv, non_blocking=True)
+            for n in out_names:
+                ho[n].copy_(getattr(st, n), non_blocking=True)
             ev_down[s].record(down)
 
     def run(n, start=None, end=None):
@@ -420,13 +436,13 @@ def measure_configs(bss, dev, peaks):
     x = {k: t.to(dev) for k, t in make_inputs(w).items()}
     ms = bench_kernel(lambda: bss.attn_fwd(x["q"], x["k"], x["v"], scale=w.scale), reps=50)
     out[w.name] = {"us": round(ms * 1e3, 2)}
-    # dense causal target at L=16384
+    # dense causal target at L=16384, timed alone (the step times it in place)
     w = CAUSAL_16K
     x = {k: t.to(dev) for k, t in make_inputs(w).items()}
     o = torch.empty_like(x["q"])
     lse = torch.empty(w.B, w.H, w.L, device=dev)
     ms = bench_kernel(lambda: bss.attn_fwd(x["q"], x["k"], x["v"], causal=True, scale=w.scale,
-                                           out=o, lse=lse))
+                                           out=o, lse=lse), reps=20)
     fl = 4 * w.d * w.B * w.H * causal_pairs(w.L, w.L)
     tf = fl / ms / 1e9
     out[w.name] = {"ms": round(ms, 4), "tflops": round(tf, 1), "frac_burst": round(tf / pk, 4),
@@ -434,6 +450,35 @@ def measure_configs(bss, dev, peaks):
                    "frac_ex2_ceiling": round(tf / (4 * w.d * ex2_rate / 1e12), 4),
                    "target_frac": 0.6}
     del x, o, lse
+    # causal B=4 H=16 L=4096 d=128: forward, 8-chunk split-KV, backward
+    w = CAUSAL_4K
+    x = {k: t.to(dev) for k, t in make_inputs(
+        Workload(w.name, w.B, w.H, w.L, w.d, True, w.seed, backward=True)).items()}
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(w.B, w.H, w.L, device=dev)
+    ms_f = bench_kernel(lambda: bss.attn_fwd(x["q"], x["k"], x["v"], causal=True, scale=w.scale,
+                                             out=o, lse=lse), reps=20)
+    ws = torch.empty(bss.attn_fwd_splitkv_workspace_bytes(w.B, w.H, w.L, w.L, w.d, 8),
+                     device=dev, dtype=torch.uint8)
+    o2, lse2 = torch.empty_like(o), torch.empty_like(lse)
+    ms_s = bench_kernel(lambda: bss.attn_fwd_splitkv(x["q"], x["k"], x["v"], 8, causal=True,
+                                                     scale=w.scale, workspace=ws, out=o2,
+                                                     lse=lse2), reps=20)
+    wsb = torch.empty(bss.attn_bwd_workspace_bytes(w.B, w.H, w.L, w.d), device=dev,
+                      dtype=torch.uint8)
+    g = [torch.empty_like(x["q"]) for _ in range(3)]
+    dl = torch.empty_like(lse)
+    ms_b = bench_kernel(lambda: bss.attn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], causal=True,
+                                             scale=w.scale, workspace=wsb, dq=g[0], dk=g[1],
+                                             dv=g[2], delta=dl), reps=20)
+    pairs = w.B * w.H * causal_pairs(w.L, w.L)
+    out[w.name] = {"fwd_ms": round(ms_f, 4), "fwd_tflops": round(4 * w.d * pairs / ms_f / 1e9, 1),
+                   "fwd_frac_burst": round(4 * w.d * pairs / ms_f / 1e9 / pk, 4),
+                   "splitkv8_ms": round(ms_s, 4),
+                   "splitkv8_tflops": round(4 * w.d * pairs / ms_s / 1e9, 1),
+                   "bwd_ms": round(ms_b, 4), "bwd_tflops": round(10 * w.d * pairs / ms_b / 1e9, 1),
+                   "bwd_frac_burst": round(10 * w.d * pairs / ms_b / 1e9 / pk, 4)}
+    del x, o, lse, ws, o2, lse2, wsb, g, dl
     # block-sparse L'=16320
     w = SPARSE_16K
     x = {k: t.to(dev) for k, t in make_inputs(w).items()}
@@ -503,7 +548,7 @@ def measure_configs(bss, dev, peaks):
             bss.attn_fwd_partial(x["q"], kc[c], vc[c], causal=True, scale=w.scale, k_offset=s,
                                  m=m[c], l=l_[c], acc=acc[c])
 
-    ms_p = bench_kernel(partials, reps=2, warmup=1)
+    ms_p = bench_kernel(partials, reps=5, warmup=1)
     ms_m = bench_kernel(lambda: bss.attn_merge_states(m, l_, acc, out=o, lse=lse), reps=10)
     del m, l_, acc, kc, vc
     # the same in one split-KV launch (chunks read in place) + merge
@@ -511,7 +556,7 @@ def measure_configs(bss, dev, peaks):
                      device=dev, dtype=torch.uint8)
     ms_s = bench_kernel(lambda: bss.attn_fwd_splitkv(x["q"], x["k"], x["v"], w.chunks, causal=True,
                                                      scale=w.scale, workspace=ws, out=o, lse=lse),
-                        reps=3, warmup=1)
+                        reps=5, warmup=1)
     fl = 4 * w.d * w.B * w.H * causal_pairs(w.L, w.L)
     rows = w.B * w.H * w.L
     nonempty = sum(w.B * w.H * max(0, w.L - s) for s, _ in bounds)
@@ -599,7 +644,7 @@ def run_gpu(args):
     import block_sparse_softmax_gb300 as bss
     bss.library()
     peaks = load_peaks()
-    w = rank_workload(CAUSAL_4K, rank)
+    w = rank_workload(STEP_WORKLOAD, rank)
     step = Step(bss, w, dev)
     # warm-up, then the timed region (device-resident inputs); every row of
     # every step is bracketed by CUDA events on the launching stream
@@ -628,46 +673,65 @@ def run_gpu(args):
     ms_step = start.elapsed_time(end) / args.steps
     row_avg = {k: statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for ev in events)
                for k in step.flops}
+    ms_fwd = row_avg["fwd"]
     if world > 1:
         ms_step = max_over_ranks(ms_step, dev)
+        ms_fwd = max_over_ranks(ms_fwd, dev)
 
-    # end to end through the public API: pinned host inputs in, results out,
-    # copies overlapping the neighbouring steps (a second device buffer set)
-    names_in = ["q", "k", "v", "do"]
-    host_in = {n: step.cpu[n].pin_memory() for n in names_in}
-    host_outs = [{**{n: torch.empty(step.o.shape, dtype=torch.bfloat16).pin_memory()
-                     for n in ("o", "dq", "dk", "dv")},
-                  "lse": torch.empty(step.lse.shape).pin_memory()} for _ in range(2)]
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_outs[0].values())
-    sets = [step, Step(bss, w, dev)]
-    ms_e2e = e2e_pipelined_ms(sets, host_in, host_outs, max(3, args.steps // 2), 2, sync_all)
-    del sets
+    # end to end through the public API, pinned host buffers in and out, copies
+    # overlapping the neighbouring steps (a second device buffer set):
+    #   the metric's own operation: upload Q, K, V; attn_fwd; download O, LSE
+    #   the whole step: upload Q, K, V, dO; every row; download O, LSE, dQ, dK, dV
+    sets = [step, Step(bss, w, dev, cpu=step.cpu)]
+    fwd_in = {n: step.cpu[n].pin_memory() for n in ("q", "k", "v")}
+    step_in = {**fwd_in, "do": step.cpu["do"].pin_memory()}
 
-    # the same with no overlap: upload, step, download on one stream
+    def host_like(names):
+        return [{n: torch.empty(getattr(step, n).shape, dtype=getattr(step, n).dtype).pin_memory()
+                 for n in names} for _ in range(2)]
+
+    fwd_out_names, step_out_names = ("o", "lse"), ("o", "lse", "dq", "dk", "dv")
+    fwd_outs, step_outs = host_like(fwd_out_names), host_like(step_out_names)
+    nbytes = lambda d: sum(t.numel() * t.element_size() for t in d.values())
+    n_e2e = max(3, args.steps // 2)
+    ms_e2e = e2e_pipelined_ms(sets, fwd_in, fwd_outs, fwd_out_names, Step.run_fwd, n_e2e, 2,
+                              sync_all)
+    ms_e2e_step = e2e_pipelined_ms(sets, step_in, step_outs, step_out_names, Step.run, n_e2e, 2,
+                                   sync_all)
+
+    # the forward with no overlap: upload, attn_fwd, download on one stream
     def e2e_serial(_timed):
-        for n in names_in:
-            step.dev[n].copy_(host_in[n], non_blocking=True)
-        step.run()
-        for n, t in (("o", step.o), ("lse", step.lse), ("dq", step.dq), ("dk", step.dk),
-                     ("dv", step.dv)):
-            host_outs[0][n].copy_(t, non_blocking=True)
+        for n, t in fwd_in.items():
+            step.dev[n].copy_(t, non_blocking=True)
+        step.run_fwd()
+        for n in fwd_out_names:
+            fwd_outs[0][n].copy_(getattr(step, n), non_blocking=True)
 
-    ms_e2e_serial = time_loop(e2e_serial, max(3, args.steps // 2), 2, sync_all)
+    ms_e2e_serial = time_loop(e2e_serial, n_e2e, 2, sync_all)
+    del sets
     if world > 1:
         ms_e2e = max_over_ranks(ms_e2e, dev)
+        ms_e2e_step = max_over_ranks(ms_e2e_step, dev)
         ms_e2e_serial = max_over_ranks(ms_e2e_serial, dev)
     status = bss.attn_poll_status()
+    # the step's block list as the library counts it (listed, executed,
+    # causal-future blocks, allowed pairs), beside the host accounting
+    list_stats = bss.attn_blocklist_stats(step.rp_dev, step.ci_dev, w.L, causal=True).cpu().tolist()[0]
 
-    fwd_tf = step.flops["fwd"] / row_avg["fwd"] / 1e9
-    bwd_tf = step.flops["bwd"] / row_avg["bwd"] / 1e9
-    value = job_throughput(step.total_flops, ms_step, world)
+    pk_b, pk_s = peaks["bf16_burst"], peaks["bf16_sustained"]
+    value = job_throughput(step.flops["fwd"], ms_fwd, world)
+    step_tf = job_throughput(step.total_flops, ms_step, world)
+    row_tf = {k: step.flops[k] / row_avg[k] / 1e9 for k in step.flops}
     # dominant kernel: the largest share of the step's time
     dom = max(row_avg, key=row_avg.get)
-    dom_tf = step.flops[dom] / row_avg[dom] / 1e9
+    dom_tf = row_tf[dom]
     traffic, traffic_note = dram_traffic(dom)
+    traffic_f, traffic_note_f = dram_traffic("fwd")
+    timed_s = ms_step * args.steps / 1e3
     # the per-workload table is one GPU's measurement: rank 0 alone takes it
     extra = {} if (args.quick or rank != 0) else measure_configs(bss, dev, peaks)
+    peak_kind = (f"bf16 burst ({peaks['source']}): the timed region lasts {timed_s:.2f} s, "
+                 f"not a seconds-long run at the power cap")
     out = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -682,37 +746,55 @@ def run_gpu(args):
         "dtype": "bf16",
         "data": "synthetic: torch.randn seeded, rounded to bf16 (no dataset)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "causal": True,
+                   "value": "causal forward (attn_fwd): 4d FLOPs per allowed pair over its mean "
+                            "CUDA-event time inside the timed steps, summed over ranks",
                    "step": "causal fwd + 8-chunk split-KV fwd and merge + block-sparse fwd "
                            "(local+global+random, 128-blocks) + recompute bwd",
-                   "l2": "inputs 268 MB per step > 129 MB L2; no flush",
+                   "l2": "inputs 537 MB per step > 129 MB L2; no flush",
                    "parallelism": f"replicas x{world} (independent heads per GPU)"},
-        "fwd_tflops": round(fwd_tf, 1),
-        "fwd_frac_of_burst_peak": round(fwd_tf / peaks["bf16_burst"], 4),
-        "bwd_tflops": round(bwd_tf, 1),
+        "fwd_ms": round(ms_fwd, 4),
+        "fwd_frac_of_burst_peak": round(value / world / pk_b, 4),
+        "step_tflops": round(step_tf, 2),
+        "row_tflops": {k: round(v, 1) for k, v in row_tf.items()},
+        "row_ms": {k: round(v, 4) for k, v in row_avg.items()},
         "sparse_pairs_per_s": step.pairs_sparse / row_avg["sparse"] * 1e3,
         "sparse_executed_tiles": step.tiles_sparse,
-        "row_ms": {k: round(v, 4) for k, v in row_avg.items()},
+        "sparse_list_stats": dict(zip(("listed", "executed", "future", "pairs"), list_stats)),
         "roofline": {"kernel": KERNEL_OF_ROW[dom],
                      "share_of_step": round(row_avg[dom] / sum(row_avg.values()), 4),
                      "bound": "tensor", "achieved": round(dom_tf, 1),
-                     "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": round(dom_tf / peaks["bf16_sustained"], 4),
-                     "peak_kind": f"bf16 sustained ({peaks['source']})",
+                     "peak": pk_b, "unit": "TFLOP/s",
+                     "frac": round(dom_tf / pk_b, 4),
+                     "frac_of_sustained": round(dom_tf / pk_s, 4),
+                     "peak_kind": peak_kind,
+                     "flops_per_launch": step.flops[dom],
                      "traffic": traffic, "traffic_note": traffic_note},
+        "roofline_fwd": {"kernel": KERNEL_OF_ROW["fwd"], "bound": "tensor",
+                         "achieved": round(row_tf["fwd"], 1), "peak": pk_b, "unit": "TFLOP/s",
+                         "frac": round(row_tf["fwd"] / pk_b, 4),
+                         "frac_of_sustained": round(row_tf["fwd"] / pk_s, 4),
+                         "flops_per_launch": step.flops["fwd"], "target_frac": 0.6,
+                         "traffic": traffic_f, "traffic_note": traffic_note_f},
         "clocks": clock_info,
-        "e2e": {"value": round(job_throughput(step.total_flops, ms_e2e, world), 2), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+        "e2e": {"value": round(job_throughput(step.flops["fwd"], ms_e2e, world), 2), "unit": UNIT,
+                "h2d_bytes_per_step": nbytes(fwd_in), "d2h_bytes_per_step": nbytes(fwd_outs[0]),
                 "ms_per_step": round(ms_e2e, 4),
+                "what": "attn_fwd through the public API: Q, K, V uploaded from pinned host "
+                        "memory, O and LSE downloaded, every step",
                 "copies": "one stream per direction, overlapping the neighbouring steps",
-                "serial_value": round(job_throughput(step.total_flops, ms_e2e_serial, world), 2),
-                "serial_ms_per_step": round(ms_e2e_serial, 4)},
+                "serial_value": round(job_throughput(step.flops["fwd"], ms_e2e_serial, world), 2),
+                "serial_ms_per_step": round(ms_e2e_serial, 4),
+                "step": {"tflops": round(job_throughput(step.total_flops, ms_e2e_step, world), 2),
+                         "ms_per_step": round(ms_e2e_step, 4),
+                         "h2d_bytes_per_step": nbytes(step_in),
+                         "d2h_bytes_per_step": nbytes(step_outs[0])}},
         "gpu_launches": step.launches_per_step * args.steps,
         "device_status": status,
         "wall_s_timed": round(wall, 3),
         "configs_measured": extra,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(step_sample_seconds=args.cpu_seconds)
+        out["cpu_baseline"] = cpu_baseline(sample_seconds=args.cpu_seconds)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -724,58 +806,52 @@ def run_gpu(args):
 # CPU oracle timing (the baseline arm)
 # ---------------------------------------------------------------------------
 
-def oracle_step_one_head(cpu, w, head=(0, 0)):
-    """The oracle on one (b, h) head of the step: returns its algorithmic FLOPs."""
+def oracle_forward_sample(cpu, w, stride=16, offset=0):
+    """The oracle's causal forward on every ``stride``-th query row of one head
+    (rows offset, offset+stride, ...) of the step's workload; returns the
+    algorithmic FLOPs of those rows (4d per allowed pair)."""
     import oracle
     from workloads import to_f64
-    b, h = head
-    q, k, v, do = (to_f64(cpu[n][b:b + 1, h:h + 1]) for n in ("q", "k", "v", "do"))
-    L, d = w.L, w.d
-    oracle.attention_forward(q, k, v, w.scale, causal=True)
-    states = []
-    for s, e in chunk_bounds(L, 8):
-        M = oracle.allowed_rows(np.arange(L), e - s, causal=True, k_offset=s)
-        states.append(oracle.partial_state(q[0, 0], k[0, 0, s:e], v[0, 0, s:e], w.scale, M))
-    oracle.merge_states(np.stack([x[0] for x in states]), np.stack([x[1] for x in states]),
-                        np.stack([x[2] for x in states]))
-    rp, ci = local_global_random_blocklist((L + 127) // 128, seed=2)
-    oracle.attention_forward(q, k, v, w.scale, causal=True, block=128, row_ptr=rp, col_idx=ci)
-    oracle.attention_backward(q, k, v, do, w.scale, causal=True)
-    pairs = causal_pairs(L, L)
-    sp, _ = sparse_counts(L, rp, ci, True)
-    return 4 * d * pairs * 2 + 4 * d * sp + 10 * d * pairs
+    q, k, v = (to_f64(cpu[n][0:1, 0:1]) for n in ("q", "k", "v"))
+    rows = np.arange(offset % stride, w.L, stride)
+    oracle.attention_forward(q, k, v, w.scale, causal=True, rows=rows)
+    return 4 * w.d * int((rows + 1).sum())
 
 
-def cpu_baseline(step_sample_seconds=20.0):
-    w = CAUSAL_4K
-    cpu = make_inputs(Workload(w.name, 1, 1, w.L, w.d, True, w.seed, backward=True))
+def _oracle_inputs(w):
+    return make_inputs(Workload(w.name, 1, 1, w.L, w.d, True, w.seed))
+
+
+def cpu_baseline(sample_seconds=15.0):
+    w = STEP_WORKLOAD
+    cpu = _oracle_inputs(w)
     t0 = time.time()
     flops = 0
     n = 0
     while True:
-        flops += oracle_step_one_head(cpu, w)
+        flops += oracle_forward_sample(cpu, w, offset=n)
         n += 1
-        if time.time() - t0 >= step_sample_seconds or n >= 8:
+        if time.time() - t0 >= sample_seconds or n >= 16:
             break
     dt = time.time() - t0
     return {"value": round(flops / dt / 1e12, 6), "unit": UNIT,
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"{n} x one head (B=1,H=1) of the step workload L={w.L} d={w.d}: causal fwd, "
-                      f"8-chunk partial+merge, block-sparse fwd, bwd; fp64 numpy, {dt:.1f} s"}
+            "sample": f"{n} x every 16th query row (1024 rows) of one head (B=1, H=1) of the "
+                      f"step's workload L={w.L} d={w.d}: causal forward, fp64 numpy, {dt:.1f} s"}
 
 
 def run_reference(args):
     rank, world, _ = dist_setup()
     if rank != 0:
         return
-    w = CAUSAL_4K
-    cpu = make_inputs(Workload(w.name, 1, 1, w.L, w.d, True, w.seed, backward=True))
-    for _ in range(args.warmup):
-        oracle_step_one_head(cpu, w)
+    w = STEP_WORKLOAD
+    cpu = _oracle_inputs(w)
+    for i in range(args.warmup):
+        oracle_forward_sample(cpu, w, offset=i)
     t0 = time.time()
     flops = 0
-    for _ in range(args.steps):
-        flops += oracle_step_one_head(cpu, w)
+    for i in range(args.steps):
+        flops += oracle_forward_sample(cpu, w, offset=i)
     dt = time.time() - t0
     value = flops / dt / 1e12
     out = {
@@ -793,22 +869,29 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic: torch.randn seeded, rounded to bf16, upcast to fp64",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "causal": True,
-                   "sample_per_step": "one head (b=0, h=0) of the workload through every row",
+                   "sample_per_step": "every 16th query row (1024 rows) of one head (B=1, H=1) "
+                                      "drawn like the workload; causal forward",
                    "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT,
                          "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-                         "sample": "one head per step of the L=4096 d=128 causal workload: fwd, "
-                                   "8-chunk partial+merge, block-sparse fwd, bwd (fp64 numpy)"},
+                         "sample": "per step, every 16th query row of one L=16384 d=128 head: "
+                                   "the oracle's causal forward (fp64 numpy)"},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out), flush=True)
 
 
+PROFILE_CASES = ("fwd", "fwd16k", "sparse", "sparse16k", "sparse_bwd", "bwd", "bwd16k", "fwd64",
+                 "bwd64", "partial", "merge", "splitkv", "splitkv16k", "select", "decode")
+
+
 def run_profile_case(kind: str):
-    """One kernel of the bench step on the step's own workload (causal B=4 H=16
-    L=4096 d=128, inputs 268 MB > L2), or the L=16384 target shape, for ncu:
-    one warm-up launch and one measured launch."""
+    """One kernel on one workload, for ncu: two launches (a warm-up and a
+    measured one).  Unsuffixed cases use the causal B=4 H=16 L=4096 d=128
+    workload (inputs 268 MB > L2); "16k" cases the bench step's B=2 H=16
+    L=16384 d=128 workload; "sparse_bwd" the block-sparse L'=16320 workload;
+    "fwd64"/"bwd64" the B=8 H=16 L=8192 d=64 workload."""
     import block_sparse_softmax_gb300 as bss
     bss.library()
     dev = torch.device("cuda", 0)
@@ -829,26 +912,40 @@ def run_profile_case(kind: str):
         fn = lambda: bss.attn_select_blocks(x["q"], x["k"], 4, local_blocks=4, causal=True,
                                             n_lists=w.B * w.H, scale=w.scale)
         return _run_profile_fn(kind, fn)
-    w = CAUSAL_16K if kind == "fwd16k" else CAUSAL_4K
+    if kind in ("fwd16k", "sparse16k", "bwd16k", "splitkv16k"):
+        w = CAUSAL_16K
+    elif kind == "sparse_bwd":
+        w = SPARSE_16K
+    elif kind in ("fwd64", "bwd64"):
+        w = BWD_8K
+    else:
+        w = CAUSAL_4K
     w = Workload(w.name, w.B, w.H, w.L, w.d, True, w.seed, backward=True)
     x = {k: t.to(dev) for k, t in make_inputs(w).items()}
-    if kind in ("fwd", "fwd16k"):
+    base = kind.replace("16k", "").replace("64", "")
+    if base == "fwd":
         fn = lambda: bss.attn_fwd(x["q"], x["k"], x["v"], causal=True, scale=w.scale)
-    elif kind == "sparse":
+    elif base in ("sparse", "sparse_bwd"):
         rp, ci = local_global_random_blocklist(w.n_blocks, seed=2)
         rpd, cid = torch.from_numpy(rp).to(dev), torch.from_numpy(ci).to(dev)
         fn = lambda: bss.attn_fwd_blocksparse(x["q"], x["k"], x["v"], rpd, cid, causal=True,
                                               scale=w.scale)
-    elif kind == "bwd":
+        if base == "sparse_bwd":
+            o, lse = fn()
+            ws = torch.empty(bss.attn_bwd_blocksparse_workspace_bytes(w.B, w.H, w.L, w.d),
+                             device=dev, dtype=torch.uint8)
+            fn = lambda: bss.attn_bwd_blocksparse(x["q"], x["k"], x["v"], o, lse, x["do"], rpd,
+                                                  cid, causal=True, scale=w.scale, workspace=ws)
+    elif base == "bwd":
         o, lse = bss.attn_fwd(x["q"], x["k"], x["v"], causal=True, scale=w.scale)
         fn = lambda: bss.attn_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], causal=True,
                                   scale=w.scale)
-    elif kind == "splitkv":
+    elif base == "splitkv":
         ws = torch.empty(bss.attn_fwd_splitkv_workspace_bytes(w.B, w.H, w.L, w.L, w.d, 8),
                          device=dev, dtype=torch.uint8)
         fn = lambda: bss.attn_fwd_splitkv(x["q"], x["k"], x["v"], 8, causal=True,
                                           scale=w.scale, workspace=ws)
-    elif kind in ("partial", "merge"):
+    elif base in ("partial", "merge"):
         bounds = chunk_bounds(w.L, 8)
         kc = [x["k"][:, :, s:e].contiguous() for s, e in bounds]
         vc = [x["v"][:, :, s:e].contiguous() for s, e in bounds]
@@ -861,7 +958,7 @@ def run_profile_case(kind: str):
             for c, (s, _) in enumerate(bounds):
                 bss.attn_fwd_partial(x["q"], kc[c], vc[c], causal=True, scale=w.scale,
                                      k_offset=s, m=m[c], l=l_[c], acc=acc[c])
-        if kind == "partial":
+        if base == "partial":
             fn = partials
         else:
             partials()
@@ -884,9 +981,7 @@ def _run_profile_fn(kind: str, fn):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--profile", choices=["fwd", "fwd16k", "sparse", "bwd", "partial", "merge",
-                                            "splitkv", "select", "decode"],
-                    default=None,
+    ap.add_argument("--profile", choices=PROFILE_CASES, default=None,
                     help="run one small case of one kernel (for ncu) and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
@@ -894,7 +989,7 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--quick", action="store_true", help="skip the per-workload measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

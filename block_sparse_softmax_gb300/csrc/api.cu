@@ -180,6 +180,29 @@ attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int
   }
   if (static_cast<long long>(p.n_chunks) * B * H * p.n_pairs > 0x7FFFFFFFll) return ATTN_ERR_UNSUPPORTED;
   p.n_items = p.n_chunks * B * H * p.n_pairs;
+  // Items in groups of query heads whose K and V (4 Lk d bytes per K/V head)
+  // take about 64 MiB, so that the K/V tiles the running items stream stay in
+  // L2 (which holds 129 MB): whole sets of the query heads that share a K/V
+  // head, at least two waves of items per group on the 152 SMs, and groups of
+  // nearly equal size (a small last group would start its longest items
+  // late and leave a tail).  Measured: at B=2 H=16 L=16384 the DRAM reads
+  // fell from 5x to 1.3x the algorithmic bytes at the same speed, and the
+  // 8-chunk split of B=1 H=8 L=131072 ran 6 % faster; 32 MiB groups were
+  // 6 % slower at L=16384.
+  {
+    const long long G = H / Hkv;
+    const long long kvh = static_cast<long long>(B) * Hkv;
+    const long long kv_bytes = 4ll * (Lk > 0 ? Lk : 1) * d;
+    long long g_kv = (64ll << 20) / kv_bytes;
+    const long long per_kv_items = static_cast<long long>(p.n_chunks) * p.n_pairs * G;
+    const long long min_kv = (2ll * 152 + per_kv_items - 1) / per_kv_items;
+    if (g_kv < min_kv) g_kv = min_kv;
+    if (g_kv < 1) g_kv = 1;
+    long long n_groups = (kvh + g_kv / 2) / g_kv;          // nearest whole number of groups
+    if (n_groups < 1) n_groups = 1;
+    g_kv = (kvh + n_groups - 1) / n_groups;
+    p.head_group = static_cast<int>(g_kv * G);
+  }
 #ifdef BSS_TRACE
   p.trace = g_trace_buf;
   p.trace_cta = g_trace_cta;

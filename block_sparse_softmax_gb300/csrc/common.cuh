@@ -163,6 +163,7 @@ struct FwdParams {
   int n_chunks;            // key chunks, each with its own partial state (1: none)
   int chunk_len;           // keys per chunk (a multiple of 128 when n_chunks > 1)
   int n_items;             // work items (= CTAs launched): n_chunks * B * H * n_pairs
+  int head_group;          // query heads whose items are numbered together (fwd_item)
   int* err;
   long long* trace;        // trace builds only (nullptr otherwise)
   int trace_cta;

@@ -131,9 +131,10 @@ struct FwdRegs {
 };
 
 // One work item: two consecutive 128-row query tiles of one (b, h), which
-// share a single K/V stream.  Items are numbered row-pair-major with every
-// head of a pair side by side; under a causal mask the last pair (whose rows
-// see the most keys) comes first, so that the longest items start first.
+// share a single K/V stream.  Items are numbered by fwd_item below: in groups
+// of heads, row-pair-major inside a group with every head of a pair side by
+// side; under a causal mask the last pair (whose rows see the most keys) comes
+// first, so that the longest items start first.
 struct FwdItem {
   int b, h, bh;
   int hkv;         // K/V head read by query head h
@@ -153,18 +154,27 @@ struct FwdItem {
   bool alt;
 };
 
-// Items are numbered row-pair-major, then key chunk, then head: under a
-// causal mask the last pair (whose rows see the most keys) comes first, and
-// the heads of one pair and chunk sit side by side.
+// Items come in groups of p.head_group query heads (every group but the last
+// full).  Inside a group they are numbered row-pair-major, then key chunk,
+// then head: under a causal mask the last pair (whose rows see the most keys)
+// comes first, and the heads of one pair and chunk sit side by side.  The
+// items running at any moment then read the K and V of one group's heads,
+// which the host sizes to stay in L2, instead of streaming every head's K and
+// V through it.
 template <bool CAUSAL, bool ALT>
 __device__ __forceinline__ FwdItem fwd_item(int item, const FwdParams& p) {
   FwdItem it;
   const int BH = p.B * p.H;
-  const int per_rank = BH * p.n_chunks;
-  const int rank = item / per_rank;
-  const int rem = item - rank * per_rank;
-  it.c = rem / BH;
-  it.bh = rem - it.c * BH;
+  const int gh = p.head_group;
+  const int per_group = gh * p.n_chunks * p.n_pairs;
+  const int grp = item / per_group;
+  const int gsz = min(gh, BH - grp * gh);
+  const int within = item - grp * per_group;
+  const int per_rank = gsz * p.n_chunks;
+  const int rank = within / per_rank;
+  const int rem = within - rank * per_rank;
+  it.c = rem / gsz;
+  it.bh = grp * gh + (rem - it.c * gsz);
   it.b = it.bh / p.H;
   it.h = it.bh - it.b * p.H;
   it.hkv = it.h / (p.H / p.Hkv);

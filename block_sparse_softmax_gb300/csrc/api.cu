@@ -198,6 +198,9 @@ attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int
     const long long min_kv = (2ll * 152 + per_kv_items - 1) / per_kv_items;
     if (g_kv < min_kv) g_kv = min_kv;
     if (g_kv < 1) g_kv = 1;
+    // a block-sparse launch reads only the listed blocks: all heads side by
+    // side (grouping measured 5 % slower there)
+    if (sparse) g_kv = kvh;
     long long n_groups = (kvh + g_kv / 2) / g_kv;          // nearest whole number of groups
     if (n_groups < 1) n_groups = 1;
     g_kv = (kvh + n_groups - 1) / n_groups;

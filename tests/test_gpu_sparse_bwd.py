@@ -199,3 +199,62 @@ def test_sparse_16k_full_size_sampled(bss):
             assert np.abs(dk[b, h, sl].double().cpu().numpy() - gk).max() <= TOL_GRAD
             assert np.abs(dv[b, h, sl].double().cpu().numpy() - gv).max() <= TOL_GRAD
             assert np.abs(dq[b, h, rows].double().cpu().numpy() - gq).max() <= TOL_GRAD
+
+
+def _global_at(n, g, seed):
+    """Raw CSR of the local + global + random pattern with the global block at
+    g instead of 0 (rows before g list it too: under a causal mask it lies in
+    their future and contributes nothing)."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for a in range(n):
+        row = [a - t for t in range(4) if a - t >= 0] + [g]
+        if a >= 1:
+            row += [int(rng.integers(0, a)) for _ in range(2)]
+        rows.append(row)
+    rp = np.zeros(n + 1, np.int32)
+    for a, r in enumerate(rows):
+        rp[a + 1] = rp[a] + len(r)
+    return rp, np.array([c for r in rows for c in r], np.int32)
+
+
+def test_long_columns_first_with_per_group_lists(bss):
+    """Lists per K/V head whose global block (listed by every row) differs, so
+    that each list has one key column far longer than the mean: the backward
+    launches those key tiles first.  B=1, H=4 query heads over 2 K/V heads,
+    L=4096 (32 blocks), causal, d=64; every gradient against the oracle with
+    each head's own list, dK and dV summed over the heads of a group."""
+    L, d, H, Hkv = 4096, 64, 4, 2
+    n = L // 128
+    lists = [_global_at(n, 0, seed=5), _global_at(n, 9, seed=6)]
+    rp = np.zeros((2, n + 1), np.int32)
+    rp[0] = lists[0][0]
+    rp[1] = lists[1][0] + len(lists[0][1])
+    ci = np.concatenate([lists[0][1], lists[1][1]]).astype(np.int32)
+    w = Workload("lc", 1, H, L, d, True, seed=77, backward=True, Hkv=Hkv)
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    _, _, dq, dk, dv, _ = _fwd_bwd(bss, inp, rp, ci, True, w.scale)
+    stats = bss.attn_blocklist_stats(rp, ci, L, causal=True).cpu().tolist()
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    for li, (r, c) in enumerate(lists):
+        s = oracle.blocklist_stats(r, c, L, causal=True)
+        assert stats[li] == [s["listed"], s["executed"], s["future"], s["pairs"]]
+    assert stats[1][2] == 9                       # rows 0..8 list the future block 9
+    q, k, v, do = (to_f64(cpu[x]) for x in ("q", "k", "v", "do"))
+    G = H // Hkv
+    dk_ref = np.zeros_like(k)
+    dv_ref = np.zeros_like(v)
+    for h in range(H):
+        r, c = lists[h // G]
+        M = oracle.allowed_mask(L, L, causal=True, block=128, row_ptr=r, col_idx=c)
+        gq, gk, gv, _ = oracle.backward_head(q[0, h], k[0, h // G], v[0, h // G], do[0, h],
+                                             w.scale, M)
+        err = np.abs(dq[0, h].double().cpu().numpy() - gq).max()
+        assert err <= TOL_GRAD, f"head {h}: max|ddq| = {err:.3e}"
+        dk_ref[0, h // G] += gk
+        dv_ref[0, h // G] += gv
+    for name, g, ref in (("dk", dk, dk_ref), ("dv", dv, dv_ref)):
+        err = np.abs(g.double().cpu().numpy() - ref).max()
+        assert err <= TOL_GRAD, f"max|d{name}| = {err:.3e}"

@@ -101,6 +101,8 @@ struct FwdCfg {
   static constexpr int kXchBytes = 3 * kTileM * 4;
   static constexpr int kBitmapRegion =
       2 * kBitmapWords * 4 > kXchBytes ? 2 * kBitmapWords * 4 : kXchBytes;
+  static_assert(2 * kBitmapWords * 4 + 16 <= kBitmapRegion,
+                "the block-sparse row bounds follow the bitmaps inside their region");
   static constexpr int kSmemBytes = kBitmapOff + kBitmapRegion + 1024;
   static_assert(kSmemBytes <= 232448, "forward shared memory exceeds the 227 KB a CTA may use");
   static constexpr uint32_t kTmemCols = 512;
@@ -297,6 +299,21 @@ __global__ void __launch_bounds__(384, 1)
   if (*reinterpret_cast<volatile int*>(p.err) == ATTN_ERR_TIMEOUT) return;
 
   // ---- set-up: barriers, tensor memory, block-sparse bitmaps -------------
+  // A block-sparse CTA runs one item.  Its two CSR row bounds are read first
+  // (into shared memory past the bitmaps) and its two Q tiles are loaded as
+  // soon as the barriers exist, so that both latencies overlap the rest of
+  // the set-up instead of preceding the first key block.
+  int* rp_s = reinterpret_cast<int*>(smem + C::kBitmapOff) + 2 * C::kBitmapWords;
+  if (SPARSE && tid < 4) {
+    const FwdItem it0 = fwd_item<CAUSAL, kAlt>(blockIdx.x, p);
+    const int t = tid >> 1;
+    const int qb = it0.r0[t] / kTileM;
+    int v = INT_MIN;                             // no such query block
+    if (it0.r0[t] < p.Lq && qb < p.n_qblk)
+      v = __ldg(p.row_ptr + static_cast<size_t>(it0.bh / p.heads_per_list) * (p.n_qblk + 1) + qb +
+                (tid & 1));
+    rp_s[tid] = v;
+  }
   if (tid == 0) {
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kBarQFull + t), 1);
@@ -322,6 +339,17 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar(C::kBarXEmpty), 4 * 32);
     *abort_flag = 0;
     fence_barrier_init();
+    if (SPARSE) {
+      // both Q tiles of the item (a tile past Lq reads the zero fill)
+      const FwdItem it0 = fwd_item<CAUSAL, kAlt>(blockIdx.x, p);
+      for (int t = 0; t < 2; ++t) {
+        const uint32_t qs = sbase + C::kQOff + t * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_4d(qs + c * C::kChunkBytes, &tmQ, bar(C::kBarQFull + t), c * 64, it0.r0[t], it0.h,
+                      it0.b);
+      }
+    }
   }
   if (warp == 0) {
     tmem_alloc(sbase + C::kTmemSlotOff, C::kTmemCols);
@@ -329,17 +357,14 @@ __global__ void __launch_bounds__(384, 1)
   }
   BSS_TRACE_EV(p, tr && tid == 0, 6, 0);
   if (SPARSE) {
-    const FwdItem it0 = fwd_item<CAUSAL, kAlt>(blockIdx.x, p);
     const int nk = (p.Lk + kTileN - 1) / kTileN;
     for (int i = tid; i < 2 * C::kBitmapWords; i += C::kThreads) bitmap[i] = 0u;
     __syncthreads();
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const int qb = it0.r0[t] / kTileM;
-      if (it0.r0[t] >= p.Lq || qb >= p.n_qblk) continue;
-      const int* rp = p.row_ptr + static_cast<size_t>(it0.bh / p.heads_per_list) * (p.n_qblk + 1);
-      const int beg = __ldg(rp + qb);
-      const int end = __ldg(rp + qb + 1);
+      const int beg = rp_s[2 * t];
+      const int end = rp_s[2 * t + 1];
+      if (beg == INT_MIN) continue;              // no such query block
       if (beg < 0 || end < beg || end > p.nnz) {
         if (tid == 0) record_error(p.err, ATTN_ERR_BAD_BLOCKLIST);
         continue;
@@ -370,7 +395,8 @@ __global__ void __launch_bounds__(384, 1)
       int item = static_cast<int>(blockIdx.x);
       int n = 0;              // items finished
       int ik = 0, iv = 0;     // K and V tiles loaded (over all items)
-      int qn[2] = {0, 0};     // Q tiles loaded into each tile slot
+      int qn[2] = {SPARSE ? 1 : 0, SPARSE ? 1 : 0};   // Q tiles loaded into each tile slot
+                              // (a block-sparse CTA's two were loaded at set-up)
       int clc_k = 0;          // cancel requests answered
       bool clc_live = !SPARSE;
       bool clc_out = false;   // a cancel request is in flight
@@ -384,7 +410,7 @@ __global__ void __launch_bounds__(384, 1)
       while (ok) {
         const FwdItem it = fwd_item<CAUSAL, kAlt>(item, p);
         const Schedule sch(it, sched_bm, C::kBitmapWords);
-        bool qloaded[2] = {false, false};
+        bool qloaded[2] = {SPARSE, SPARSE};
         for (int kb = sch.next(-1); kb >= 0;) {
           const int nkb = sch.next(kb);
           // The next item is asked for as this item's last block is loaded.
@@ -1120,12 +1146,14 @@ cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUte
                        const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                        cudaStream_t st) {
   // The alternating schedule of single-tile pairs is compiled into every dense
-  // kernel without a partial output; the partial-state kernels have a second
-  // instantiation without it, which launches with full pairs only run.  A
-  // launch whose query rows fit one tile (decoding) runs the instantiation
-  // with a single Q buffer and one more K stage.
+  // kernel; a launch whose pairs are all full runs an instantiation without
+  // it (partial states, and the bf16 output at d=128, where that copy
+  // compiles without register spills and measured 1.7 % faster; at d=64 the
+  // copy with the path measured faster and serves every launch).  A launch
+  // whose query rows fit one tile (decoding) runs the instantiation with a
+  // single Q buffer and one more K stage.
   const bool single_tile_pair = (p.Lq % (2 * kTileM)) != 0 && (p.Lq % (2 * kTileM)) <= kTileM;
-  const bool alt = !sparse && (!partial || single_tile_pair);
+  const bool alt = !sparse && (single_tile_pair || (!partial && d == 64));
   const bool dec = alt && p.Lq >= 1 && p.Lq <= kTileM;
 #define BSS_FWD_CASE(DD, CA, SP, PA, AL, DE)                                              \
   if (d == DD && causal == CA && sparse == SP && partial == PA && alt == AL && dec == DE) \
@@ -1133,6 +1161,8 @@ cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUte
 #define BSS_FWD_CASE_D(DD, CA, SP, PA, AL) \
   BSS_FWD_CASE(DD, CA, SP, PA, AL, false)  \
   BSS_FWD_CASE(DD, CA, SP, PA, AL, true)
+  BSS_FWD_CASE(128, false, false, false, false, false)
+  BSS_FWD_CASE(128, true, false, false, false, false)
   BSS_FWD_CASE_D(64, false, false, false, true)
   BSS_FWD_CASE_D(64, true, false, false, true)
   BSS_FWD_CASE_D(128, false, false, false, true)

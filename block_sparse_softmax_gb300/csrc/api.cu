@@ -186,7 +186,7 @@ attn_status_t fwd_common(const void* q, const void* k, const void* v, int B, int
   // head, at least two waves of items per group on the 152 SMs, and groups of
   // nearly equal size (a small last group would start its longest items
   // late and leave a tail).  Measured: at B=2 H=16 L=16384 the DRAM reads
-  // fell from 5x to 1.3x the algorithmic bytes at the same speed, and the
+  // fell from 5x to 1.5x the algorithmic bytes at the same speed, and the
   // 8-chunk split of B=1 H=8 L=131072 ran 6 % faster; 32 MiB groups were
   // 6 % slower at L=16384.
   {

@@ -16,8 +16,8 @@
 //     once and one item's epilogue overlaps the next item's loads and MMAs;
 //   * warp 0 issues TMA loads (128-byte swizzled boxes of 128 rows x 64 d) into
 //     a ring of K and V stages and schedules items; warp 1 (one thread) issues
-//     every tcgen05.mma (block-sparse: warps 1 and 2, one per tile slot);
-//     warpgroups 1 and 2 (warps 4-7, 8-11) run the online
+//     every tcgen05.mma; in a block-sparse launch warp 3 claims the next item
+//     and builds its bitmaps; warpgroups 1 and 2 (warps 4-7, 8-11) run the online
 //     softmax and the epilogue of tile 0 and tile 1, one thread per query row
 //     (TMEM lane = row), with a larger register budget handed over from
 //     warpgroup 0 (setmaxnreg);
@@ -38,25 +38,21 @@
 //     keeps the result exact because l and A always share the same reference m;
 //   * causal: blocks wholly in the future are never visited, the element mask
 //     is applied only where a block crosses the diagonal or the sequence end;
-//   * block-sparse: each CTA turns its two CSR rows into bitmaps in shared
-//     memory (duplicates collapse, order is irrelevant) and visits the union,
-//     each tile computing only the blocks of its own list.
+//   * block-sparse: an item's two CSR rows become bitmaps in shared memory
+//     (duplicates collapse, order is irrelevant); every role visits the union
+//     in ascending order, each tile computing only the blocks of its own list.
+//     Two bitmap buffers let the next item's be built while the current item
+//     runs.
 #include "common.cuh"
 
 namespace bss {
 namespace {
 
-// Compile-time tile slot for the per-slot MMA issuers.
-template <int T>
-struct SlotTag {
-  static constexpr int value = T;
-};
-
 // DEC: every query block is a single tile (Lq <= 128, decoding).  Both tile
 // slots then compute on the same query rows, so one Q buffer serves both and
 // the second becomes one more K stage (deeper key prefetch for a stream that
 // is bound by memory latency rather than by the tensor core).
-template <int D, bool DEC = false>
+template <int D, bool DEC = false, bool SPARSE = false>
 struct FwdCfg {
   static constexpr int kChunks = D / 64;                   // 128-byte swizzle atoms across d
   static constexpr int kChunkBytes = kTileM * 128;         // 128 rows x 128 bytes
@@ -86,7 +82,8 @@ struct FwdCfg {
   static constexpr int kBarMmaDone = kBarClc + 1;
   static constexpr int kBarXFull = kBarMmaDone + 1;    // tile 1's row state handed over
   static constexpr int kBarXEmpty = kBarXFull + 1;     // ... and read by tile 0
-  static constexpr int kNumBars = kBarXEmpty + 1;
+  static constexpr int kBarBmEmpty = kBarXEmpty + 1;   // [2] an item's bitmaps walked by every role
+  static constexpr int kNumBars = kBarBmEmpty + (SPARSE ? 2 : 0);
   // 16-byte aligned: cancel answer (16) | TMEM base | abort flag | next item [2]
   static constexpr int kMiscOff = (kBarOff + kNumBars * 8 + 15) & ~15;
   static constexpr int kClcOff = kMiscOff;
@@ -97,12 +94,21 @@ struct FwdCfg {
   static constexpr int kBitmapOff = kMiscOff + 32;
   // A dense launch has no bitmaps; the same bytes carry the (m, mt, l) rows
   // one softmax warpgroup hands to the other (three arrays of 128 floats).
+  // A block-sparse launch keeps the bitmaps of two items there (two per item,
+  // one word per 32 key blocks of the launch) and, in the region's last 16
+  // bytes, the first item's CSR row bounds.  Its region takes what the 227 KB
+  // leave, up to four bitmaps of the largest key range.  (The dense kernels
+  // keep their own smaller layout: the block-sparse barriers and region in
+  // them measured 0.9 % slower at L=16384, for no use.)
   static constexpr int kXchOff = kBitmapOff;
   static constexpr int kXchBytes = 3 * kTileM * 4;
+  static constexpr int kRegionFree = 232448 - 1024 - kBitmapOff;
+  static constexpr int kRegionWanted = 4 * kBitmapWords * 4 + 16;
   static constexpr int kBitmapRegion =
-      2 * kBitmapWords * 4 > kXchBytes ? 2 * kBitmapWords * 4 : kXchBytes;
-  static_assert(2 * kBitmapWords * 4 + 16 <= kBitmapRegion,
-                "the block-sparse row bounds follow the bitmaps inside their region");
+      !SPARSE ? kXchBytes : (kRegionFree < kRegionWanted ? kRegionFree : kRegionWanted);
+  static_assert(kBitmapRegion >= kXchBytes &&
+                    (!SPARSE || kBitmapRegion >= 2 * kBitmapWords * 4 + 16),
+                "one item's bitmaps and the row bounds (or the exchanged rows) must fit");
   static constexpr int kSmemBytes = kBitmapOff + kBitmapRegion + 1024;
   static_assert(kSmemBytes <= 232448, "forward shared memory exceeds the 227 KB a CTA may use");
   static constexpr uint32_t kTmemCols = 512;
@@ -111,19 +117,22 @@ struct FwdCfg {
   static constexpr uint32_t kColO = 256;                    // O_t at 256 + t*D
   static constexpr int kThreads = 384;
   // Readers of each next-item slot: the MMA thread and one lane of each of the
-  // eight softmax warps (one more MMA thread in a block-sparse launch).
+  // eight softmax warps (and the producer in a block-sparse launch, where
+  // warp 3 writes the slots).
   static constexpr int kItemReaders = 1 + 8;
 };
 
 // Register split per warpgroup (setmaxnreg): warpgroup 0 (TMA and scheduler,
-// MMA, two idle warps) gets kLow registers a thread, the two softmax warpgroups
+// MMA, an idle warp, and warp 3: idle, or preparing block-sparse items) gets
+// kLow registers a thread, the two softmax warpgroups
 // kHigh.  Each SM sub-partition holds one warp of every warpgroup, so
 // kLow + 2 kHigh must stay within its 512 registers a lane, and the whole
 // split within the 384 * 168 registers the launch holds (launch_one refuses
 // to launch if ptxas gave the kernel fewer than 168 a thread, which would
 // leave setmaxnreg.inc waiting for registers that never come).  The
 // block-sparse instantiations take the same split: with 152/176 their
-// softmax warpgroups spilled, and 136/184 measured 3.5 % faster.
+// softmax warpgroups spilled, and 136/184 measured 3.5 % faster.  Their
+// producer's Q loads for later items spill a few bytes (8 at d=128).
 template <bool SPARSE>
 struct FwdRegs {
   static constexpr uint32_t kLow = 136;
@@ -268,16 +277,18 @@ struct Schedule {
 // item's Q and K loads and S = Q K^T overlapping the previous item's epilogue,
 // and the items handed out greedily in order (longest first under a causal
 // mask).  The producer passes each next item index to the other roles through
-// a two-slot ring in shared memory.  A block-sparse launch runs one item per
-// CTA (its bitmaps are built per item at set-up).
+// a two-slot ring in shared memory.  In a block-sparse launch warp 3 takes the
+// producer's part in this: it claims the next item as soon as a bitmap buffer
+// is free (about one item ahead), builds the item's bitmaps there and writes
+// the ring, so that the producer finds the next item ready when it reaches
+// the end of the current one.
 template <int D, bool CAUSAL, bool SPARSE, bool PARTIAL, bool ALT, bool DEC>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   constexpr bool kAlt = ALT && !SPARSE;   // single-tile pairs may alternate
   constexpr bool kDec = DEC && kAlt;      // one Q buffer for both slots
-  constexpr int kIssuers = SPARSE ? 2 : 1; // MMA-issuing threads (one per tile slot when 2)
-  using C = FwdCfg<D, kDec>;
+  using C = FwdCfg<D, kDec, SPARSE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -288,7 +299,6 @@ __global__ void __launch_bounds__(384, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kAbortOff);
   volatile int* next_item = reinterpret_cast<volatile int*>(smem + C::kNextItemOff);
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(smem + C::kBitmapOff);
-  const uint32_t* sched_bm = SPARSE ? bitmap : nullptr;
 
   const int warp = static_cast<int>(warp_id());
   const int lane = static_cast<int>(lane_id());
@@ -300,11 +310,20 @@ __global__ void __launch_bounds__(384, 1)
   if (*reinterpret_cast<volatile int*>(p.err) == ATTN_ERR_TIMEOUT) return;
 
   // ---- set-up: barriers, tensor memory, block-sparse bitmaps -------------
-  // A block-sparse CTA runs one item.  Its two CSR row bounds are read first
-  // (into shared memory past the bitmaps) and its two Q tiles are loaded as
-  // soon as the barriers exist, so that both latencies overlap the rest of
-  // the set-up instead of preceding the first key block.
-  int* rp_s = reinterpret_cast<int*>(smem + C::kBitmapOff) + 2 * C::kBitmapWords;
+  // A block-sparse CTA builds its first item's bitmaps here.  The item's two
+  // CSR row bounds are read first (into the last 16 bytes of the bitmap
+  // region) and its two Q tiles are loaded as soon as the barriers exist, so
+  // that both latencies overlap the rest of the set-up instead of preceding
+  // the first key block.  Later items' bitmaps come from warp 3, in the other
+  // of two buffers (bw words a bitmap); a key range too long for two buffers
+  // runs one item per CTA.
+  const int bw = SPARSE ? ((p.Lk + kTileN - 1) / kTileN + 31) >> 5 : 0;
+  const bool persist_sparse = SPARSE && 16 * bw + 16 <= C::kBitmapRegion;
+  int* rp_s = reinterpret_cast<int*>(smem + C::kBitmapOff + C::kBitmapRegion - 16);
+  // the bitmaps of the n-th item a CTA runs (nullptr: a dense key range)
+  auto item_bm = [&](int n) -> const uint32_t* {
+    return SPARSE ? bitmap + (n & 1) * 2 * bw : nullptr;
+  };
   if (SPARSE && tid < 4) {
     const FwdItem it0 = fwd_item<CAUSAL, kAlt>(blockIdx.x, p);
     const int t = tid >> 1;
@@ -325,17 +344,19 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(bar(C::kBarOEmpty + t), 4 * 32);
       mbar_init(bar(C::kBarItemFull + t), 1);
       mbar_init(bar(C::kBarItemEmpty + t), C::kItemReaders + (SPARSE ? 1 : 0));
+      // producer, MMA thread, one lane of each softmax warp
+      if (SPARSE) mbar_init(bar(C::kBarBmEmpty + t), 1 + 1 + 8);
     }
     for (int s = 0; s < C::kStagesK; ++s) {
       mbar_init(bar(C::kBarKFull + s), 1);
-      mbar_init(bar(C::kBarKEmpty + s), kIssuers);
+      mbar_init(bar(C::kBarKEmpty + s), 1);
     }
     for (int s = 0; s < C::kStagesV; ++s) {
       mbar_init(bar(C::kBarVFull + s), 1);
-      mbar_init(bar(C::kBarVEmpty + s), kIssuers);
+      mbar_init(bar(C::kBarVEmpty + s), 1);
     }
     mbar_init(bar(C::kBarClc), 1);
-    mbar_init(bar(C::kBarMmaDone), kIssuers);
+    mbar_init(bar(C::kBarMmaDone), 1);
     mbar_init(bar(C::kBarXFull), 4 * 32);
     mbar_init(bar(C::kBarXEmpty), 4 * 32);
     *abort_flag = 0;
@@ -359,7 +380,7 @@ __global__ void __launch_bounds__(384, 1)
   BSS_TRACE_EV(p, tr && tid == 0, 6, 0);
   if (SPARSE) {
     const int nk = (p.Lk + kTileN - 1) / kTileN;
-    for (int i = tid; i < 2 * C::kBitmapWords; i += C::kThreads) bitmap[i] = 0u;
+    for (int i = tid; i < 2 * bw; i += C::kThreads) bitmap[i] = 0u;
     __syncthreads();
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
@@ -376,7 +397,7 @@ __global__ void __launch_bounds__(384, 1)
           record_error(p.err, ATTN_ERR_BAD_BLOCKLIST);
           continue;
         }
-        atomicOr(bitmap + t * C::kBitmapWords + (c >> 5), 1u << (c & 31));
+        atomicOr(bitmap + t * bw + (c >> 5), 1u << (c & 31));
       }
     }
   }
@@ -410,8 +431,8 @@ __global__ void __launch_bounds__(384, 1)
       };
       while (ok) {
         const FwdItem it = fwd_item<CAUSAL, kAlt>(item, p);
-        const Schedule sch(it, sched_bm, C::kBitmapWords);
-        bool qloaded[2] = {SPARSE, SPARSE};
+        const Schedule sch(it, item_bm(n), bw);
+        bool qloaded[2] = {SPARSE && n == 0, SPARSE && n == 0};
         for (int kb = sch.next(-1); kb >= 0;) {
           const int nkb = sch.next(kb);
           // The next item is asked for as this item's last block is loaded.
@@ -468,6 +489,19 @@ __global__ void __launch_bounds__(384, 1)
           kb = nkb;
         }
         if (!ok) break;
+        if (SPARSE) {
+          // block-sparse: this item's bitmaps are walked; warp 3 has claimed
+          // and prepared the next item, which the ring holds
+          mbar_arrive(bar(C::kBarBmEmpty + (n & 1)));
+          const int s = n & 1;
+          if (!wait_bar(bar(C::kBarItemFull + s), (n >> 1) & 1, abort_flag, p.err)) break;
+          const int next = next_item[s];
+          mbar_arrive(bar(C::kBarItemEmpty + s));
+          ++n;
+          if (next < 0) break;
+          item = next;
+          continue;
+        }
         if (clc_live && !clc_out) request_item();   // an item without blocks
         int next = -1;
         if (clc_out) {
@@ -511,7 +545,7 @@ __global__ void __launch_bounds__(384, 1)
         if (qn[t] > 0) drain_bar(bar(C::kBarQFull + t), (qn[t] - 1) & 1);
       if (clc_out) drain_bar(bar(C::kBarClc), clc_k & 1);
     }
-  } else if (!SPARSE && warp == 1) {
+  } else if (warp == 1) {
     // =================== MMA issuer (one thread) ===================
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(kTileM, kTileN, false, false);
@@ -525,7 +559,7 @@ __global__ void __launch_bounds__(384, 1)
       bool ok = true;
       while (ok) {
         const FwdItem it = fwd_item<CAUSAL, kAlt>(item, p);
-        const Schedule sch(it, sched_bm, C::kBitmapWords);
+        const Schedule sch(it, item_bm(n), bw);
         const int lastkb[2] = {sch.last(0), sch.last(1)};
         bool qready[2] = {false, false};
         bool ostarted[2] = {false, false};
@@ -655,6 +689,26 @@ __global__ void __launch_bounds__(384, 1)
         }
         }
         if (!ok) break;
+        if (SPARSE) {
+          mbar_arrive(bar(C::kBarBmEmpty + (n & 1)));   // this item's bitmaps walked
+          // The first item's two Q tiles were loaded at set-up: a tile with no
+          // block in it hands its buffer back once the load has landed (so
+          // that the next item's Q load into it waits on the right phase).
+          bool qok = true;
+          if (n == 0) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              if (lastkb[t] < 0 && qok) {
+                qok = wait_bar(bar(C::kBarQFull + t), qn[t] & 1, abort_flag, p.err);
+                if (qok) {
+                  mbar_arrive(bar(C::kBarQEmpty + t));
+                  qready[t] = true;
+                }
+              }
+            }
+          }
+          if (!qok) break;
+        }
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           if (ostarted[t]) {
@@ -675,166 +729,102 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(bar(C::kBarMmaDone));
       drain_bar(bar(C::kBarMmaDone), 0);
     }
-  } else if (SPARSE && (warp == 1 || warp == 2)) {
-    // =================== block-sparse MMA issuers: warp 1 for tile slot 0, warp 2 for slot 1 ===================
-    // The two tiles of a block-sparse pair visit different key blocks, and a
-    // single issuer in strict alternation would make each tile wait for the
-    // other's hand-offs; one thread per slot issues that slot's tcgen05.mma
-    // instead (measured 6 % faster on the block-sparse workload, and slower
-    // on dense pairs, whose S groups then interleave with the other tile's).  Per slot the order is P V(j),
-    // then S(j+1): S(j+1) overwrites the columns that P V(j) reads, and one
-    // thread's MMAs execute in issue order.  The K/V stages are shared and
-    // read-only: each is released by both issuers (two arrivals), the one
-    // that computes on it by a commit, the other by a plain arrival made only
-    // after that stage's load has completed (so an arrival can never count
-    // towards the stage's previous use).
-    auto run_issuer = [&](auto tag) {
-      constexpr int T = decltype(tag)::value;
-      constexpr int q = kDec ? 0 : T;              // the Q buffer this slot reads
-      constexpr uint32_t kIdescQK = idesc_bf16_f32(kTileM, kTileN, false, false);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(kTileM, D, false, true);
-      int item = static_cast<int>(blockIdx.x);
-      int n = 0;                // items finished
-      int i = 0;                // key blocks walked (over all items)
-      int qn = 0;               // Q tiles of buffer q consumed
-      int pcount = 0;           // P tiles consumed
-      int on = 0;               // O accumulations handed to the epilogue
-      bool ok = true;
-      while (ok) {
-        const FwdItem it = fwd_item<CAUSAL, kAlt>(item, p);
-        const Schedule sch(it, sched_bm, C::kBitmapWords);
-        const int mylast = sch.last(T);
-        const int other_last = sch.last(1 - T);
-        const int qlast = mylast > other_last ? mylast : other_last;
-        bool qready = false;
-        bool ostarted = false;
-
-        auto wait_q = [&]() -> bool {
-          if (!qready) {
-            if (!wait_bar(bar(C::kBarQFull + q), qn & 1, abort_flag, p.err)) return false;
-            qready = true;
-          }
-          return true;
-        };
-        auto issue_qk = [&](int sk, int kb) -> bool {
-          if (!wait_q()) return false;
-          const uint64_t dq = sdesc_sw128(sbase + C::kQOff + q * C::kTileBytes, 16, 1024);
-          const uint64_t dk = sdesc_sw128(sbase + C::kKOff + sk * C::kTileBytes, 16, 1024);
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-            mma_ss(tmem + C::kColS + T * 128, sdesc_add(dq, off), sdesc_add(dk, off), kIdescQK,
-                   kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(C::kBarSFull + T));
-          // Q is free for the next item once this slot's last S lands (with a
-          // shared buffer, once both slots' last S land: two arrivals)
-          if (kb == mylast) mma_commit(bar(C::kBarQEmpty + q));
-          return true;
-        };
-        auto issue_pv = [&](int sv) -> bool {
-          if (!ostarted && on > 0) {
-            // O still holds the previous item's result until its epilogue read it
-            if (!wait_bar(bar(C::kBarOEmpty + T), (on - 1) & 1, abort_flag, p.err)) return false;
-            tc_fence_after();
-          }
-          const uint64_t dv = sdesc_sw128(sbase + C::kVOff + sv * C::kTileBytes, C::kChunkBytes, 1024);
-#pragma unroll
-          for (int kk = 0; kk < kTileN / 16; ++kk) {
-            mma_ts(tmem + C::kColO + T * D, tmem + C::kColS + T * 128 + C::kColP + kk * 8,
-                   sdesc_add(dv, kk * 16 * 128), kIdescPV, (ostarted || kk > 0) ? 1u : 0u);
-          }
-          ostarted = true;
-          return true;
-        };
-        // block j's K stage: S of this slot if it takes part, then the release
-        auto k_step = [&](int j, int kb, bool mine) -> bool {
-          const int sk = j % C::kStagesK;
-          if (!wait_bar(bar(C::kBarKFull + sk), (j / C::kStagesK) & 1, abort_flag, p.err)) return false;
-          tc_fence_after();
-          if (mine) {
-            if (!issue_qk(sk, kb)) return false;
-            BSS_TRACE_EV(p, tr && j > 0, 7, 4 * (j - 1) + 2 * T + 1);   // S of the next block issued
-            mma_commit(bar(C::kBarKEmpty + sk));
+  } else if (SPARSE && warp == 3) {
+    // =================== block-sparse item preparation (warp 3) ===================
+    // Item k (k >= 1) of this CTA: claimed by cluster launch control (the CTA
+    // cancels a not-yet-started CTA of the grid and takes its item), its two
+    // bitmaps built in buffer k & 1 from its CSR rows, and its index written
+    // to ring slot (k - 1) & 1, which every role reads at the end of item
+    // k - 1.  The buffer was last used by item k - 2, so the claim comes as
+    // soon as every role has walked that item: about one item ahead.  (A
+    // claim made only once the producer had issued item k - 1's loads left
+    // the producer waiting for the bitmaps and measured 4 % slower.)
+    const int nk = (p.Lk + kTileN - 1) / kTileN;
+    bool live = persist_sparse;   // false: every item claimed, or one item per CTA
+    int clc_k = 0;                // cancel requests answered
+    bool clc_out = false;         // a cancel request is in flight
+    for (int k = 1;; ++k) {
+      const int s = (k - 1) & 1;  // ring slot carrying item k
+      const int b = k & 1;        // bitmap buffer of item k
+      // the slot's previous entry (item k - 2) has been read by every role
+      if (k >= 3 && !__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarItemEmpty + s),
+                                                      (((k - 1) >> 1) & 1) ^ 1, abort_flag, p.err)))
+        break;
+      int next = -1;
+      if (live) {
+        // the buffer's previous item (k - 2) has been walked by every role
+        if (k >= 2 && !__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarBmEmpty + b),
+                                                        ((k - 2) >> 1) & 1, abort_flag, p.err)))
+          break;
+        int x = -1, got = 0, fail = 0;
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(bar(C::kBarClc), 16);
+          clc_try_cancel(sbase + C::kClcOff, bar(C::kBarClc));
+          clc_out = true;
+          if (!wait_bar(bar(C::kBarClc), clc_k & 1, abort_flag, p.err)) {
+            fail = 1;
           } else {
-            mbar_arrive(bar(C::kBarKEmpty + sk));
-          }
-          return true;
-        };
-        // block j's V stage: P V of this slot if it takes part, then the release
-        auto v_step = [&](int j, bool mine) -> bool {
-          const int sv = j % C::kStagesV;
-          if (!wait_bar(bar(C::kBarVFull + sv), (j / C::kStagesV) & 1, abort_flag, p.err)) return false;
-          if (T == 0) BSS_TRACE_EV(p, tr, 1, 4 * j);
-          if (mine) {
-            if (!wait_bar(bar(C::kBarPFull + T), pcount & 1, abort_flag, p.err)) return false;
-            ++pcount;
-            BSS_TRACE_EV(p, tr, 1, 4 * j + 1 + T);
-            tc_fence_after();
-            if (!issue_pv(sv)) return false;
-            BSS_TRACE_EV(p, tr, 7, 4 * j + 2 * T);             // P V of the slot issued
-            mma_commit(bar(C::kBarVEmpty + sv));
-          } else {
-            tc_fence_after();
-            mbar_arrive(bar(C::kBarVEmpty + sv));
-          }
-          return true;
-        };
-
-        if (kAlt && it.alt) {
-          // Each key block serves one slot (kb & 1): this slot's S of its
-          // first block, then per block its P V followed by its S two blocks on.
-          const int nb = it.kbmax[0] + 1;
-          ok = k_step(i, 0, T == 0) && k_step(i + 1, 1, T == 1);
-          for (int kb = 0; kb < nb && ok; ++kb) {
-            const bool mine = (kb & 1) == T;
-            ok = v_step(i + kb, mine);
-            if (ok && kb + 2 < nb) ok = k_step(i + kb + 2, kb + 2, mine);
-          }
-          i += nb;
-        } else {
-          int kb = sch.next(-1);
-          if (kb >= 0) ok = k_step(i, kb, (sch.member(kb) >> T) & 1);
-          while (kb >= 0 && ok) {
-            const int nkb = sch.next(kb);
-            ok = v_step(i, (sch.member(kb) >> T) & 1);
-            if (ok && nkb >= 0) ok = k_step(i + 1, nkb, (sch.member(nkb) >> T) & 1);
-            if (T == 0) BSS_TRACE_EV(p, tr, 1, 4 * i + 3);
-            kb = nkb;
-            ++i;
+            clc_out = false;
+            ++clc_k;
+            if (clc_query(sbase + C::kClcOff, x)) {
+              if (x >= 0 && x < p.n_items)
+                got = 1;
+              else
+                record_error(p.err, ATTN_ERR_CUDA);   // not an index of this grid
+            }
           }
         }
-        if (!ok) break;
-        // a shared Q buffer this slot never read in the item: hand it back
-        // once the item's Q has landed (so that the arrival is the item's own)
-        if (kDec && mylast < 0 && qlast >= 0) {
-          if (!wait_q()) break;
-          mbar_arrive(bar(C::kBarQEmpty + q));
-        }
-        if (ostarted) {
-          mma_commit(bar(C::kBarOFull + T));
-          ++on;
-        }
-        if (qready) ++qn;
-        const int s = n & 1;
-        if (!wait_bar(bar(C::kBarItemFull + s), (n >> 1) & 1, abort_flag, p.err)) break;
-        const int next = next_item[s];
-        mbar_arrive(bar(C::kBarItemEmpty + s));
-        ++n;
-        if (next < 0) break;
-        item = next;
+        if (__shfl_sync(0xFFFFFFFFu, fail, 0)) break;
+        got = __shfl_sync(0xFFFFFFFFu, got, 0);
+        x = __shfl_sync(0xFFFFFFFFu, x, 0);
+        if (got)
+          next = x;
+        else
+          live = false;   // nothing left to take (no request follows a failed one)
       }
-      // every MMA issued (by both issuers) has completed before tensor memory
-      // is released
-      mma_commit(bar(C::kBarMmaDone));
-      drain_bar(bar(C::kBarMmaDone), 0);
-    };
-    if (lane == 0) {
-      if (warp == 1)
-        run_issuer(SlotTag<0>{});
-      else
-        run_issuer(SlotTag<1>{});
+      if (next >= 0) {
+        // the item's bitmaps: clear the buffer, then one bit per listed block
+        const FwdItem it = fwd_item<CAUSAL, kAlt>(next, p);
+        uint32_t* bm = bitmap + b * 2 * bw;
+        for (int i = lane; i < 2 * bw; i += 32) bm[i] = 0u;
+        int v = INT_MIN;                           // no such query block
+        if (lane < 4) {
+          const int t = lane >> 1;
+          const int qb = it.r0[t] / kTileM;
+          if (it.r0[t] < p.Lq && qb < p.n_qblk)
+            v = __ldg(p.row_ptr + static_cast<size_t>(it.bh / p.heads_per_list) * (p.n_qblk + 1) +
+                      qb + (lane & 1));
+        }
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int beg = __shfl_sync(0xFFFFFFFFu, v, 2 * t);
+          const int end = __shfl_sync(0xFFFFFFFFu, v, 2 * t + 1);
+          if (beg == INT_MIN) continue;
+          if (beg < 0 || end < beg || end > p.nnz) {
+            if (lane == 0) record_error(p.err, ATTN_ERR_BAD_BLOCKLIST);
+            continue;
+          }
+          for (int e = beg + lane; e < end; e += 32) {
+            const int c = __ldg(p.col_idx + e);
+            if (c < 0 || c >= nk) {
+              record_error(p.err, ATTN_ERR_BAD_BLOCKLIST);
+              continue;
+            }
+            atomicOr(bm + t * bw + (c >> 5), 1u << (c & 31));
+          }
+        }
+        __threadfence_block();
+        __syncwarp();
+      }
+      if (lane == 0) {
+        next_item[s] = next;
+        mbar_arrive(bar(C::kBarItemFull + s));   // releases the bitmaps built above
+      }
+      if (next < 0) break;
     }
+    if (lane == 0 && clc_out) drain_bar(bar(C::kBarClc), clc_k & 1);
   }
   } else {
     regs_set<FwdRegs<SPARSE>::kHigh, FwdRegs<SPARSE>::kLaunchRegs>();
@@ -861,7 +851,11 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     while (ok) {
       const FwdItem it = fwd_item<CAUSAL, kAlt>(item, p);
-      const Schedule sch(it, sched_bm, C::kBitmapWords);
+      const Schedule sch(it, item_bm(n), bw);
+      // block-sparse: whether slot 0 (1) accumulates into O_0 (O_1) in this
+      // item, read before the item's bitmaps are released
+      const bool has0 = SPARSE && sch.last(0) >= 0;
+      const bool has1 = SPARSE && sch.last(1) >= 0;
       const int r0 = t ? it.r0[1] : it.r0[0];
       const int row = r0 + row_in_tile;
 
@@ -971,6 +965,10 @@ __global__ void __launch_bounds__(384, 1)
         ++ci;
       }
       if (!ok) break;
+      if (SPARSE) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(C::kBarBmEmpty + (n & 1)));   // bitmaps walked
+      }
 
       if (kAlt && it.alt && t == 1) {
         // Alternating item: this row's state over the odd key blocks goes to
@@ -1093,8 +1091,8 @@ __global__ void __launch_bounds__(384, 1)
         if (inb) p.lse[row_g] = l > 0.f ? (m2 + __log2f(l)) * kLn2 : NEG_INF;
       }
       }
-      on0 += sch.last(0) >= 0 ? 1 : 0;
-      on1 += sch.last(1) >= 0 ? 1 : 0;
+      on0 += (SPARSE ? has0 : sch.last(0) >= 0) ? 1 : 0;
+      on1 += (SPARSE ? has1 : sch.last(1) >= 0) ? 1 : 0;
       BSS_TRACE_EV(p, trw, 4 + t, 2 * n + 1);
       // ---- next item ----
       const int s = n & 1;
@@ -1121,7 +1119,7 @@ __global__ void __launch_bounds__(384, 1)
 template <int D, bool CAUSAL, bool SPARSE, bool PARTIAL, bool ALT, bool DEC>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, cudaStream_t st) {
-  using C = FwdCfg<D, DEC && ALT && !SPARSE>;
+  using C = FwdCfg<D, DEC && ALT && !SPARSE, SPARSE>;
   auto kern = attn_fwd_kernel<D, CAUSAL, SPARSE, PARTIAL, ALT, DEC>;
   constexpr int kMaxDev = 64;
   static bool configured[kMaxDev] = {};  // the attribute is per device and function

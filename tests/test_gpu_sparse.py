@@ -159,3 +159,38 @@ def test_blocksparse_16k_full_size_sampled(bss):
     for n_, (b, h) in enumerate(heads):
         compare_forward(o[b, h, rows], lse[b, h, rows], O_ref[n_], l_ref[n_], f"head {(b, h)}")
     assert torch.isfinite(o).all()
+
+
+@pytest.mark.parametrize("d,causal", [(128, True), (128, False), (64, True)])
+def test_persistent_items_odd_tile_count_per_head_lists(bss, d, causal):
+    """More items than SMs (2 x 24 heads x 13 query pairs = 624), so that each
+    CTA runs several in turn and prepares the next item's bitmaps while the
+    current one runs; 25 query tiles, so that under the causal mask the first
+    items (the last pairs) hold a single tile and the CTA hands back the Q
+    buffer its empty slot never read; one random list per head, with empty
+    rows, duplicates and future blocks.  Whole heads against the oracle, each
+    head's items spread over the whole launch."""
+    n = 25
+    L = n * 128 - 50
+    B, H = 2, 24
+    w = Workload("persist", B, H, L, d, causal, seed=31 + d)
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    lists = [random_blocklist(n, n, seed=100 + x) for x in range(B * H)]
+    rp = np.zeros((B * H, n + 1), np.int32)
+    cis, off = [], 0
+    for x, (r, c) in enumerate(lists):
+        rp[x] = r + off
+        cis.append(c)
+        off += len(c)
+    ci = np.concatenate(cis).astype(np.int32)
+    o, lse = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=causal,
+                                      scale=w.scale)
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    assert torch.isfinite(o).all()
+    for b, h in ((0, 0), (0, 17), (1, 6), (1, 23)):
+        r, c = lists[b * H + h]
+        O_ref, l_ref = oracle_forward(cpu, w.scale, heads=[(b, h)], causal=causal, block=128,
+                                      row_ptr=r, col_idx=c)
+        compare_forward(o[b, h], lse[b, h], O_ref[0], l_ref[0], f"head {(b, h)}")

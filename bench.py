@@ -15,8 +15,9 @@ V and dO, larger than the 129 MB L2):
 (4d FLOPs per allowed pair) over its CUDA-event time inside the timed steps,
 summed over ranks.  `step_tflops` is the whole step's algorithmic TFLOP/s
 (10d per allowed pair for the backward).  Sparse pairs/s, the roofline of the
-step's dominant kernel and of the forward, and the other workload shapes are
-reported beside it.
+step's dominant kernel (the backward's main kernel, its own launch timed by
+CUDA events the library records around it) and of the forward, and the other
+workload shapes are reported beside it.
 
 --impl reference times the fp64 CPU oracle's forward on a bounded sample of
 the same workload (rows of one head) on the host cores, with the same metric
@@ -105,6 +106,12 @@ KERNEL_OF_ROW = {
     "bwd": "attn_bwd call: attn_bwd_preprocess_kernel + attn_bwd_main_kernel + "
            "attn_bwd_dq_convert_kernel (timed together)",
 }
+# The dominant row's own kernel where the row's call launches more than one:
+# the backward's main kernel, timed by the CUDA events attn_bwd records around
+# its launch (attn_bwd_time_main).
+MAIN_KERNEL_OF_ROW = {"bwd": "attn_bwd_main_kernel: its own launch, between CUDA events the "
+                             "library records around it inside attn_bwd (preprocess and dQ "
+                             "conversion excluded)"}
 TRAFFIC_KERNEL = {"fwd": "attn_fwd_kernel", "bwd": "attn_bwd_main_kernel"}
 KERNEL_SOURCES = {"attn_fwd_kernel": ["fwd.cu", "common.cuh", "ptx.cuh"],
                   "attn_bwd_main_kernel": ["bwd.cu", "common.cuh", "ptx.cuh"]}
@@ -301,15 +308,21 @@ class Step:
         if ev is not None:
             ev["sparse"][1].record()
             ev["bwd"][0].record()
+            # the backward's main kernel alone: events the library records
+            # around its launch inside attn_bwd
+            bss.attn_bwd_time_main(*self.main_events)
         bss.attn_bwd(d["q"], d["k"], d["v"], self.o, self.lse, d["do"], causal=True,
                      scale=w.scale, workspace=self.ws, dq=self.dq, dk=self.dk, dv=self.dv,
                      delta=self.delta)
         if ev is not None:
+            bss.attn_bwd_time_main()
             ev["bwd"][1].record()
 
     def new_events(self):
         self.events = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                        for k in self.flops}
+        self.main_events = (torch.cuda.Event(enable_timing=True),
+                            torch.cuda.Event(enable_timing=True))
 
 
 def time_loop(fn, steps, warmup, sync_all):
@@ -653,10 +666,11 @@ def run_gpu(args):
         step.run()
     torch.cuda.synchronize()
     sync_all()
-    events = []
+    events, main_events = [], []
     for _ in range(args.steps):
         step.new_events()
         events.append(step.events)
+        main_events.append(step.main_events)
     clocks.start()
     t0 = time.time()
     start = torch.cuda.Event(enable_timing=True)
@@ -664,6 +678,7 @@ def run_gpu(args):
     start.record()
     for i in range(args.steps):
         step.events = events[i]
+        step.main_events = main_events[i]
         step.run(timed_rows=True)
     end.record()
     torch.cuda.synchronize()
@@ -673,6 +688,7 @@ def run_gpu(args):
     ms_step = start.elapsed_time(end) / args.steps
     row_avg = {k: statistics.mean(ev[k][0].elapsed_time(ev[k][1]) for ev in events)
                for k in step.flops}
+    ms_bwd_main = statistics.mean(a.elapsed_time(b) for a, b in main_events)
     ms_fwd = row_avg["fwd"]
     if world > 1:
         ms_step = max_over_ranks(ms_step, dev)
@@ -722,9 +738,11 @@ def run_gpu(args):
     value = job_throughput(step.flops["fwd"], ms_fwd, world)
     step_tf = job_throughput(step.total_flops, ms_step, world)
     row_tf = {k: step.flops[k] / row_avg[k] / 1e9 for k in step.flops}
-    # dominant kernel: the largest share of the step's time
+    # dominant kernel: the largest share of the step's time; for the backward
+    # row its main kernel, timed by itself
     dom = max(row_avg, key=row_avg.get)
-    dom_tf = row_tf[dom]
+    dom_ms = ms_bwd_main if dom == "bwd" else row_avg[dom]
+    dom_tf = step.flops[dom] / dom_ms / 1e9
     traffic, traffic_note = dram_traffic(dom)
     traffic_f, traffic_note_f = dram_traffic("fwd")
     timed_s = ms_step * args.steps / 1e3
@@ -760,7 +778,7 @@ def run_gpu(args):
         "sparse_pairs_per_s": step.pairs_sparse / row_avg["sparse"] * 1e3,
         "sparse_executed_tiles": step.tiles_sparse,
         "sparse_list_stats": dict(zip(("listed", "executed", "future", "pairs"), list_stats)),
-        "roofline": {"kernel": KERNEL_OF_ROW[dom],
+        "roofline": {"kernel": MAIN_KERNEL_OF_ROW.get(dom, KERNEL_OF_ROW[dom]),
                      "share_of_step": round(row_avg[dom] / sum(row_avg.values()), 4),
                      "bound": "tensor", "achieved": round(dom_tf, 1),
                      "peak": pk_b, "unit": "TFLOP/s",
@@ -768,6 +786,10 @@ def run_gpu(args):
                      "frac_of_sustained": round(dom_tf / pk_s, 4),
                      "peak_kind": peak_kind,
                      "flops_per_launch": step.flops[dom],
+                     "ms_per_launch": round(dom_ms, 4),
+                     "call": {"what": KERNEL_OF_ROW[dom], "ms": round(row_avg[dom], 4),
+                              "achieved": round(row_tf[dom], 1),
+                              "frac": round(row_tf[dom] / pk_b, 4)},
                      "traffic": traffic, "traffic_note": traffic_note},
         "roofline_fwd": {"kernel": KERNEL_OF_ROW["fwd"], "bound": "tensor",
                          "achieved": round(row_tf["fwd"], 1), "peak": pk_b, "unit": "TFLOP/s",

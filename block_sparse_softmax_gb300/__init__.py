@@ -10,7 +10,8 @@ Functions carry the C names: ``attn_fwd``, ``attn_fwd_partial``,
 ``attn_merge_states``, ``attn_fwd_splitkv``, ``attn_blocklist_normalize``,
 ``attn_blocklist_stats``, ``attn_fwd_blocksparse``, ``attn_select_blocks``,
 ``attn_bwd``, ``attn_bwd_blocksparse``, ``attn_bwd_noalloc``, ``attn_poll_status``,
-``attn_watchdog_selftest``, ``attn_probe_ex2_rate``.  Each call runs on the
+``attn_bwd_time_main``, ``attn_watchdog_selftest``, ``attn_probe_ex2_rate``.  Each
+call runs on the
 device of its tensors and on that device's current stream.
 """
 from __future__ import annotations
@@ -29,7 +30,7 @@ __all__ = [
     "attn_fwd_blocksparse", "attn_select_blocks", "attn_select_blocks_workspace_bytes",
     "attn_select_blocks_nnz", "attn_bwd", "attn_bwd_workspace_bytes", "attn_bwd_blocksparse",
     "attn_bwd_blocksparse_workspace_bytes", "attn_bwd_noalloc", "attn_poll_status",
-    "attn_watchdog_selftest", "attn_probe_ex2_rate", "library",
+    "attn_bwd_time_main", "attn_watchdog_selftest", "attn_probe_ex2_rate", "library",
 ]
 
 OK = 0
@@ -393,6 +394,22 @@ def attn_poll_status(device=None) -> int:
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream(dev).cuda_stream
         return int(_lib.load().attn_poll_status(stream))
+
+
+def attn_bwd_time_main(begin: Optional[torch.cuda.Event] = None,
+                       end: Optional[torch.cuda.Event] = None) -> None:
+    """Record ``begin`` and ``end`` (torch.cuda.Event, enable_timing=True, on
+    the device of the calls) just before and after the main kernel of every
+    following backward call, so that ``begin.elapsed_time(end)`` is that
+    kernel's own duration; ``attn_bwd_time_main()`` stops it.  Stop it before
+    the events are dropped."""
+    def handle(e):
+        if e is None:
+            return None
+        if not e.cuda_event:       # the CUDA event is created at its first record
+            e.record()
+        return e.cuda_event
+    _check(_lib.load().attn_bwd_time_main(handle(begin), handle(end)), "attn_bwd_time_main")
 
 
 def attn_probe_ex2_rate(blocks: int, iters: int, sink: Optional[torch.Tensor] = None,

@@ -65,6 +65,7 @@ _SIGNATURES = {
                                     _C.c_void_p, _C.c_void_p, _C.c_int, _C.c_int, _C.c_int,
                                     _C.c_int, _C.c_int, _C.c_float, _C.c_int, _C.c_void_p]),
     "attn_poll_status": (_C.c_int, [_C.c_void_p]),
+    "attn_bwd_time_main": (_C.c_int, [_C.c_void_p, _C.c_void_p]),
     "attn_watchdog_selftest": (_C.c_int, [_C.c_ulonglong, _C.c_void_p]),
     "attn_probe_ex2_rate": (_C.c_int, [_C.c_void_p, _C.c_int, _C.c_int, _C.c_void_p]),
 }

@@ -29,6 +29,10 @@ EncodeTiledFn g_encode = nullptr;
 
 thread_local char g_last_error[256] = {0};
 
+// attn_bwd_time_main: events recorded around each backward's main kernel
+// (process-wide; NULL when off)
+cudaEvent_t g_bwd_main_ev[2] = {nullptr, nullptr};
+
 #ifdef BSS_TRACE
 long long* g_trace_buf = nullptr;
 int g_trace_cta = 0;
@@ -313,7 +317,8 @@ attn_status_t bwd_common(const void* q, const void* k, const void* v, const void
     if (s != ATTN_OK) return s;
   }
   return cuda_status("attn_bwd launch", launch_bwd(d, sparse, tq, tk, tv, tdo, tdq, p,
-                                                   static_cast<cudaStream_t>(stream)));
+                                                   static_cast<cudaStream_t>(stream),
+                                                   g_bwd_main_ev[0], g_bwd_main_ev[1]));
 }
 
 // Split-KV forward: keys in chunks of a multiple of 128, each chunk's partial
@@ -622,6 +627,13 @@ attn_status_t attn_poll_status(void* stream) {
     if (e != cudaSuccess) return cuda_status("status reset", e);
   }
   return static_cast<attn_status_t>(value);
+}
+
+attn_status_t attn_bwd_time_main(void* begin, void* end) {
+  if ((begin == nullptr) != (end == nullptr)) return ATTN_ERR_INVALID_ARG;
+  g_bwd_main_ev[0] = static_cast<cudaEvent_t>(begin);
+  g_bwd_main_ev[1] = static_cast<cudaEvent_t>(end);
+  return ATTN_OK;
 }
 
 attn_status_t attn_probe_ex2_rate(float* sink, int blocks, int iters, void* stream) {

@@ -1029,7 +1029,8 @@ cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int
 
 cudaError_t launch_bwd(int d, bool sparse, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
-                       const BwdParams& p, cudaStream_t st) {
+                       const BwdParams& p, cudaStream_t st, cudaEvent_t main_begin,
+                       cudaEvent_t main_end) {
   const long long rows = static_cast<long long>(p.B) * p.H * p.L;
   cudaError_t e;
   if (d == 64) {
@@ -1040,6 +1041,8 @@ cudaError_t launch_bwd(int d, bool sparse, const CUtensorMap& tq, const CUtensor
     return cudaErrorInvalidValue;
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // optional timing of the main kernel alone (attn_bwd_time_main)
+  if (main_begin && (e = cudaEventRecord(main_begin, st)) != cudaSuccess) return e;
 #define BSS_BWD_CASE(DD, CA, SP)                                  \
   if (d == DD && (p.causal != 0) == CA && sparse == SP)           \
     e = launch_main<DD, CA, SP>(tq, tk, tv, tdo, tdq, p, st);
@@ -1054,6 +1057,7 @@ cudaError_t launch_bwd(int d, bool sparse, const CUtensorMap& tq, const CUtensor
   BSS_BWD_CASE(128, true, true)
 #undef BSS_BWD_CASE
   if (e != cudaSuccess) return e;
+  if (main_end && (e = cudaEventRecord(main_end, st)) != cudaSuccess) return e;
   const long long n8 = rows * d / 8;
   attn_bwd_dq_convert_kernel<<<grid_for(n8, 256), 256, 0, st>>>(p.dq_acc, p.dq, n8);
   return cudaGetLastError();

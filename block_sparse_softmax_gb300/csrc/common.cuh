@@ -216,7 +216,8 @@ cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUte
 cudaError_t launch_merge(int d, const MergeParams& p, int* err, cudaStream_t st);
 cudaError_t launch_bwd(int d, bool sparse, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
-                       const BwdParams& p, cudaStream_t st);
+                       const BwdParams& p, cudaStream_t st, cudaEvent_t main_begin = nullptr,
+                       cudaEvent_t main_end = nullptr);
 cudaError_t launch_bwd_cta_order(const uint32_t* bitmap, int words, int nq, int B, int H, int Hkv,
                                  int heads_per_list, int head_group, int* order, cudaStream_t st);
 cudaError_t launch_blocklist_columns(const int* row_ptr, const int* col_idx, int n_lists, int n_qblk,

@@ -336,6 +336,23 @@ attn_status_t attn_bwd_noalloc(const void* q, const void* k, const void* v, cons
 attn_status_t attn_poll_status(void* stream);
 
 /*
+ * attn_bwd_time_main - measurement aid: the backward calls (attn_bwd,
+ * attn_bwd_blocksparse, attn_bwd_noalloc) launch three kernels, the row
+ * statistic D = rowsum(dO * O), the main kernel that recomputes the score
+ * tiles and produces dK, dV and the dQ accumulator ("Exact Blocks, Rings, and
+ * Sparsity", section 3), and the dQ conversion to bf16.  While `begin` and
+ * `end` are set, every backward call records `begin` on its stream just
+ * before the main kernel's launch and `end` just after it, so that the
+ * elapsed time between them (cudaEventElapsedTime) is that kernel's own
+ * duration.  `begin`, `end`: cudaEvent_t handles owned by the caller, created
+ * on the device of the calls (and with timing enabled, for elapsed times).
+ * Both NULL switches the recording off.  The setting is process-wide: set and
+ * clear it from the thread that makes the calls.  Returns
+ * ATTN_ERR_INVALID_ARG when exactly one of the two is NULL, else ATTN_OK.
+ */
+attn_status_t attn_bwd_time_main(void* begin, void* end);
+
+/*
  * attn_probe_ex2_rate - measurement aid for the softmax's second ceiling:
  * the forward evaluates one exponential per pair ("FlashAttention: Fast and
  * Memory Efficient Exact Attention with IO Awareness", section 5.1, the

@@ -163,6 +163,10 @@ def test_argument_errors_return_codes_before_any_device_work(lib):
     assert lib.attn_bwd_blocksparse(*sp(nq=7)) == 3              # CSR row count mismatch
     assert lib.attn_bwd_blocksparse(*sp(rp=None)) == 1           # missing row_ptr
     assert lib.attn_bwd_blocksparse(*sp(ws_=wss - 4)) == 6       # workspace too small
+    # main-kernel timing hook: both events or neither (no device work)
+    assert lib.attn_bwd_time_main(P, None) == 1
+    assert lib.attn_bwd_time_main(None, P) == 1
+    assert lib.attn_bwd_time_main(None, None) == 0
     # exponential-rate probe: sink and sizes
     assert lib.attn_probe_ex2_rate(None, 8, 16, None) == 1
     assert lib.attn_probe_ex2_rate(bad, 8, 16, None) == 1        # misaligned sink

@@ -81,3 +81,31 @@ def test_backward_8k_full_size(bss):
     gq, gk, gv, _ = oracle.attention_backward(q, k, v, do, w.scale, causal=True, heads=heads)
     for n_, (b, h) in enumerate(heads):
         _check_grads((dq[b, h], dk[b, h], dv[b, h]), (gq[n_], gk[n_], gv[n_]), f"head {(b, h)}")
+
+
+def test_main_kernel_timing_events(bss):
+    """attn_bwd_time_main: the events bracket the main kernel alone, so their
+    interval is positive and shorter than the whole call's; clearing stops the
+    recording, and setting only one event is refused."""
+    import torch
+    w = Workload("tm", 1, 4, 2048, 128, True, seed=8, backward=True)
+    inp = to_cuda(make_inputs(w))
+    o, lse = bss.attn_fwd(inp["q"], inp["k"], inp["v"], causal=True, scale=w.scale)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    bss.attn_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], causal=True, scale=w.scale)
+    bss.attn_bwd_time_main(ev[1], ev[2])
+    ev[0].record()
+    bss.attn_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], causal=True, scale=w.scale)
+    ev[3].record()
+    bss.attn_bwd_time_main()
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    main_ms, call_ms = ev[1].elapsed_time(ev[2]), ev[0].elapsed_time(ev[3])
+    assert 0 < main_ms < call_ms
+    # cleared: a later call leaves the events where they were
+    t_before = ev[1].elapsed_time(ev[2])
+    bss.attn_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    assert ev[1].elapsed_time(ev[2]) == t_before
+    from block_sparse_softmax_gb300 import _lib
+    assert _lib.load().attn_bwd_time_main(ev[1].cuda_event, None) == bss.ERR_INVALID_ARG

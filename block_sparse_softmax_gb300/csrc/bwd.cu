@@ -390,8 +390,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mma_commit(bar(C::kBarDPFull + h));
         return true;
       };
+      // Block-sparse launches issue dP^T as one N=128 group once both halves
+      // of dQ's columns are free: an N=64 MMA costs the tensor pipe nearly as
+      // much as an N=128 one (93 against 102 cycles in a probe), and with a CTA's query
+      // tiles spread out the halves' earlier start does not pay for the extra
+      // eight (0.868 -> 0.850 ms on the L'=16320 workload; the dense and
+      // causal backward measured 2.8 % slower with it, 1 % slower when the
+      // single group was taken only when both halves were already free).
+      constexpr bool kDPHalves = C::kDQOverDP && !SPARSE;
       auto issue_dp = [&](int it) -> bool {
-        if (C::kDQOverDP) return issue_dp_half(it, 0) && issue_dp_half(it, 1);
+        if (kDPHalves) return issue_dp_half(it, 0) && issue_dp_half(it, 1);
         if (!wait_bar(bar(C::kBarDOFull + it % C::kStagesDO), (it / C::kStagesDO) & 1, abort_flag, p.err))
           return false;
         tc_fence_after();
@@ -453,13 +461,19 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         mma_commit(bar(C::kBarQEmpty + it % C::kStagesQ));
         BSS_TRACE_EV(p, tr, 1, 4 * it + 2);
         if (more) {
-          if (C::kDQOverDP) {
+          if (kDPHalves) {
             // dP^T(i+1) over dQ(i): each half once its columns have been read out
             if (!wait_bar(bar(C::kBarDQFree), it & 1, abort_flag, p.err)) break;
             if (!issue_dp_half(it + 1, 0)) break;
             if (!wait_bar(bar(C::kBarDQFree + 1), it & 1, abort_flag, p.err)) break;
             BSS_TRACE_EV(p, tr, 1, 4 * it + 3);
             if (!issue_dp_half(it + 1, 1)) break;
+          } else if (C::kDQOverDP) {
+            // one N=128 group once both halves of dQ's columns are read out
+            if (!wait_bar(bar(C::kBarDQFree), it & 1, abort_flag, p.err)) break;
+            if (!wait_bar(bar(C::kBarDQFree + 1), it & 1, abort_flag, p.err)) break;
+            BSS_TRACE_EV(p, tr, 1, 4 * it + 3);
+            if (!issue_dp(it + 1)) break;
           } else {
             BSS_TRACE_EV(p, tr, 1, 4 * it + 3);
             if (!issue_dp(it + 1)) break;

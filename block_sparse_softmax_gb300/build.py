@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB_PATH = os.path.join(LIB_DIR, "libbss_attn.so")
-SOURCES = ["api.cu", "fwd.cu", "merge.cu", "bwd.cu", "select.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "fwd.cu", "fwd_wide.cu", "merge.cu", "bwd.cu", "select.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]

@@ -213,6 +213,10 @@ namespace bss {
 cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                        cudaStream_t st);
+// The forward with 256-key score tiles (fwd_wide.cu): d = 128, dense or
+// causal, bf16 output; attn_fwd's launches of that kind run it.
+cudaError_t launch_fwd_wide(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const FwdParams& p, cudaStream_t st);
 cudaError_t launch_merge(int d, const MergeParams& p, int* err, cudaStream_t st);
 cudaError_t launch_bwd(int d, bool sparse, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,

@@ -1151,6 +1151,9 @@ cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUte
   // copy with the path measured faster and serves every launch).  A launch
   // whose query rows fit one tile (decoding) runs the instantiation with a
   // single Q buffer and one more K stage.
+  // d = 128 without block lists or partial states: the kernel with 256-key
+  // score tiles (fwd_wide.cu)
+  if (d == 128 && !sparse && !partial) return launch_fwd_wide(causal, tq, tk, tv, p, st);
   const bool single_tile_pair = (p.Lq % (2 * kTileM)) != 0 && (p.Lq % (2 * kTileM)) <= kTileM;
   const bool alt = !sparse && (single_tile_pair || (!partial && d == 64));
   const bool dec = alt && p.Lq >= 1 && p.Lq <= kTileM;

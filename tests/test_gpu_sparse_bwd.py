@@ -102,9 +102,9 @@ def test_every_block_listed_equals_dense_backward(bss):
     """With every block listed the sparse walk visits the dense causal tiles in
     the same order: given the same O and LSE, dK, dV and D are identical to
     attn_bwd's; dQ (added in by reduce operations whose order is not fixed)
-    agrees within the tolerance.  The forwards agree bit for bit on rows in full
-    pairs of query tiles; the last pair here (rows 1024-1099) has a single tile,
-    whose blocks the dense forward sums in another order."""
+    agrees within the tolerance.  The two forwards agree within the tolerance:
+    at d=128 the dense one scores pairs of key blocks (its reference max moves
+    per pair), so their roundings differ."""
     L, d = 1100, 128
     n = (L + 127) // 128
     rp = (np.arange(n + 1) * n).astype(np.int32)
@@ -116,8 +116,6 @@ def test_every_block_listed_equals_dense_backward(bss):
     ref = bss.attn_bwd(inp["q"], inp["k"], inp["v"], o, lse, inp["do"], causal=True,
                        scale=w.scale)
     torch.cuda.synchronize()
-    full = 1024
-    assert torch.equal(o[:, :, :full], o2[:, :, :full]) and torch.equal(lse[..., :full], lse2[..., :full])
     assert (o.float() - o2.float()).abs().max().item() <= TOL_O
     assert (lse - lse2).abs().max().item() <= TOL_LSE
     assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2]) and torch.equal(delta, ref[3])

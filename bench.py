@@ -100,7 +100,7 @@ def load_peaks():
 # kernel whose DRAM traffic is reported (the traffic recorded for a kernel is
 # used only while those sources are unchanged).
 KERNEL_OF_ROW = {
-    "fwd": "attn_fwd_kernel (causal, persistent): the whole attn_fwd call",
+    "fwd": "attn_fwd_wide_kernel (causal, persistent, 256-key score tiles): the whole attn_fwd call",
     "splitkv": "attn_fwd_kernel (partial, 8 key chunks in one launch) + merge_states_kernel",
     "sparse": "attn_fwd_kernel (block-sparse)",
     "bwd": "attn_bwd call: attn_bwd_preprocess_kernel + attn_bwd_main_kernel + "
@@ -112,8 +112,8 @@ KERNEL_OF_ROW = {
 MAIN_KERNEL_OF_ROW = {"bwd": "attn_bwd_main_kernel: its own launch, between CUDA events the "
                              "library records around it inside attn_bwd (preprocess and dQ "
                              "conversion excluded)"}
-TRAFFIC_KERNEL = {"fwd": "attn_fwd_kernel", "bwd": "attn_bwd_main_kernel"}
-KERNEL_SOURCES = {"attn_fwd_kernel": ["fwd.cu", "common.cuh", "ptx.cuh"],
+TRAFFIC_KERNEL = {"fwd": "attn_fwd_wide_kernel", "bwd": "attn_bwd_main_kernel"}
+KERNEL_SOURCES = {"attn_fwd_wide_kernel": ["fwd_wide.cu", "common.cuh", "ptx.cuh"],
                   "attn_bwd_main_kernel": ["bwd.cu", "common.cuh", "ptx.cuh"]}
 STEP_WORKLOAD = CAUSAL_16K
 

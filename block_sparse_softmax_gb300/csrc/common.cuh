@@ -213,10 +213,14 @@ namespace bss {
 cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUtensorMap& tq,
                        const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                        cudaStream_t st);
-// The forward with 256-key score tiles (fwd_wide.cu): d = 128, dense or
-// causal, bf16 output; attn_fwd's launches of that kind run it.
-cudaError_t launch_fwd_wide(bool causal, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const FwdParams& p, cudaStream_t st);
+// The forward with 256-key score tiles (fwd_wide.cu): d = 128, dense, causal
+// or block-sparse, a bf16 output or (partial, not block-sparse) fp32 partial
+// states per key chunk.  launch_fwd picks it; fwd_wide_takes_sparse tells
+// whether its block-sparse bitmaps cover a key range of Lk.
+bool fwd_wide_takes_sparse(int Lk);
+cudaError_t launch_fwd_wide(bool causal, bool partial, bool sparse, const CUtensorMap& tq,
+                            const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                            cudaStream_t st);
 cudaError_t launch_merge(int d, const MergeParams& p, int* err, cudaStream_t st);
 cudaError_t launch_bwd(int d, bool sparse, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,

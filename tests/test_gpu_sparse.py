@@ -59,33 +59,61 @@ def test_unstructured_lists(bss, seed, d):
     compare_forward(o, lse, O_ref, l_ref, f"random list seed={seed}")
 
 
-def test_order_and_duplicates_are_bit_identical(bss):
-    L, d = 1500, 128
+def _repeat_rows(rp, ci, times, rng=None):
+    """Each row's entries `times` times over, in a random order when `rng`."""
+    rows = [np.repeat(ci[rp[a]:rp[a + 1]], times) for a in range(len(rp) - 1)]
+    if rng is not None:
+        rows = [rng.permutation(r) for r in rows]
+    return (rp * times).astype(np.int32), np.concatenate(rows).astype(np.int32)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_order_and_duplicates_are_bit_identical(bss, d):
+    """Lists of one set run the same kernel, and agree bit for bit, when their
+    raw lengths fall on the same side of the bound that picks the kernel (8
+    entries per query block on average, at d=128): the raw list against a
+    permutation of every row; the normalised list against its rows listed
+    twice (both short); three times against four times over, permuted (at
+    d=128 both long, the kernel with 256-key score tiles).  Short and long
+    forms of the set agree within the tolerance."""
+    L = 1500
     n = (L + 127) // 128
     rp, ci = random_blocklist(n, n, seed=9, max_per_row=7, p_empty=0.1)
     cp, cc = bss.attn_blocklist_normalize(rp, ci, n)
+    assert len(ci) < 8 * n and 2 * len(cc) < 8 * n and 3 * len(cc) >= 8 * n
     rng = np.random.default_rng(0)
-    perm_ci = np.concatenate([rng.permutation(np.repeat(cc[cp[a]:cp[a + 1]], 3))
-                              for a in range(n)]).astype(np.int32)
-    perm_rp = (cp * 3).astype(np.int32)
+    lists = {"raw": (rp, ci), "raw permuted": _repeat_rows(rp, ci, 1, rng),
+             "normalised": (cp, cc), "twice": _repeat_rows(cp, cc, 2),
+             "3x": _repeat_rows(cp, cc, 3, rng), "4x": _repeat_rows(cp, cc, 4, rng)}
     w = Workload("p", 1, 2, L, d, True, seed=5)
     inp = to_cuda(make_inputs(w))
-    a = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=True)
-    b = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], cp, cc, causal=True)
-    c = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], perm_rp, perm_ci, causal=True)
+    out = {k: bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], r, c, causal=True)
+           for k, (r, c) in lists.items()}
     torch.cuda.synchronize()
-    for x in (b, c):
-        assert torch.equal(a[0], x[0]) and torch.equal(a[1], x[1])
+    same = [("raw", "raw permuted"), ("normalised", "twice"), ("raw", "normalised"),
+            ("3x", "4x")]
+    for a, b in same:
+        assert torch.equal(out[a][0], out[b][0]) and torch.equal(out[a][1], out[b][1]), (a, b)
+    assert (out["raw"][0].float() - out["4x"][0].float()).abs().max().item() <= TOL_O
+    la, lb = out["raw"][1], out["4x"][1]
+    assert torch.equal(torch.isneginf(la), torch.isneginf(lb))
+    fin = ~torch.isneginf(la)
+    assert (la[fin] - lb[fin]).abs().max().item() <= TOL_LSE
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("L", [700, 777])
-def test_all_blocks_listed_equals_dense_kernel(bss, causal, L):
+@pytest.mark.parametrize("d,L", [(64, 700), (64, 777), (128, 1900), (128, 2047)])
+def test_all_blocks_listed_equals_dense_kernel(bss, causal, L, d):
     """Where a pair of query tiles is full, both kernels visit the same blocks in
-    the same order and agree bit for bit.  A last pair with a single tile (rows
-    768-776 at L=777) is split over both tile slots by the dense kernel, which
-    sums its blocks in another order: those rows agree within the tolerance."""
-    d = 64
+    the same order and agree bit for bit.  At d=64 a last pair with a single
+    tile (rows 768-776 at L=777) is split over both tile slots by the dense
+    kernel, which sums its blocks in another order: those rows agree within the
+    tolerance.  At d=128 (15 and 16 blocks: lists of 8 or more entries a row
+    on average, so both launches run the kernel with 256-key score tiles) both
+    take one query tile an item and key blocks two at a time in ascending
+    order; where the count is odd the block-sparse item scores its last block
+    alone and the dense one beside a masked block, whose P is exactly zero:
+    every row agrees bit for bit."""
     n = (L + 127) // 128
     if causal:
         rows = [list(range(a + 1)) for a in range(n)]
@@ -97,7 +125,7 @@ def test_all_blocks_listed_equals_dense_kernel(bss, causal, L):
     o_s, l_s = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=causal)
     o_d, l_d = bss.attn_fwd(inp["q"], inp["k"], inp["v"], causal=causal)
     torch.cuda.synchronize()
-    full = (L // 256) * 256 if 0 < L % 256 <= 128 else L    # rows in full pairs
+    full = (L // 256) * 256 if d == 64 and 0 < L % 256 <= 128 else L    # rows in full pairs
     assert torch.equal(o_s[:, :, :full], o_d[:, :, :full])
     assert torch.equal(l_s[:, :, :full], l_d[:, :, :full])
     if full < L:
@@ -161,15 +189,19 @@ def test_blocksparse_16k_full_size_sampled(bss):
     assert torch.isfinite(o).all()
 
 
-@pytest.mark.parametrize("d,causal", [(128, True), (128, False), (64, True)])
-def test_persistent_items_odd_tile_count_per_head_lists(bss, d, causal):
+@pytest.mark.parametrize("d,causal,repeat", [(128, True, 1), (128, False, 1), (64, True, 1),
+                                             (128, True, 4), (128, False, 4)])
+def test_persistent_items_odd_tile_count_per_head_lists(bss, d, causal, repeat):
     """More items than SMs (2 x 24 heads x 13 query pairs = 624), so that each
     CTA runs several in turn and prepares the next item's bitmaps while the
     current one runs; 25 query tiles, so that under the causal mask the first
     items (the last pairs) hold a single tile and the CTA hands back the Q
     buffer its empty slot never read; one random list per head, with empty
     rows, duplicates and future blocks.  Whole heads against the oracle, each
-    head's items spread over the whole launch."""
+    head's items spread over the whole launch.  With every entry repeated 4
+    times the d=128 lists are long enough on average for the kernel with
+    256-key score tiles, whose warp 3 claims the items and builds their
+    bitmaps."""
     n = 25
     L = n * 128 - 50
     B, H = 2, 24
@@ -177,6 +209,7 @@ def test_persistent_items_odd_tile_count_per_head_lists(bss, d, causal):
     cpu = make_inputs(w)
     inp = to_cuda(cpu)
     lists = [random_blocklist(n, n, seed=100 + x) for x in range(B * H)]
+    lists = [(r * repeat, np.repeat(c, repeat)) for r, c in lists]
     rp = np.zeros((B * H, n + 1), np.int32)
     cis, off = [], 0
     for x, (r, c) in enumerate(lists):
@@ -194,3 +227,85 @@ def test_persistent_items_odd_tile_count_per_head_lists(bss, d, causal):
         O_ref, l_ref = oracle_forward(cpu, w.scale, heads=[(b, h)], causal=causal, block=128,
                                       row_ptr=r, col_idx=c)
         compare_forward(o[b, h], lse[b, h], O_ref[0], l_ref[0], f"head {(b, h)}")
+
+
+@pytest.mark.parametrize("repeat", [1, 8])
+@pytest.mark.parametrize("causal", [True, False])
+def test_odd_and_even_block_counts(bss, causal, repeat):
+    """Rows listing 0 to 7 blocks (a lone last block, a lone first block, the
+    diagonal alone, the partial last block alone), d=128, whole heads against
+    the oracle.  Every entry repeated 8 times (the same sets) makes the lists
+    long enough on average for the kernel with 256-key score tiles, which
+    scores a lone last block by itself; listed once, they run the two-tile
+    kernel."""
+    L, d = 1100, 128                                 # 9 blocks, the last one 76 keys
+    n = (L + 127) // 128
+    rows = [[], [1], [0, 1], [2, 0, 1], [3], [4, 2, 0, 3, 1], [8], [1, 3, 5, 6, 0, 2, 4],
+            [8, 0, 2]]
+    if causal:
+        rows[6] = [6]
+        rows[8] = [8, 7, 6, 5, 4, 3, 2]
+    rows = [r * repeat for r in rows]
+    rp = np.cumsum([0] + [len(r) for r in rows]).astype(np.int32)
+    ci = np.array([c for r in rows for c in r], np.int32)
+    w = Workload("odd", 2, 3, L, d, causal, seed=61)
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    o, lse = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=causal,
+                                      scale=w.scale)
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    O_ref, l_ref = oracle_forward(cpu, w.scale, causal=causal, block=128, row_ptr=rp, col_idx=ci)
+    compare_forward(o, lse, O_ref, l_ref, f"odd counts causal={causal}")
+
+
+@pytest.mark.parametrize("n_blocks", [2048, 2049])
+def test_longest_key_ranges_at_d128(bss, n_blocks):
+    """One head at d=128 with 2048 key blocks (the most one item's bitmap
+    covers in the kernel with 256-key score tiles) and 2049 (handed to the
+    two-tile kernel, whose bitmaps cover up to 4096 blocks), the last block
+    partial; every entry listed twice (lists long enough on average for the
+    first kernel).  Sampled rows against the oracle, the emptied middle block
+    exactly empty."""
+    L = n_blocks * 128 - 40
+    w = Workload("sparse_long", 1, 1, L, 128, True, seed=n_blocks)
+    cpu = make_inputs(w)
+    rp, ci = local_global_random_blocklist(n_blocks, seed=n_blocks)
+    rp, ci = 2 * rp, np.repeat(ci, 2)
+    inp = to_cuda(cpu)
+    o, lse = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=True,
+                                      scale=w.scale)
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    e = n_blocks // 2
+    assert torch.all(torch.isneginf(lse[0, 0, e * 128:(e + 1) * 128]))
+    assert torch.all(o[0, 0, e * 128:(e + 1) * 128] == 0)
+    rng = np.random.default_rng(n_blocks)
+    rows = np.unique(np.concatenate([np.arange(0, 3), np.arange(e * 128 - 2, e * 128 + 2),
+                                     np.arange(L - 130, L, 5), rng.integers(0, L, size=24)]))
+    O_ref, l_ref = oracle_forward(cpu, w.scale, rows=rows, causal=True, block=128, row_ptr=rp,
+                                  col_idx=ci)
+    compare_forward(o[0, 0, rows], lse[0, 0, rows], O_ref[0, 0], l_ref[0, 0], f"{n_blocks} blocks")
+    assert torch.isfinite(o).all()
+
+
+def test_long_lists_16k_full_size_sampled(bss):
+    """B=2 H=16 L'=16320 d=128 with 16 local and 8 random blocks a row (about
+    24 entries: the kernel with 256-key score tiles), causal; sampled heads and
+    rows against the oracle, the emptied middle row exactly empty."""
+    w = SPARSE_16K
+    rp, ci = local_global_random_blocklist(w.n_blocks, seed=w.seed, n_local=16, n_random=8)
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    o, lse = bss.attn_fwd_blocksparse(inp["q"], inp["k"], inp["v"], rp, ci, causal=True,
+                                      scale=w.scale)
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    assert torch.all(torch.isneginf(lse[:, :, 64 * 128:65 * 128]))
+    rows = tile_edge_rows(w.L, n_random=48, seed=4)[::2]
+    heads = [(0, 5), (1, 9)]
+    O_ref, l_ref = oracle_forward(cpu, w.scale, rows=rows, heads=heads, causal=True, block=128,
+                                  row_ptr=rp, col_idx=ci)
+    for n_, (b, h) in enumerate(heads):
+        compare_forward(o[b, h, rows], lse[b, h, rows], O_ref[n_], l_ref[n_], f"head {(b, h)}")
+    assert torch.isfinite(o).all()

@@ -67,10 +67,11 @@ def test_prefill_shapes_match_oracle(bss, causal, chunks):
     compare_forward(o, lse, O_ref, l_ref, f"prefill chunks={chunks} causal={causal}")
 
 
-def test_queries_before_every_key_are_empty(bss):
+@pytest.mark.parametrize("d", [64, 128])
+def test_queries_before_every_key_are_empty(bss, d):
     """Causal with k_offset beyond the first queries: those rows see no key in
     any chunk, so their merged state is empty (O = 0, LSE = -inf)."""
-    Lq, Lk, d = 300, 1000, 64
+    Lq, Lk = 300, 1000
     w = Workload("ko", 1, 2, Lk, d, True, seed=7, Lq=Lq)
     cpu = make_inputs(w)
     inp = to_cuda(cpu)

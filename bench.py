@@ -520,6 +520,22 @@ def measure_configs(bss, dev, peaks):
                    "bwd_ms": round(ms_b, 4),
                    "bwd_tflops_logical": round(10 * w.d * pairs / ms_b / 1e9, 1)}
     del do, ws, g, dl
+    # the same inputs with long lists (16 local and 8 random blocks a row,
+    # about 24 raw entries): at d=128 the kernel with 256-key score tiles
+    lrp, lci = local_global_random_blocklist(w.n_blocks, seed=w.seed, n_local=16, n_random=8)
+    lrpd, lcid = torch.from_numpy(lrp).to(dev), torch.from_numpy(lci).to(dev)
+    ms_l = bench_kernel(lambda: bss.attn_fwd_blocksparse(x["q"], x["k"], x["v"], lrpd, lcid,
+                                                         causal=True, scale=w.scale, out=o,
+                                                         lse=lse))
+    lpairs, ltiles = sparse_counts(w.L, lrp, lci, True)
+    lpairs *= w.B * w.H
+    ltiles *= w.B * w.H
+    out[w.name]["long_lists"] = {
+        "entries_per_row": round(len(lci) / w.n_blocks, 1), "ms": round(ms_l, 4),
+        "logical_pairs": lpairs, "executed_tiles": ltiles, "pairs_per_s": lpairs / ms_l * 1e3,
+        "tflops_logical": round(4 * w.d * lpairs / ms_l / 1e9, 1),
+        "tflops_executed": round(4 * w.d * ltiles * 128 * 128 / ms_l / 1e9, 1)}
+    del lrpd, lcid
     # mean-pooled selector on the same inputs: one list per head of the 4 local
     # and 4 best-scoring blocks; HBM-bound (Q and K read once for the block
     # means), then the block-sparse forward on the lists it chose

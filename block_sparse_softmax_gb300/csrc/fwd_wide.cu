@@ -65,17 +65,19 @@ struct WideCfg {
   static constexpr int kBarVEmpty = 8;      // [2]
   static constexpr int kBarSFull = 10;      // a pair's S in TMEM
   static constexpr int kBarSFree = 11;      // ... read into registers by both warpgroups
-  static constexpr int kBarPFull = 12;      // both halves of P written
-  static constexpr int kBarPvDone = 13;     // a pair's P V completed (P and O free)
-  static constexpr int kBarXch = 14;        // [2] row values exchanged, by parity
-  static constexpr int kBarOFull = 16;
-  static constexpr int kBarOEmpty = 17;
-  static constexpr int kBarItemFull = 18;   // [2]
-  static constexpr int kBarItemEmpty = 20;  // [2]
-  static constexpr int kBarClc = 22;
-  static constexpr int kBarMmaDone = 23;
-  static constexpr int kBarBmEmpty = 24;    // [2] block-sparse: an item's bitmap walked by every role
-  static constexpr int kNumBars = 24 + (SPARSE ? 2 : 0);
+  // [2] P of key block X written by warpgroup X; block 0's also waits for
+  // warpgroup 1's rescale of its half of O (the P V of block 0 writes all of O)
+  static constexpr int kBarPFull = 12;
+  static constexpr int kBarPvDone = 14;     // [2] a pair's P V of block X completed (P block X free)
+  static constexpr int kBarXch = 16;        // [2] row values exchanged, by parity
+  static constexpr int kBarOFull = 18;
+  static constexpr int kBarOEmpty = 19;
+  static constexpr int kBarItemFull = 20;   // [2]
+  static constexpr int kBarItemEmpty = 22;  // [2]
+  static constexpr int kBarClc = 24;
+  static constexpr int kBarMmaDone = 25;
+  static constexpr int kBarBmEmpty = 26;    // [2] block-sparse: an item's bitmap walked by every role
+  static constexpr int kNumBars = 26 + (SPARSE ? 2 : 0);
   // cancel answer (16) | TMEM base | abort flag | next item [2]
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;
   static constexpr int kClcOff = kMiscOff;
@@ -290,8 +292,10 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(bar(C::kBarSFull), 1);
     mbar_init(bar(C::kBarSFree), 2 * 4 * 32);
-    mbar_init(bar(C::kBarPFull), 2 * 4 * 32);
-    mbar_init(bar(C::kBarPvDone), 1);
+    mbar_init(bar(C::kBarPFull + 0), 2 * 4 * 32);
+    mbar_init(bar(C::kBarPFull + 1), 4 * 32);
+    mbar_init(bar(C::kBarPvDone + 0), 1);
+    mbar_init(bar(C::kBarPvDone + 1), 1);
     mbar_init(bar(C::kBarOFull), 1);
     mbar_init(bar(C::kBarOEmpty), 2 * 4 * 32);
     mbar_init(bar(C::kBarClc), 1);
@@ -491,30 +495,33 @@ __global__ void __launch_bounds__(384, 1)
           ++sn;
           return true;
         };
+        // P V block by block: block X's MMAs go as soon as warpgroup X has
+        // written its P, and their completion frees that block's P columns
         auto issue_pv = [&](bool first, bool alone) -> bool {
-          if (!wait_bar(bar(C::kBarPFull), pn & 1, abort_flag, p.err)) return false;
-          ++pn;
-          tc_fence_after();
-          if (first && on > 0) {
-            // O still holds the previous item's result until its epilogue read it
-            if (!wait_bar(bar(C::kBarOEmpty), (on - 1) & 1, abort_flag, p.err)) return false;
-            tc_fence_after();
-          }
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (SPARSE && alone && t == 1) break;
-            const int s = iv % C::kStagesV;
-            if (!wait_bar(bar(C::kBarVFull + s), (iv / C::kStagesV) & 1, abort_flag, p.err)) return false;
+            if (!wait_bar(bar(C::kBarPFull + t), pn & 1, abort_flag, p.err)) return false;
             tc_fence_after();
-            const uint64_t dv = sdesc_sw128(sbase + C::kVOff + s * C::kTileBytes, C::kChunkBytes, 1024);
+            if (t == 0 && first && on > 0) {
+              // O still holds the previous item's result until its epilogue read it
+              if (!wait_bar(bar(C::kBarOEmpty), (on - 1) & 1, abort_flag, p.err)) return false;
+              tc_fence_after();
+            }
+            if (!(SPARSE && alone && t == 1)) {
+              const int s = iv % C::kStagesV;
+              if (!wait_bar(bar(C::kBarVFull + s), (iv / C::kStagesV) & 1, abort_flag, p.err)) return false;
+              tc_fence_after();
+              const uint64_t dv = sdesc_sw128(sbase + C::kVOff + s * C::kTileBytes, C::kChunkBytes, 1024);
 #pragma unroll
-            for (int kk = 0; kk < kTileN / 16; ++kk)
-              mma_ts(tmem + C::kColO, tmem + C::kColP + (t * 8 + kk) * 8, sdesc_add(dv, kk * 16 * 128),
-                     kIdescPV, (!first || t > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(bar(C::kBarVEmpty + s));
-            ++iv;
+              for (int kk = 0; kk < kTileN / 16; ++kk)
+                mma_ts(tmem + C::kColO, tmem + C::kColP + (t * 8 + kk) * 8, sdesc_add(dv, kk * 16 * 128),
+                       kIdescPV, (!first || t > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(bar(C::kBarVEmpty + s));
+              ++iv;
+            }
+            mma_commit(bar(C::kBarPvDone + t));
           }
-          mma_commit(bar(C::kBarPvDone));
+          ++pn;
           return true;
         };
         while (ok) {
@@ -730,10 +737,41 @@ __global__ void __launch_bounds__(384, 1)
           moved = true;
         }
         const float mu = (m2 == NEG_INF) ? 0.f : m2;
-        // P and O are written below: the previous pair's P V (which reads P
-        // and accumulates into O) must have completed
+        // Where the reference max moved, this warpgroup's half of O is
+        // rescaled: after the previous pair's whole P V (both blocks write
+        // all of O).  Warpgroup 1 does it first and then releases block 0's
+        // P V; warpgroup 0 after writing its P, before releasing it.
+        const bool fix = moved && k > 0;
+        const bool any_fix = __any_sync(0xFFFFFFFFu, fix);
+        auto rescale_o = [&]() -> bool {
+          if (!__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarPvDone + 1), (cnt - 1) & 1, abort_flag, p.err)))
+            return false;
+          tc_fence_after();
+          const float a = fix ? alpha : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * a);
+            tmem_st32(tO + c * 32, o);
+          }
+          return true;
+        };
+        if (X == 1) {
+          if (any_fix && !rescale_o()) {
+            ok = false;
+            break;
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(bar(C::kBarPFull + 0));
+        }
+        // P block X is written below: the previous pair's P V of block X
+        // (which reads it) must have completed
         if (cnt > 0 &&
-            !__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarPvDone), (cnt - 1) & 1, abort_flag, p.err))) {
+            !__all_sync(0xFFFFFFFFu, wait_bar(bar(C::kBarPvDone + X), (cnt - 1) & 1, abort_flag, p.err))) {
           ok = false;
           break;
         }
@@ -762,23 +800,13 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st32(tP + half * 32, pk);
         }
         l = l * alpha + (((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7])));
-        // rescale this warpgroup's half of O when the reference max moved
-        const bool fix = moved && k > 0;
-        if (__any_sync(0xFFFFFFFFu, fix)) {
-          const float a = fix ? alpha : 1.f;
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait(o);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * a);
-            tmem_st32(tO + c * 32, o);
-          }
+        if (X == 0 && any_fix && !rescale_o()) {
+          ok = false;
+          break;
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(bar(C::kBarPFull));
+        mbar_arrive(bar(C::kBarPFull + X));
         ++cnt;
       }
       if (!ok) break;

@@ -102,7 +102,7 @@ def load_peaks():
 KERNEL_OF_ROW = {
     "fwd": "attn_fwd_wide_kernel (causal, persistent, 256-key score tiles): the whole attn_fwd call",
     "splitkv": "attn_fwd_kernel (partial, 8 key chunks in one launch) + merge_states_kernel",
-    "sparse": "attn_fwd_kernel (block-sparse)",
+    "sparse": "attn_fwd_wide_kernel (block-sparse, 256-key score tiles)",
     "bwd": "attn_bwd call: attn_bwd_preprocess_kernel + attn_bwd_main_kernel + "
            "attn_bwd_dq_convert_kernel (timed together)",
 }

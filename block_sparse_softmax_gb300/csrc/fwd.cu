@@ -1159,20 +1159,14 @@ cudaError_t launch_fwd(int d, bool causal, bool sparse, bool partial, const CUte
   // many) run faster: 8 chunks of 512 keys at B=4 H=16 L=4096 took 0.576 ms
   // there against 0.507 ms here, chunks of 2048 keys ran alike, and chunks of
   // 16384 keys 8 % faster there.
-  // Block-sparse launches at d = 128 run it where the lists hold at least 8
-  // entries per query block on average (duplicates counted: the host sees
-  // only nnz), up to the key range its bitmaps cover.  Its items are one
-  // query tile each, so short lists leave it waiting on every item's Q and
-  // first K/V tiles: at B=2 H=16 L'=16320 (causal) lists of 6.5 entries a row
-  // ran 2 % slower there, and lists of 12.6, 23.8 and 44.6 entries 9 %, 17 %
-  // and 17 % faster.
+  // Block-sparse launches at d = 128 run it too, up to the key range its
+  // bitmaps cover: at B=2 H=16 L'=16320 (causal) it ran lists of 6.5, 12.6,
+  // 23.8 and 44.6 entries a row 4 %, 12 %, 17 % and 16 % faster than this
+  // kernel.
   if (d == 128 && !sparse && (!partial || p.chunk_len >= 4096))
     return launch_fwd_wide(causal, partial, false, tq, tk, tv, p, st);
-  if (d == 128 && sparse && !partial && fwd_wide_takes_sparse(p.Lk) && p.heads_per_list > 0) {
-    const long long n_lists = static_cast<long long>(p.B) * p.H / p.heads_per_list;
-    if (static_cast<long long>(p.nnz) >= 8ll * n_lists * p.n_qblk)
-      return launch_fwd_wide(causal, false, true, tq, tk, tv, p, st);
-  }
+  if (d == 128 && sparse && !partial && fwd_wide_takes_sparse(p.Lk))
+    return launch_fwd_wide(causal, false, true, tq, tk, tv, p, st);
   const bool single_tile_pair = (p.Lq % (2 * kTileM)) != 0 && (p.Lq % (2 * kTileM)) <= kTileM;
   const bool alt = !sparse && (single_tile_pair || (!partial && d == 64));
   const bool dec = alt && p.Lq >= 1 && p.Lq <= kTileM;

@@ -174,13 +174,10 @@ attn_status_t attn_blocklist_normalize(const int32_t* row_ptr, const int32_t* co
  *   attn_poll_status; so is a row whose row_ptr range is not inside [0, nnz]
  *   (that row is then treated as empty).  A query block with an empty list
  *   gets O = 0, LSE = -inf.  L <= 4096*128 (at most 4096 key blocks).
- *   Kernel choice (speed only): at d = 128, with at most 2048 key blocks and
- *   nnz >= 8 * n_lists * n_qblk (lists of 8 or more raw entries per query
- *   block on average), the launch runs the kernel with 256-key score tiles;
- *   otherwise the two-tile kernel.  Lists of one set give bit-identical
- *   results whenever they run the same kernel (any order; duplicates that
- *   keep nnz on the same side of that bound), and results within rounding
- *   of each other otherwise.
+ *   Lists of one set (any order, any duplicates) give bit-identical results.
+ *   At d = 128 with at most 2048 key blocks the launch runs the kernel with
+ *   256-key score tiles, otherwise the two-tile kernel (speed only: both
+ *   agree with the dense forward within rounding).
  */
 attn_status_t attn_fwd_blocksparse(const void* q, const void* k, const void* v, void* o,
                                    float* lse, int B, int H, int H_kv, int L, int d, float scale,

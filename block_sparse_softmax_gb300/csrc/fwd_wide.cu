@@ -24,7 +24,11 @@
 //     block X of every pair (S columns 128X ..), and the two exchange their
 //     rows' block maxima through shared memory (mbarriers with bounded
 //     waits) so that both use one reference max.  Each keeps its own row sum,
-//     writes its half of P, and rescales and stores its half of O's columns;
+//     writes its half of P, and rescales and stores its half of O's columns.
+//     P V runs block by block: block X's 8 MMAs wait for warpgroup X's P
+//     only, and their completion frees only block X's P columns, so
+//     warpgroup 0 writes the next P while block 1's MMAs still run (an O
+//     rescale still waits for both);
 //   * shared memory: Q (32 KB) | two stages of key-block pairs (64 KB each;
 //     the two blocks' 64-column chunks interleaved, so that one descriptor of
 //     256 rows covers the pair) | two V tile stages (32 KB each).  The

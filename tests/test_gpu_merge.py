@@ -204,3 +204,58 @@ def test_long_context_per_chunk_launches_full_size(bss):
     for n_, (b, h) in enumerate(heads):
         compare_forward(o[b, h, rows], lse[b, h, rows], O_ref[n_], l_ref[n_], f"head {(b, h)}")
     assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_chunk_partial_state_matches_oracle(bss, causal):
+    """One chunk of 4296 keys (34 blocks, the last one 72 keys) at d=128: the
+    kernel with 256-key score tiles takes chunks of 4096 keys or more.  The
+    state against the oracle, dense and causal (the chunk starts at key 700,
+    so the first 700 query rows see none of it under the causal mask)."""
+    L, s, e = 5000, 700, 4996
+    w = Workload("pl", 1, 2, L, 128, causal, seed=71)
+    cpu = make_inputs(w)
+    q = cpu["q"][:, :, :300 + 128 * 9].contiguous()
+    Lq = q.shape[2]
+    kc = cpu["k"][:, :, s:e].contiguous().cuda()
+    vc = cpu["v"][:, :, s:e].contiguous().cuda()
+    m, l, acc = bss.attn_fwd_partial(q.cuda(), kc, vc, causal=causal, scale=w.scale, k_offset=s)
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    qn, kn, vn = (to_f64(t) for t in (q, cpu["k"], cpu["v"]))
+    for h in range(2):
+        M = oracle.allowed_rows(np.arange(Lq), e - s, causal=causal, k_offset=s)
+        mr, lr, Ar = oracle.partial_state(qn[0, h], kn[0, h, s:e], vn[0, h, s:e], w.scale, M)
+        mg = m[0, h].double().cpu().numpy()
+        lg = l[0, h].double().cpu().numpy()
+        Ag = acc[0, h].double().cpu().numpy()
+        empty = np.isneginf(mr)
+        assert np.array_equal(np.isneginf(mg), empty)
+        assert causal == bool(empty.any())
+        assert np.all(lg[empty] == 0)
+        f = ~empty
+        assert np.abs(mg[f] - mr[f]).max() <= TOL_LSE
+        assert np.abs((Ag[f] / lg[f, None]) - (Ar[f] / lr[f, None])).max() <= TOL_O
+        assert np.abs((mg[f] + np.log(lg[f])) - (mr[f] + np.log(lr[f]))).max() <= TOL_LSE
+        assert lg[f].min() >= 1.0 - 1e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_split_kv_long_chunks_match_oracle(bss, causal):
+    """L=9000 in 2 chunks (4608 keys, then 4392 with a partial last block) at
+    d=128, B=1 H=3: both chunks run the kernel with 256-key score tiles.  The
+    merged O and LSE against the oracle on every tile edge and random rows,
+    and against the unsplit forward."""
+    L = 9000
+    w = Workload("sl", 1, 3, L, 128, causal, seed=73)
+    cpu = make_inputs(w)
+    inp = to_cuda(cpu)
+    o, lse = bss.attn_fwd_splitkv(inp["q"], inp["k"], inp["v"], 2, causal=causal, scale=w.scale)
+    o1, l1 = bss.attn_fwd(inp["q"], inp["k"], inp["v"], causal=causal, scale=w.scale)
+    torch.cuda.synchronize()
+    assert bss.attn_poll_status() == 0
+    rows = tile_edge_rows(L, n_random=32, seed=5)[::3]
+    O_ref, l_ref = oracle_forward(cpu, w.scale, rows=rows, causal=causal)
+    compare_forward(o[:, :, rows], lse[:, :, rows], O_ref, l_ref, f"2 long chunks causal={causal}")
+    assert (o.float() - o1.float()).abs().max().item() <= TOL_O
+    assert (lse - l1).abs().max().item() <= TOL_LSE
